@@ -1,0 +1,210 @@
+"""Python binding of libgemm.so, the GB300 dense GEMM library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI (include/gemm.h).  Loading fails loudly when the
+compiled library is missing -- there is no Python or CPU fallback.
+
+Operands may be given as torch tensors (device memory for the device forms,
+host memory for the ``*_host`` forms) or as raw integer addresses.  Leading
+dimensions default to the natural row-major ones (lda=K, ldb=N, ldc=N).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "GemmError", "lib", "library_path", "gemm_f16", "sgemm_f32", "gemm_f16_host",
+    "sgemm_f32_host", "l2_flush", "force_path", "force_splits", "set_wait_limit_ns",
+    "debug_status", "last_path", "release", "EXPORTS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgemm.so")
+_lock = threading.Lock()
+_lib = None
+
+# Every symbol include/gemm.h declares.
+EXPORTS = (
+    "gemm_f16", "gemm_f16_ld", "sgemm_f32", "sgemm_f32_ld", "gemm_f16_host", "sgemm_f32_host",
+    "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
+    "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
+)
+
+PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = lib().gemm_strerror(code).decode() if _lib is not None else str(code)
+        super().__init__("%s failed: %s (%d)" % (where, msg, code))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded library (ctypes.CDLL).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError("libgemm.so is not built (run __graft_entry__.build() or "
+                                  "python dense_gemm_03_gb300/build.py)")
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            for name in ("gemm_f16", "sgemm_f32"):
+                fn = getattr(L, name)
+                fn.restype = i
+                fn.argtypes = [vp, vp, vp, i, i, i, f, f, vp]
+            for name in ("gemm_f16_ld", "sgemm_f32_ld", "gemm_f16_host", "sgemm_f32_host"):
+                fn = getattr(L, name)
+                fn.restype = i
+                fn.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, vp]
+            L.gemm_l2_flush.restype = i
+            L.gemm_l2_flush.argtypes = [ctypes.c_size_t, vp]
+            L.gemm_force_path.restype = i
+            L.gemm_force_path.argtypes = [i]
+            L.gemm_force_splits.restype = i
+            L.gemm_force_splits.argtypes = [i]
+            L.gemm_set_wait_limit_ns.restype = ctypes.c_longlong
+            L.gemm_set_wait_limit_ns.argtypes = [ctypes.c_longlong]
+            L.gemm_debug_status.restype = i
+            L.gemm_debug_status.argtypes = []
+            L.gemm_last_path.restype = ctypes.c_char_p
+            L.gemm_last_path.argtypes = []
+            L.gemm_strerror.restype = ctypes.c_char_p
+            L.gemm_strerror.argtypes = [i]
+            L.gemm_release.restype = i
+            L.gemm_release.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _addr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):                      # numpy array
+        return x.ctypes.data
+    raise TypeError("expected a tensor, an array or an address, got %r" % type(x))
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dims(A, B, M, N, K):
+    if M is None:
+        M = A.shape[0]
+    if K is None:
+        K = A.shape[1]
+    if N is None:
+        N = B.shape[1]
+    return int(M), int(N), int(K)
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise GemmError(rc, where)
+
+
+def gemm_f16(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None, ldc=None,
+             stream=None):
+    """C := alpha*A*B + beta*C on device fp16 operands (fp32 accumulation)."""
+    M, N, K = _dims(A, B, M, N, K)
+    L = lib()
+    s = _stream(stream)
+    if lda is None and ldb is None and ldc is None:
+        rc = L.gemm_f16(_addr(A), _addr(B), _addr(C), M, N, K, float(alpha), float(beta), s)
+    else:
+        rc = L.gemm_f16_ld(_addr(A), _addr(B), _addr(C), M, N, K,
+                           int(K if lda is None else lda), int(N if ldb is None else ldb),
+                           int(N if ldc is None else ldc), float(alpha), float(beta), s)
+    _check(rc, "gemm_f16")
+
+
+def sgemm_f32(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None, ldc=None,
+              stream=None):
+    """C := alpha*A*B + beta*C on device fp32 operands."""
+    M, N, K = _dims(A, B, M, N, K)
+    L = lib()
+    s = _stream(stream)
+    if lda is None and ldb is None and ldc is None:
+        rc = L.sgemm_f32(_addr(A), _addr(B), _addr(C), M, N, K, float(alpha), float(beta), s)
+    else:
+        rc = L.sgemm_f32_ld(_addr(A), _addr(B), _addr(C), M, N, K,
+                            int(K if lda is None else lda), int(N if ldb is None else ldb),
+                            int(N if ldc is None else ldc), float(alpha), float(beta), s)
+    _check(rc, "sgemm_f32")
+
+
+def gemm_f16_host(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None,
+                  ldc=None, stream=None):
+    """Host-buffer form: copies in, computes, copies C back, synchronises."""
+    M, N, K = _dims(A, B, M, N, K)
+    rc = lib().gemm_f16_host(_addr(A), _addr(B), _addr(C), M, N, K,
+                             int(K if lda is None else lda), int(N if ldb is None else ldb),
+                             int(N if ldc is None else ldc), float(alpha), float(beta),
+                             _stream(stream))
+    _check(rc, "gemm_f16_host")
+
+
+def sgemm_f32_host(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None,
+                   ldc=None, stream=None):
+    M, N, K = _dims(A, B, M, N, K)
+    rc = lib().sgemm_f32_host(_addr(A), _addr(B), _addr(C), M, N, K,
+                              int(K if lda is None else lda), int(N if ldb is None else ldb),
+                              int(N if ldc is None else ldc), float(alpha), float(beta),
+                              _stream(stream))
+    _check(rc, "sgemm_f32_host")
+
+
+def l2_flush(nbytes: int = 0, stream=None):
+    _check(lib().gemm_l2_flush(int(nbytes), _stream(stream)), "gemm_l2_flush")
+
+
+def force_path(path: int) -> int:
+    prev = lib().gemm_force_path(int(path))
+    if prev < 0:
+        raise GemmError(prev, "gemm_force_path")
+    return prev
+
+
+def force_splits(splits: int) -> int:
+    prev = lib().gemm_force_splits(int(splits))
+    if prev < 0:
+        raise GemmError(prev, "gemm_force_splits")
+    return prev
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(lib().gemm_set_wait_limit_ns(int(ns)))
+
+
+def debug_status() -> int:
+    return int(lib().gemm_debug_status())
+
+
+def last_path() -> str:
+    return lib().gemm_last_path().decode()
+
+
+def release():
+    _check(lib().gemm_release(), "gemm_release")

@@ -1,0 +1,468 @@
+// api.cu -- the C ABI of libgemm.so (declared in include/gemm.h): argument
+// checks, path choice, tensor-map construction, workspace management and
+// kernel launches on the caller's stream.
+//
+// Path choice for the half-precision GEMM (gemm_f16_ld):
+//   1. M == 0 or N == 0                 -> nothing to do
+//   2. alpha == 0 or K == 0             -> scale-only kernel, C := beta*C
+//   3. tile width BN from N (64 / 128 / 256)
+//   4. operand loads: TMA when A and B start on 16-byte boundaries and
+//      lda*2, ldb*2 are multiples of 16 bytes, else predicated element loads
+//      (the run-time alignment check of the "advanced SGEMM" page, kernel
+//      selection section, extended to the 16-byte rule of TMA)
+//   5. epilogue: TMA for C under the same rule, else predicated accesses
+//   6. split-K over an fp32 workspace when the output tiles alone cannot
+//      fill the SMs and K is long enough to share out
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+__device__ DeviceStatus g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+struct DevState {
+  bool init = false;
+  int err = 0;
+  int sm_count = 0;
+  int l2_bytes = 0;
+  DeviceStatus* status = nullptr;
+  void* ws = nullptr;           // split-K workspace
+  size_t ws_bytes = 0;
+  void* flush = nullptr;        // L2 flush buffer
+  size_t flush_bytes = 0;
+  void* host_buf[3] = {nullptr, nullptr, nullptr};  // staging for the host-buffer forms
+  size_t host_bytes[3] = {0, 0, 0};
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+std::atomic<int> g_force_path{0};
+std::atomic<int> g_force_splits{0};
+std::atomic<long long> g_wait_limit_ns{2000000000ll};
+thread_local const char* t_last_path = "none";
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int encode_fn(EncodeTiledFn* out) {
+  if (g_encode) {
+    *out = g_encode;
+    return GEMM_OK;
+  }
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return GEMM_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  *out = g_encode;
+  return GEMM_OK;
+}
+
+// Per-device set-up: capability check, SM count, L2 size, status word.
+int device_state(DevState** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      d.err = GEMM_ERR_DEVICE;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return GEMM_ERR_CUDA;
+      d.status = static_cast<DeviceStatus*>(p);
+    }
+    d.init = true;
+  }
+  if (d.err) return d.err;
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return GEMM_OK;
+}
+
+// Grows a library-owned device buffer (synchronising the device before a
+// buffer that may be in use is replaced).
+int ensure_buffer(void** buf, size_t* have, size_t need) {
+  if (*have >= need && *buf) return GEMM_OK;
+  if (*buf) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+    cudaFree(*buf);
+    *buf = nullptr;
+    *have = 0;
+  }
+  size_t sz = std::max(need, static_cast<size_t>(1) << 20);
+  if (cudaMalloc(buf, sz) != cudaSuccess) {
+    *buf = nullptr;
+    return GEMM_ERR_CUDA;
+  }
+  *have = sz;
+  return GEMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
+                 int box_cols, int box_rows) {
+  EncodeTiledFn enc = nullptr;
+  if (int rc = encode_fn(&enc)) return rc;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int scale_grid(const DevState& d, long long elems) {
+  const long long blocks = (elems + 255) / 256;
+  return static_cast<int>(std::max(1ll, std::min<long long>(blocks, 8ll * d.sm_count)));
+}
+
+const char* kPathNames[3][3][3] = {
+    // [bn index][load][epi]
+    {{"f16.tc.bn64.tma.epi_tma", "f16.tc.bn64.tma.epi_manual", "f16.tc.bn64.tma.splitk"},
+     {"f16.tc.bn64.manual.epi_tma", "f16.tc.bn64.manual.epi_manual", "f16.tc.bn64.manual.splitk"}},
+    {{"f16.tc.bn128.tma.epi_tma", "f16.tc.bn128.tma.epi_manual", "f16.tc.bn128.tma.splitk"},
+     {"f16.tc.bn128.manual.epi_tma", "f16.tc.bn128.manual.epi_manual",
+      "f16.tc.bn128.manual.splitk"}},
+    {{"f16.tc.bn256.tma.epi_tma", "f16.tc.bn256.tma.epi_manual", "f16.tc.bn256.tma.splitk"},
+     {"f16.tc.bn256.manual.epi_tma", "f16.tc.bn256.manual.epi_manual",
+      "f16.tc.bn256.manual.splitk"}},
+};
+
+int check_common(const void* A, const void* B, const void* C, int M, int N, int K, long long lda,
+                 long long ldb, long long ldc, float alpha) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_DIM;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (ldc < N || (K > 0 && (lda < K || ldb < N))) return GEMM_ERR_LD;
+  if (C == nullptr) return GEMM_ERR_NULL;
+  if (K > 0 && alpha != 0.0f && (A == nullptr || B == nullptr)) return GEMM_ERR_NULL;
+  return GEMM_OK;
+}
+
+int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                    long long lda, long long ldb, long long ldc, float alpha, float beta,
+                    cudaStream_t stream) {
+  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha)) return rc;
+  if (M == 0 || N == 0) {
+    t_last_path = "noop";
+    return GEMM_OK;
+  }
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+
+  if (alpha == 0.0f || K == 0) {
+    t_last_path = "f16.scale";
+    return launch_scale_f16(C, ldc, M, N, beta, scale_grid(*d, 1ll * M * N), stream) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+  }
+
+  const int force = g_force_path.load();
+  const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+  const bool ab_tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
+  const bool c_tma = aligned16(C) && (ldc * 2) % 16 == 0;
+  int load = (ab_tma && force != 2) ? kLoadTma : kLoadManual;
+  int epi = (c_tma && force != 2) ? kEpiTma : kEpiManual;
+
+  TcArgs a{};
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.lda = lda;
+  a.ldb = ldb;
+  a.ldc = ldc;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.tiles_m = (M + kBM - 1) / kBM;
+  a.tiles_n = (N + bn - 1) / bn;
+  a.kb_total = (K + kBK - 1) / kBK;
+  a.group_m = 8;
+  a.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+  a.status = d->status;
+
+  // Split-K when the tiles alone leave most SMs idle.
+  const long long tiles = 1ll * a.tiles_m * a.tiles_n;
+  int splits = 1;
+  const int fs = g_force_splits.load();
+  if (force == 3 || (force == 0 && tiles * 2 <= d->sm_count && a.kb_total >= 8)) {
+    splits = fs > 0 ? fs
+                    : static_cast<int>(std::min<long long>(
+                          {(d->sm_count + tiles - 1) / tiles, static_cast<long long>(a.kb_total / 4),
+                           16ll}));
+    splits = std::max(1, std::min(splits, a.kb_total));
+  }
+  if (splits > 1) {
+    a.kb_per_split = (a.kb_total + splits - 1) / splits;
+    splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;  // no empty slice
+  } else {
+    a.kb_per_split = a.kb_total;
+  }
+  a.splits = splits;
+  if (tiles * splits > 0x7fffffffll) return GEMM_ERR_ARG;
+  a.num_units = static_cast<int>(tiles * splits);
+
+  if (splits > 1) {
+    epi = kEpiPartial;
+    a.ws_ld = (N + 3) / 4 * 4;
+    const size_t need = sizeof(float) * static_cast<size_t>(splits) * M * a.ws_ld;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (int rc = ensure_buffer(&d->ws, &d->ws_bytes, need)) return rc;
+      a.ws = static_cast<float*>(d->ws);
+    }
+  }
+
+  CUtensorMap tmA{}, tmB{}, tmC{};
+  if (load == kLoadTma) {
+    if (int rc = make_map_f16(&tmA, A, M, K, lda, 64, kBM)) return rc;
+    if (int rc = make_map_f16(&tmB, B, K, N, ldb, 64, 64)) return rc;
+  }
+  if (epi == kEpiTma) {
+    if (int rc = make_map_f16(&tmC, C, M, N, ldc, 64, 32)) return rc;
+  }
+  const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
+  const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
+  t_last_path = kPathNames[bi][load][epi];
+  if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (splits > 1) {
+    const long long groups = 1ll * M * ((N + 3) / 4);
+    if (launch_splitk_reduce_f16(a.ws, a.ws_ld, splits, C, ldc, M, N, alpha, beta,
+                                 scale_grid(*d, groups), stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  return GEMM_OK;
+}
+
+int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int K, long long lda,
+                     long long ldb, long long ldc, float alpha, float beta, cudaStream_t stream) {
+  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha)) return rc;
+  if (M == 0 || N == 0) {
+    t_last_path = "noop";
+    return GEMM_OK;
+  }
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  if (alpha == 0.0f || K == 0) {
+    t_last_path = "f32.scale";
+    return launch_scale_f32(C, ldc, M, N, beta, scale_grid(*d, 1ll * M * N), stream) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+  }
+  const bool vec = g_force_path.load() != 4 && aligned16(A) && aligned16(B) && aligned16(C) &&
+                   lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0;
+  SgemmArgs s{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta};
+  t_last_path = vec ? "f32.ffma.vec" : "f32.ffma.scalar";
+  return launch_sgemm_ffma(vec, s, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+size_t extent_bytes(int rows, int cols, long long ld, size_t elem) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return (static_cast<size_t>(rows - 1) * static_cast<size_t>(ld) + static_cast<size_t>(cols)) *
+         elem;
+}
+
+template <typename T, typename Fn>
+int host_form(const T* A, const T* B, T* C, int M, int N, int K, int lda, int ldb, int ldc,
+              float alpha, float beta, cudaStream_t stream, Fn device_fn) {
+  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha)) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  const bool read_ab = alpha != 0.0f && K > 0;
+  const size_t ba = read_ab ? extent_bytes(M, K, lda, sizeof(T)) : 0;
+  const size_t bb = read_ab ? extent_bytes(K, N, ldb, sizeof(T)) : 0;
+  const size_t bc = extent_bytes(M, N, ldc, sizeof(T));
+  T *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (read_ab) {
+      if (int rc = ensure_buffer(&d->host_buf[0], &d->host_bytes[0], ba)) return rc;
+      if (int rc = ensure_buffer(&d->host_buf[1], &d->host_bytes[1], bb)) return rc;
+      dA = static_cast<T*>(d->host_buf[0]);
+      dB = static_cast<T*>(d->host_buf[1]);
+    }
+    if (int rc = ensure_buffer(&d->host_buf[2], &d->host_bytes[2], bc)) return rc;
+    dC = static_cast<T*>(d->host_buf[2]);
+  }
+  if (read_ab) {
+    if (cudaMemcpyAsync(dA, A, ba, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dB, B, bb, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  // C is copied in whole when beta != 0, and also when ldc > N so that the
+  // padding between rows comes back unchanged.
+  if (beta != 0.0f || ldc > N) {
+    if (cudaMemcpyAsync(dC, C, bc, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  if (int rc = device_fn(dA, dB, dC, M, N, K, lda, ldb, ldc, alpha, beta, stream)) return rc;
+  if (cudaMemcpyAsync(C, dC, bc, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+int gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, float alpha,
+             float beta, cudaStream_t stream) {
+  return gemm_f16_device(A, B, C, M, N, K, K, N, N, alpha, beta, stream);
+}
+
+int gemm_f16_ld(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, int lda,
+                int ldb, int ldc, float alpha, float beta, cudaStream_t stream) {
+  return gemm_f16_device(A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, stream);
+}
+
+int sgemm_f32(const float* A, const float* B, float* C, int M, int N, int K, float alpha,
+              float beta, cudaStream_t stream) {
+  return sgemm_f32_device(A, B, C, M, N, K, K, N, N, alpha, beta, stream);
+}
+
+int sgemm_f32_ld(const float* A, const float* B, float* C, int M, int N, int K, int lda, int ldb,
+                 int ldc, float alpha, float beta, cudaStream_t stream) {
+  return sgemm_f32_device(A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, stream);
+}
+
+int gemm_f16_host(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, int lda,
+                  int ldb, int ldc, float alpha, float beta, cudaStream_t stream) {
+  return host_form<uint16_t>(A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, stream,
+                             [](const uint16_t* a, const uint16_t* b, uint16_t* c, int m, int n,
+                                int k, long long la, long long lb, long long lc, float al,
+                                float be, cudaStream_t s) {
+                               return gemm_f16_device(a, b, c, m, n, k, la, lb, lc, al, be, s);
+                             });
+}
+
+int sgemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int lda, int ldb,
+                   int ldc, float alpha, float beta, cudaStream_t stream) {
+  return host_form<float>(A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, stream,
+                          [](const float* a, const float* b, float* c, int m, int n, int k,
+                             long long la, long long lb, long long lc, float al, float be,
+                             cudaStream_t s) {
+                            return sgemm_f32_device(a, b, c, m, n, k, la, lb, lc, al, be, s);
+                          });
+}
+
+int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  const size_t n = bytes ? bytes : 2 * static_cast<size_t>(d->l2_bytes);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int rc = ensure_buffer(&d->flush, &d->flush_bytes, n)) return rc;
+  }
+  return cudaMemsetAsync(d->flush, 0, n, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int gemm_force_path(int path) {
+  if (path < 0 || path > 4) return GEMM_ERR_ARG;
+  return g_force_path.exchange(path);
+}
+
+int gemm_force_splits(int splits) {
+  if (splits < 0) return GEMM_ERR_ARG;
+  return g_force_splits.exchange(splits);
+}
+
+long long gemm_set_wait_limit_ns(long long ns) {
+  return g_wait_limit_ns.exchange(ns > 0 ? ns : 2000000000ll);
+}
+
+int gemm_debug_status(void) {
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+  DeviceStatus s{};
+  if (cudaMemcpy(&s, d->status, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  const DeviceStatus zero{};
+  if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  return s.code;
+}
+
+const char* gemm_last_path(void) { return t_last_path; }
+
+const char* gemm_strerror(int code) {
+  switch (code) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_NULL: return "null pointer";
+    case GEMM_ERR_DIM: return "negative dimension";
+    case GEMM_ERR_LD: return "leading dimension smaller than the row length";
+    case GEMM_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case GEMM_ERR_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_TIMEOUT: return "a kernel gave up waiting (time limit reached)";
+    case GEMM_ERR_ARG: return "invalid argument";
+    default: return "unknown error";
+  }
+}
+
+int gemm_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GEMM_ERR_CUDA;
+  int rc = GEMM_OK;
+  for (int dev = 0; dev < kMaxDevices; ++dev) {
+    DevState& d = g_dev[dev];
+    void** bufs[5] = {&d.ws, &d.flush, &d.host_buf[0], &d.host_buf[1], &d.host_buf[2]};
+    size_t* sizes[5] = {&d.ws_bytes, &d.flush_bytes, &d.host_bytes[0], &d.host_bytes[1],
+                        &d.host_bytes[2]};
+    bool any = false;
+    for (void** b : bufs) any = any || *b != nullptr;
+    if (!any) continue;
+    if (cudaSetDevice(dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      rc = GEMM_ERR_CUDA;
+      continue;
+    }
+    for (int i = 0; i < 5; ++i) {
+      if (*bufs[i]) cudaFree(*bufs[i]);
+      *bufs[i] = nullptr;
+      *sizes[i] = 0;
+    }
+  }
+  cudaSetDevice(prev);
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// internal.h -- declarations shared by the host dispatcher and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300 {
+
+struct DeviceStatus;
+
+// Operand-load modes of the tensor-core kernel.
+enum LoadMode : int { kLoadTma = 0, kLoadManual = 1 };
+// Epilogue modes: TMA load/store of C, predicated element access of C, or
+// raw fp32 partial sums to the split-K workspace.
+enum EpiMode : int { kEpiTma = 0, kEpiManual = 1, kEpiPartial = 2 };
+
+struct TcArgs {
+  const uint16_t* A;
+  const uint16_t* B;
+  uint16_t* C;
+  int M, N, K;
+  long long lda, ldb, ldc;
+  float alpha, beta;
+  int tiles_m, tiles_n;
+  int splits;         // number of K slices (1 = no split)
+  int kb_total;       // ceil(K / 64)
+  int kb_per_split;   // K blocks per slice (every slice non-empty)
+  int num_units;      // tiles_m * tiles_n * splits
+  int group_m;        // tile-order grouping along M (L2 reuse of B panels)
+  float* ws;          // split-K partials [splits][M][ws_ld]
+  long long ws_ld;
+  unsigned long long wait_limit_ns;
+  DeviceStatus* status;
+};
+
+// Tensor-core fp16 GEMM (tcgen05).  Maps are ignored by the modes that do not
+// use them.  Returns a cudaError_t from the launch.
+cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, const CUtensorMap& tmC, const TcArgs& args,
+                               int grid, cudaStream_t stream);
+int tc_smem_bytes(int bn, int epi_mode);
+int tc_threads(int load_mode);
+
+// Split-K reduction: C = half(alpha * sum_s ws[s] + beta * C).
+cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int splits, uint16_t* C,
+                                     long long ldc, int M, int N, float alpha, float beta,
+                                     int grid, cudaStream_t stream);
+
+// C := beta * C (C := 0 when beta == 0): the alpha == 0 / K == 0 case.
+cudaError_t launch_scale_f16(uint16_t* C, long long ldc, int M, int N, float beta, int grid,
+                             cudaStream_t stream);
+cudaError_t launch_scale_f32(float* C, long long ldc, int M, int N, float beta, int grid,
+                             cudaStream_t stream);
+
+// FFMA SGEMM.  vec = 16-byte vector loads allowed (aligned pointers, ld % 4 == 0).
+struct SgemmArgs {
+  const float* A;
+  const float* B;
+  float* C;
+  int M, N, K;
+  long long lda, ldb, ldc;
+  float alpha, beta;
+};
+cudaError_t launch_sgemm_ffma(bool vec, const SgemmArgs& args, cudaStream_t stream);
+
+}  // namespace gb300

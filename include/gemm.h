@@ -1,0 +1,155 @@
+/*
+ * gemm.h -- C ABI of the GB300 dense GEMM library (libgemm.so).
+ *
+ * Every entry point computes, or supports the computation of,
+ *
+ *     C := alpha * A * B + beta * C
+ *
+ * on row-major operands: A is M x K, B is K x N, C is M x N, and element
+ * (r, c) of an operand with leading dimension ld lives at ptr[r*ld + c]
+ * ("advanced SGEMM on NVIDIA GPUs" summary page: introduction for the
+ * formula, section on memory layout and PTX for row-major storage and the
+ * lda/ldb/ldc convention).  The half-precision entry points follow the
+ * LeetGPU statement on the "LeetGPU GEMM T4" page (baseline section): half
+ * operands, a float accumulator, and the result acc*alpha + C*beta rounded to
+ * half.
+ *
+ * Common rules
+ *   Pointers   A, B, C are DEVICE pointers owned by the caller; the library
+ *              never frees them.  A and B are read-only; C is read (unless
+ *              beta == 0) and written.  C must not overlap A or B (not
+ *              checked; the result is undefined).
+ *   Layout     row-major; the non-_ld forms mean lda = K, ldb = N, ldc = N.
+ *              Any alignment is accepted: pointers or leading dimensions that
+ *              are not 16-byte aligned are served by a slower path.
+ *   Types      half = IEEE binary16 (bits in a uint16_t); float = binary32.
+ *   Numerics   products accumulate in fp32; the epilogue alpha*acc + beta*c
+ *              is evaluated in fp32 and rounded once, to nearest even, to the
+ *              type of C.  Accumulation order is unspecified but fixed for a
+ *              given shape and device, so repeated calls are bitwise equal.
+ *   beta == 0  C is not read (it may hold NaN or Inf); C := alpha*A*B.
+ *   alpha == 0 or K == 0
+ *              A and B are not read; C := beta*C (C := 0 when beta == 0).
+ *   M == 0 or N == 0
+ *              nothing is done; returns GEMM_OK.
+ *   Streams    work is enqueued on `stream` (NULL = the legacy default
+ *              stream) and the call returns without synchronising.  Calls on
+ *              different streams that write the same C race.
+ *   Scratch    some shapes (small M*N with a long K) split K over several
+ *              thread blocks and need an fp32 workspace; the library owns it,
+ *              per device, grows it on first need (that call may allocate
+ *              device memory) and frees it in gemm_release().
+ *   Errors     a negative return code (below) and nothing enqueued, except
+ *              GEMM_ERR_CUDA, which reports a failed launch.  Kernels never
+ *              trap: a wait that runs past its time limit sets a device
+ *              status word that gemm_debug_status() reads.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define GEMM_OK               0
+#define GEMM_ERR_NULL        -1  /* a needed pointer is NULL                          */
+#define GEMM_ERR_DIM         -2  /* M, N or K is negative                             */
+#define GEMM_ERR_LD          -3  /* lda < K, ldb < N or ldc < N (for a non-empty op)   */
+#define GEMM_ERR_CUDA        -4  /* a CUDA runtime/driver call or a launch failed     */
+#define GEMM_ERR_DEVICE      -5  /* current device is not compute capability 10.3     */
+#define GEMM_ERR_TIMEOUT     -6  /* a kernel gave up waiting (gemm_debug_status)      */
+#define GEMM_ERR_ARG         -7  /* another invalid argument (see the function)       */
+
+/*
+ * Half-precision GEMM: fp16 A, B, C; fp32 accumulation; fp16 result.
+ * ("LeetGPU GEMM T4" page, baseline section: the solve(A, B, C, M, N, K,
+ * alpha, beta) statement, with a stream argument and a status return added.)
+ */
+int gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C,
+             int M, int N, int K, float alpha, float beta, cudaStream_t stream);
+
+/* As gemm_f16, with explicit leading dimensions in elements
+ * (lda >= K, ldb >= N, ldc >= N; "advanced SGEMM" page, memory-layout
+ * section). */
+int gemm_f16_ld(const uint16_t* A, const uint16_t* B, uint16_t* C,
+                int M, int N, int K, int lda, int ldb, int ldc,
+                float alpha, float beta, cudaStream_t stream);
+
+/* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 everywhere. */
+int sgemm_f32(const float* A, const float* B, float* C,
+              int M, int N, int K, float alpha, float beta, cudaStream_t stream);
+
+int sgemm_f32_ld(const float* A, const float* B, float* C,
+                 int M, int N, int K, int lda, int ldb, int ldc,
+                 float alpha, float beta, cudaStream_t stream);
+
+/*
+ * Host-buffer forms: A, B, C are HOST pointers (pinned memory gives the
+ * fastest copies; pageable memory works).  The call copies A, B (and C when
+ * beta != 0) to library-owned device buffers, runs the GEMM on `stream`,
+ * copies C back and synchronises the stream before returning.  The device
+ * buffers are kept for reuse and freed by gemm_release().
+ */
+int gemm_f16_host(const uint16_t* A, const uint16_t* B, uint16_t* C,
+                  int M, int N, int K, int lda, int ldb, int ldc,
+                  float alpha, float beta, cudaStream_t stream);
+
+int sgemm_f32_host(const float* A, const float* B, float* C,
+                   int M, int N, int K, int lda, int ldb, int ldc,
+                   float alpha, float beta, cudaStream_t stream);
+
+/*
+ * L2 flush used between timed replays ("advanced SGEMM" page, benchmark
+ * section: a cudaMemsetAsync of an L2-sized buffer before each replay).
+ * Enqueues a memset of a library-owned buffer of `bytes` bytes (0 = twice
+ * the device's L2 size) on `stream`.
+ */
+int gemm_l2_flush(size_t bytes, cudaStream_t stream);
+
+/*
+ * Kernel path selection, for tests and benchmarks.  0 = automatic (default);
+ * 1 = tensor-memory-accelerator operand loads; 2 = predicated element loads
+ * (the path taken when strides or pointers are not 16-byte aligned);
+ * 3 = split-K over an fp32 workspace; 4 = (fp32 only) FFMA kernel with
+ * predicated scalar loads.  A forced path that cannot serve a call (e.g. TMA
+ * loads on unaligned operands) falls back to the automatic choice.  Process
+ * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
+ */
+int gemm_force_path(int path);
+
+/* Fixes the split count of the split-K path (0 = automatic).  Returns the
+ * previous value. */
+int gemm_force_splits(int splits);
+
+/* Limit, in nanoseconds, of every wait inside the kernels (0 = default of
+ * two seconds).  Returns the previous value. */
+long long gemm_set_wait_limit_ns(long long ns);
+
+/*
+ * Synchronises the device and returns, then clears, the device status word:
+ * GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel abandoned a wait since the last
+ * call.
+ */
+int gemm_debug_status(void);
+
+/* Describes the path the last call on this thread took (static string). */
+const char* gemm_last_path(void);
+
+/* Text for a return code (static string). */
+const char* gemm_strerror(int code);
+
+/* Frees every library-owned device buffer on every device (workspace,
+ * host-form staging buffers, L2-flush buffer).  Synchronises each device
+ * that has such buffers. */
+int gemm_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

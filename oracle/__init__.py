@@ -171,7 +171,8 @@ def gemm(A, B, C0, alpha: float, beta: float, M: int = None, N: int = None, K: i
     return (out, absd) if with_absdot else out
 
 
-def gemm_cols(A, B, C0, alpha, beta, cols, M=None, N=None, K=None, lda=None, ldb=None, ldc=None):
+def gemm_cols(A, B, C0, alpha, beta, cols, M=None, N=None, K=None, lda=None, ldb=None, ldc=None,
+              with_absdot: bool = False):
     """Columns ``cols`` of the result (an M x len(cols) array), computed by the
     same definition on B and C0 restricted to those columns."""
     A_ = np.asarray(A)
@@ -189,7 +190,7 @@ def gemm_cols(A, B, C0, alpha, beta, cols, M=None, N=None, K=None, lda=None, ldb
         ldc = ldc if ldc is not None else (np.asarray(C0).shape[1] if np.asarray(C0).ndim == 2 else N)
         Csub = np.stack([Cm[i * ldc + cols] for i in range(M)])
     return gemm(A, Bsub, Csub, alpha, beta, M=M, N=cols.size, K=K, lda=lda,
-                ldb=cols.size, ldc=cols.size)
+                ldb=cols.size, ldc=cols.size, with_absdot=with_absdot)
 
 
 # ----------------------------------------------------------------------------

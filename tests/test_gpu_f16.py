@@ -1,0 +1,182 @@
+"""Parity of the half-precision path (gemm_f16 / gemm_f16_ld) with the CPU
+oracle, through the C ABI, on every kernel path: TMA loads, predicated loads
+(unaligned operands), split-K, and the scale-only case."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from helpers import check, operands, padding_untouched, run, to_dev, torch
+
+pytestmark = pytest.mark.gpu
+
+AUTO, MANUAL, SPLITK = 0, 2, 3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dense_gemm_03_gb300 import build
+    build.build()
+
+
+def _exact16(ref):
+    return ref.astype(np.float16)
+
+
+def test_identity_one_tile_is_exact():
+    M = K = 128
+    N = 256
+    A = np.eye(M, dtype=np.float16)
+    B = synthetic.uniform(1, 2, (K, N), dtype=np.float16)
+    C0 = np.full((M, N), np.nan, dtype=np.float16)
+    got, path = run("f16", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    assert "tma" in path
+    assert np.array_equal(got.view(np.uint16), B.view(np.uint16))
+
+
+@pytest.mark.parametrize("path", [AUTO, MANUAL])
+def test_permutation_is_exact(path):
+    M = K = 384
+    N = 320
+    rng = np.random.default_rng(5)
+    p = rng.permutation(K)
+    A = np.zeros((M, K), np.float16)
+    A[np.arange(M), p] = 1.0
+    B = synthetic.uniform(2, 2, (K, N), dtype=np.float16)
+    C0 = np.zeros((M, N), np.float16)
+    got, _ = run("f16", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=path)
+    assert np.array_equal(got.view(np.uint16), B[p].view(np.uint16))
+
+
+@pytest.mark.parametrize("path", [AUTO, MANUAL, SPLITK])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 128), (300, 700, 1000), (129, 65, 17), (1, 1, 1),
+                                   (8, 8, 8), (130, 1000, 640)])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (2.0, -1.0)])
+def test_small_integers_bit_exact(path, M, N, K, alpha, beta):
+    """Entries in {-1, 0, 1}: every partial sum is an integer below 2048, so
+    the fp32 accumulation and the fp16 output are exact whatever the order."""
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    A = rng.integers(-1, 2, size=(M, K)).astype(np.float16)
+    B = rng.integers(-1, 2, size=(K, N)).astype(np.float16)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float16)
+    got, _ = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, N, path=path,
+                 splits=3 if path == SPLITK else 0)
+    ref = oracle.gemm(A, B, C0, alpha, beta)
+    assert np.array_equal(got.view(np.uint16), _exact16(ref).view(np.uint16))
+
+
+@pytest.mark.parametrize("path", [AUTO, MANUAL, SPLITK])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (384, 640, 320), (129, 257, 65), (7, 9, 13),
+                                   (300, 500, 1000), (1024, 1024, 1024), (200, 64, 2000),
+                                   (64, 128, 4096)])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan"),
+                                               (0.75, -0.25, "uniform")])
+def test_random_parity(path, M, N, K, alpha, beta, c_fill):
+    A, B, C0 = operands(100 + M + N + K, M, N, K, K, N, N, np.float16, c_fill=c_fill)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, N, path=path,
+                     splits=4 if path == SPLITK else 0)
+    if path == MANUAL:
+        assert "manual" in taken
+    if path == SPLITK and (K + 63) // 64 >= 2:
+        assert "splitk" in taken
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
+    (257, 255, 77, 80, 255, 255),        # nothing 16-byte aligned: predicated path
+    (200, 300, 150, 153, 305, 301),      # padding everywhere
+    (130, 190, 100, 104, 192, 200),      # strides 16-byte aligned, ld > cols
+    (64, 70, 64, 64, 71, 77),
+])
+@pytest.mark.parametrize("alpha,beta", [(0.75, -0.25), (1.0, 0.0)])
+def test_leading_dimensions(M, N, K, lda, ldb, ldc, alpha, beta):
+    A, B, C0 = operands(7 + lda + ldb, M, N, K, lda, ldb, ldc, np.float16)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc)
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc)
+    assert padding_untouched(got, C0, N)
+
+
+def test_misaligned_base_pointers():
+    """Operands starting 2 bytes past a 16-byte boundary take the predicated path."""
+    t = torch()
+    M, N, K = 150, 200, 90
+    A, B, C0 = operands(31, M, N, K, K, N, N, np.float16)
+    import dense_gemm_03_gb300 as g
+    bufs = [t.zeros(x.size + 8, dtype=t.float16, device="cuda") for x in (A, B, C0)]
+    for buf, x in zip(bufs, (A, B, C0)):
+        buf[1:1 + x.size].copy_(t.from_numpy(x.reshape(-1)).cuda())
+    es = bufs[0].element_size()
+    g.gemm_f16(bufs[0].data_ptr() + es, bufs[1].data_ptr() + es, bufs[2].data_ptr() + es,
+               1.5, 0.5, M=M, N=N, K=K)
+    assert "manual" in g.last_path()
+    t.cuda.synchronize()
+    got = bufs[2][1:1 + C0.size].cpu().numpy().reshape(M, N)
+    check("f16", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+
+
+def test_alpha_zero_and_K_zero_scale_C():
+    M, N, K = 100, 130, 40
+    A, B, C0 = operands(9, M, N, K, K, N, N, np.float16)
+    A[:] = np.nan
+    got, path = run("f16", A, B, C0, 0.0, -0.25, M, N, K, K, N, N)
+    assert path == "f16.scale"
+    assert np.array_equal(got.view(np.uint16), (C0.astype(np.float64) * -0.25).astype(np.float16).view(np.uint16))
+    got, _ = run("f16", A[:, :0], B[:0], C0, 1.5, 0.5, M, N, 0, 1, N, N)
+    assert np.array_equal(got.view(np.uint16), (C0.astype(np.float64) * 0.5).astype(np.float16).view(np.uint16))
+    got, _ = run("f16", A, B, C0, 0.0, 0.0, M, N, K, K, N, N)
+    assert not got.any()
+
+
+def test_empty_is_noop():
+    t = torch()
+    import dense_gemm_03_gb300 as g
+    C = t.full((4, 4), 3.0, dtype=t.float16, device="cuda")
+    g.gemm_f16(C, C, C, 1.0, 1.0, M=0, N=4, K=4)
+    g.gemm_f16(C, C, C, 1.0, 1.0, M=4, N=0, K=4)
+    assert g.last_path() == "noop"
+    assert bool((C == 3.0).all())
+
+
+def test_deterministic():
+    M, N, K = 512, 768, 2048
+    A, B, C0 = operands(3, M, N, K, K, N, N, np.float16)
+    r1, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    r2, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    assert np.array_equal(r1.view(np.uint16), r2.view(np.uint16))
+    s1, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=SPLITK, splits=5)
+    s2, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=SPLITK, splits=5)
+    assert np.array_equal(s1.view(np.uint16), s2.view(np.uint16))
+
+
+def test_host_form_matches_device_form():
+    import dense_gemm_03_gb300 as g
+    t = torch()
+    M, N, K = 333, 444, 555
+    A, B, C0 = operands(21, M, N, K, K, N, N, np.float16)
+    dev, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    hA = t.from_numpy(A).pin_memory()
+    hB = t.from_numpy(B).pin_memory()
+    hC = t.from_numpy(C0.copy()).pin_memory()
+    g.gemm_f16_host(hA, hB, hC, 1.5, 0.5, M=M, N=N, K=K)
+    assert np.array_equal(hC.numpy().view(np.uint16), dev.view(np.uint16))
+
+
+def test_streams_are_respected():
+    """Work goes on the caller's stream: a GEMM enqueued on a side stream after
+    an event sees the inputs the main stream wrote before it."""
+    import dense_gemm_03_gb300 as g
+    t = torch()
+    M, N, K = 256, 256, 512
+    A, B, C0 = operands(4, M, N, K, K, N, N, np.float16)
+    dA, dB = to_dev(A), to_dev(B)
+    dC = t.zeros((M, N), dtype=t.float16, device="cuda")
+    s = t.cuda.Stream()
+    dA2 = t.empty_like(dA)
+    dA2.copy_(dA)
+    ev = t.cuda.Event()
+    ev.record()
+    s.wait_event(ev)
+    with t.cuda.stream(s):
+        g.gemm_f16(dA2, dB, dC, 1.0, 0.0, M=M, N=N, K=K, stream=s)
+    s.synchronize()
+    check("f16", dC.cpu().numpy(), A, B, np.zeros((M, N), np.float16), 1.0, 0.0, M, N, K, K, N, N)
