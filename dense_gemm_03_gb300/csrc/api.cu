@@ -10,7 +10,8 @@
 //      lda*2, ldb*2 are multiples of 16 bytes, else predicated element loads
 //      (the run-time alignment check of the "advanced SGEMM" page, kernel
 //      selection section, extended to the 16-byte rule of TMA)
-//   5. epilogue: TMA for C under the same rule, else predicated accesses
+//   5. epilogue: TMA for C under the same rule when N is a multiple of 8,
+//      else predicated accesses
 //   6. split-K over an fp32 workspace when the output tiles alone cannot
 //      fill the SMs and K is long enough to share out
 #include <cuda.h>
@@ -192,7 +193,11 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   const int force = g_force_path.load();
   const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
   const bool ab_tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
-  const bool c_tma = aligned16(C) && (ldc * 2) % 16 == 0;
+  // A TMA store writes whole 16-byte pieces of a row: when N is not a multiple
+  // of 8 halves it would also write the elements just past column N (measured
+  // on GB300), which may belong to the caller.  Such shapes take the predicated
+  // epilogue.
+  const bool c_tma = aligned16(C) && (ldc * 2) % 16 == 0 && N % 8 == 0;
   int load = (ab_tma && force != 2) ? kLoadTma : kLoadManual;
   int epi = (c_tma && force != 2) ? kEpiTma : kEpiManual;
 
