@@ -16,7 +16,7 @@ import threading
 
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16", "sgemm_f32", "gemm_f16_host",
-    "sgemm_f32_host", "l2_flush", "force_path", "force_splits", "set_wait_limit_ns",
+    "sgemm_f32_host", "gemm_f16_splitk_noalloc", "l2_flush", "force_path", "force_splits", "set_wait_limit_ns",
     "debug_status", "last_path", "release", "EXPORTS",
 ]
 
@@ -30,6 +30,7 @@ EXPORTS = (
     "gemm_f16", "gemm_f16_ld", "sgemm_f32", "sgemm_f32_ld", "gemm_f16_host", "sgemm_f32_host",
     "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
     "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
+    "gemm_f16_splitk_noalloc",
 )
 
 PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
@@ -64,6 +65,8 @@ def lib():
                 fn = getattr(L, name)
                 fn.restype = i
                 fn.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, vp]
+            L.gemm_f16_splitk_noalloc.restype = i
+            L.gemm_f16_splitk_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, i, vp]
             L.gemm_l2_flush.restype = i
             L.gemm_l2_flush.argtypes = [ctypes.c_size_t, vp]
             L.gemm_force_path.restype = i
@@ -174,6 +177,19 @@ def sgemm_f32_host(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=Non
                               int(N if ldc is None else ldc), float(alpha), float(beta),
                               _stream(stream))
     _check(rc, "sgemm_f32_host")
+
+
+def gemm_f16_splitk_noalloc(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None,
+                            ldb=None, ldc=None, splits=0, stream=None):
+    """Split-K fp16 GEMM on the library's fixed static scratch array: never
+    allocates device memory (for callers that must not).  Raises GemmError
+    (GEMM_ERR_ARG) when the partial sums would not fit the array."""
+    M, N, K = _dims(A, B, M, N, K)
+    rc = lib().gemm_f16_splitk_noalloc(_addr(A), _addr(B), _addr(C), M, N, K,
+                                       int(K if lda is None else lda), int(N if ldb is None else ldb),
+                                       int(N if ldc is None else ldc), float(alpha), float(beta),
+                                       int(splits), _stream(stream))
+    _check(rc, "gemm_f16_splitk_noalloc")
 
 
 def l2_flush(nbytes: int = 0, stream=None):

@@ -343,6 +343,23 @@ int host_form(const T* A, const T* B, T* C, int M, int N, int K, int lda, int ld
 }
 
 }  // namespace
+
+// Device facts and the tensor-map encoder, for entry points defined in other
+// files of the library.
+int query_device(int* sm_count, DeviceStatus** status, unsigned long long* wait_limit_ns) {
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  *sm_count = d->sm_count;
+  *status = d->status;
+  *wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+  return GEMM_OK;
+}
+
+int encode_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
+                   int box_cols, int box_rows) {
+  return make_map_f16(map, ptr, rows, cols, ld, box_cols, box_rows);
+}
+
 }  // namespace gb300
 
 using namespace gb300;

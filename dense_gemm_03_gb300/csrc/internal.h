@@ -65,4 +65,12 @@ struct SgemmArgs {
 };
 cudaError_t launch_sgemm_ffma(bool vec, const SgemmArgs& args, cudaStream_t stream);
 
+// Current device: SM count, status word and wait limit (library set-up done
+// on first use).  Returns a GEMM_* code.
+int query_device(int* sm_count, DeviceStatus** status, unsigned long long* wait_limit_ns);
+
+// 2-D fp16 tensor map with 128-byte swizzle (rows x cols, row stride ld).
+int encode_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
+                   int box_cols, int box_rows);
+
 }  // namespace gb300

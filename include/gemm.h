@@ -104,6 +104,30 @@ int sgemm_f32_host(const float* A, const float* B, float* C,
                    float alpha, float beta, cudaStream_t stream);
 
 /*
+ * Allocation-free split-K GEMM.  The paper has no counterpart: this entry
+ * point is a service of this library.  Same computation and conventions as
+ * gemm_f16_ld, always through the split-K path, for callers that must not
+ * allocate device memory while they run (cudaMalloc may synchronise the
+ * device and may fail; some callers must draw every allocation from their
+ * own planner or a budget fixed at start-up).  The fp32 partial sums live in
+ * a fixed device array of GEMM_STATIC_SCRATCH_BYTES that every GPU loading
+ * this library holds until the library is unloaded; this call itself never
+ * allocates or frees.
+ *   splits   number of K slices, 0 = automatic (enough to fill the SMs)
+ *   returns  GEMM_ERR_ARG, with nothing enqueued, when
+ *            slices * M * roundup(N, 4) * 4 bytes exceed the array
+ *            (e.g. M=16, N=8192: up to 16 slices; M=8192, N=64: up to 4)
+ * The first call on each device (with that device current) looks up the
+ * array's device address; make it before any stream capture.  All calls share
+ * the array and it keeps the previous call's contents (nothing needs to start
+ * at zero); calls whose kernels overlap on the GPU race on it.
+ */
+#define GEMM_STATIC_SCRATCH_BYTES (8u << 20)
+int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uint16_t* C,
+                            int M, int N, int K, int lda, int ldb, int ldc,
+                            float alpha, float beta, int splits, cudaStream_t stream);
+
+/*
  * L2 flush used between timed replays ("advanced SGEMM" page, benchmark
  * section: a cudaMemsetAsync of an L2-sized buffer before each replay).
  * Enqueues a memset of a library-owned buffer of `bytes` bytes (0 = twice
