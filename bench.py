@@ -292,6 +292,7 @@ def run_ours(args, rank, world):
             "kernel_path": path32,
             "roofline": {"bound": "alu", "achieved": round(tflops32, 2), "peak": round(peak32, 2),
                          "unit": "TFLOP/s", "frac": round(tflops32 / peak32, 4),
+                         "traffic": _profiled_traffic("sgemm_ffma_4096"),
                          "peak_source": "%d SMs x 128 FP32 lanes x 2 FLOP x %.0f MHz" % (sm_count, sm_max)},
             "context_vs_page_colab_86ms": round(tflops32 / (2 * 4096 ** 3 / 86.1e-3 / 1e12), 1),
         },
@@ -313,13 +314,22 @@ def run_ours(args, rank, world):
 
 
 def _profiled_traffic(key):
-    """DRAM bytes per launch from the committed ncu summary, when one exists
-    for the current kernel (profiles/traffic.json); else null."""
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    (profiles/traffic.json), or None when there is none or when the kernel's
+    sources changed since the counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(key)
-    except (OSError, ValueError):
+            rec = json.load(f).get(key)
+        if not rec:
+            return None
+        h = hashlib.sha1()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha1"] else None
+    except (OSError, ValueError, KeyError):
         return None
 
 
