@@ -22,6 +22,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "../../include/gemm.h"
 #include "internal.h"
@@ -37,14 +38,24 @@ constexpr int kMaxDevices = 64;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
+// Scratch of one stream: fp32 partial sums (split-K or tail tiles) and the
+// tail-tile arrival counters.  Kernels on one stream run in order, so giving
+// each stream its own scratch keeps concurrent streams apart.
+struct StreamWs {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  void* counters = nullptr;     // unsigned long long[]
+  size_t counter_bytes = 0;
+  unsigned int epoch = 0;       // launches that used the counters
+};
+
 struct DevState {
   bool init = false;
   int err = 0;
   int sm_count = 0;
   int l2_bytes = 0;
   DeviceStatus* status = nullptr;
-  void* ws = nullptr;           // split-K workspace
-  size_t ws_bytes = 0;
+  std::unordered_map<uintptr_t, StreamWs> ws;   // per stream
   void* flush = nullptr;        // L2 flush buffer
   size_t flush_bytes = 0;
   void* host_buf[3] = {nullptr, nullptr, nullptr};  // staging for the host-buffer forms
@@ -130,6 +141,48 @@ int ensure_buffer(void** buf, size_t* have, size_t need) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Scratch of `stream` with at least `bytes` of partials and `counters`
+// arrival counters (fresh counters start at zero).  Caller holds g_mu.
+int stream_scratch(DevState* d, cudaStream_t stream, size_t bytes, size_t counters,
+                   StreamWs** out) {
+  StreamWs& w = d->ws[reinterpret_cast<uintptr_t>(stream)];
+  if (bytes) {
+    if (int rc = ensure_buffer(&w.ptr, &w.bytes, bytes)) return rc;
+  }
+  if (counters) {
+    const size_t cb = counters * sizeof(unsigned long long);
+    if (w.counter_bytes < cb || !w.counters) {
+      if (int rc = ensure_buffer(&w.counters, &w.counter_bytes, cb)) return rc;
+      if (cudaMemsetAsync(w.counters, 0, w.counter_bytes, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      w.epoch = 0;
+    }
+  }
+  *out = &w;
+  return GEMM_OK;
+}
+
+// Tail plan for `tiles` whole tiles on `ctas` persistent CTAs: the number of K
+// slices (1 = none) that minimises the number of tile-times, counting a tile
+// cut into s slices as 1/s of a tile-time per slice.
+int plan_tail_splits(long long tiles, long long ctas, int kb_total) {
+  if (tiles <= ctas || ctas <= 0) return 1;
+  const long long full = tiles / ctas, rem = tiles % ctas;
+  if (rem == 0) return 1;
+  int best = 1;
+  double best_t = static_cast<double>(full + 1);
+  for (int s = 2; s <= 4; ++s) {
+    if (kb_total / s < 4) break;
+    const double t = static_cast<double>(full) +
+                     static_cast<double>((rem * s + ctas - 1) / ctas) / static_cast<double>(s);
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
+}
+
 int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
                  int box_cols, int box_rows) {
   EncodeTiledFn enc = nullptr;
@@ -160,6 +213,15 @@ const char* kPathNames[3][3][3] = {
     {{"f16.tc.bn256.tma.epi_tma", "f16.tc.bn256.tma.epi_manual", "f16.tc.bn256.tma.splitk"},
      {"f16.tc.bn256.manual.epi_tma", "f16.tc.bn256.manual.epi_manual",
       "f16.tc.bn256.manual.splitk"}},
+};
+
+const char* kTailPathNames[3][2][2] = {
+    {{"f16.tc.bn64.tma.epi_tma.tail", "f16.tc.bn64.tma.epi_manual.tail"},
+     {"f16.tc.bn64.manual.epi_tma.tail", "f16.tc.bn64.manual.epi_manual.tail"}},
+    {{"f16.tc.bn128.tma.epi_tma.tail", "f16.tc.bn128.tma.epi_manual.tail"},
+     {"f16.tc.bn128.manual.epi_tma.tail", "f16.tc.bn128.manual.epi_manual.tail"}},
+    {{"f16.tc.bn256.tma.epi_tma.tail", "f16.tc.bn256.tma.epi_manual.tail"},
+     {"f16.tc.bn256.manual.epi_tma.tail", "f16.tc.bn256.manual.epi_manual.tail"}},
 };
 
 int check_common(const void* A, const void* B, const void* C, int M, int N, int K, long long lda,
@@ -238,19 +300,43 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
     a.kb_per_split = a.kb_total;
   }
   a.splits = splits;
-  if (tiles * splits > 0x7fffffffll) return GEMM_ERR_ARG;
-  a.num_units = static_cast<int>(tiles * splits);
+  if (tiles * splits * 4 > 0x7fffffffll) return GEMM_ERR_ARG;
 
+  a.dp_tiles = static_cast<int>(tiles);
+  a.tail_splits = 1;
+  a.tail_kb_per_split = a.kb_total;
   if (splits > 1) {
     epi = kEpiPartial;
     a.ws_ld = (N + 3) / 4 * 4;
     const size_t need = sizeof(float) * static_cast<size_t>(splits) * M * a.ws_ld;
-    {
+    std::lock_guard<std::mutex> lk(g_mu);
+    StreamWs* w = nullptr;
+    if (int rc = stream_scratch(d, stream, need, 0, &w)) return rc;
+    a.ws = static_cast<float*>(w->ptr);
+  } else if (force != 5) {
+    // Balance the last, partial wave: cut its tiles along K.
+    const long long ctas = std::min<long long>(tiles, d->sm_count);
+    int ts = plan_tail_splits(tiles, ctas, a.kb_total);
+    if (ts > 1) {
+      const long long tail_tiles = tiles % ctas;
+      a.tail_kb_per_split = (a.kb_total + ts - 1) / ts;
+      ts = (a.kb_total + a.tail_kb_per_split - 1) / a.tail_kb_per_split;   // no empty slice
+      a.dp_tiles = static_cast<int>(tiles - tail_tiles);
+      a.tail_splits = ts;
+      const size_t need = sizeof(float) * static_cast<size_t>(tail_tiles) * ts * kBM * bn;
       std::lock_guard<std::mutex> lk(g_mu);
-      if (int rc = ensure_buffer(&d->ws, &d->ws_bytes, need)) return rc;
-      a.ws = static_cast<float*>(d->ws);
+      StreamWs* w = nullptr;
+      if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tail_tiles) * 4, &w))
+        return rc;
+      a.tail_ws = static_cast<float*>(w->ptr);
+      a.tail_counters = static_cast<unsigned long long*>(w->counters);
+      a.epoch = ++w->epoch;
+      if (a.epoch == 0) a.epoch = ++w->epoch;   // 0 marks never-used counters
     }
   }
+
+  a.num_units = static_cast<int>(a.dp_tiles * static_cast<long long>(splits) +
+                                 (tiles - a.dp_tiles) * a.tail_splits);
 
   CUtensorMap tmA{}, tmB{}, tmC{};
   if (load == kLoadTma) {
@@ -262,7 +348,7 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
   const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  t_last_path = kPathNames[bi][load][epi];
+  t_last_path = a.tail_splits > 1 ? kTailPathNames[bi][load][epi] : kPathNames[bi][load][epi];
   if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
   if (splits > 1) {
@@ -418,7 +504,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 4) return GEMM_ERR_ARG;
+  if (path < 0 || path > 5) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 
@@ -467,21 +553,25 @@ int gemm_release(void) {
   int rc = GEMM_OK;
   for (int dev = 0; dev < kMaxDevices; ++dev) {
     DevState& d = g_dev[dev];
-    void** bufs[5] = {&d.ws, &d.flush, &d.host_buf[0], &d.host_buf[1], &d.host_buf[2]};
-    size_t* sizes[5] = {&d.ws_bytes, &d.flush_bytes, &d.host_bytes[0], &d.host_bytes[1],
-                        &d.host_bytes[2]};
-    bool any = false;
+    void** bufs[4] = {&d.flush, &d.host_buf[0], &d.host_buf[1], &d.host_buf[2]};
+    size_t* sizes[4] = {&d.flush_bytes, &d.host_bytes[0], &d.host_bytes[1], &d.host_bytes[2]};
+    bool any = !d.ws.empty();
     for (void** b : bufs) any = any || *b != nullptr;
     if (!any) continue;
     if (cudaSetDevice(dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
       rc = GEMM_ERR_CUDA;
       continue;
     }
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (*bufs[i]) cudaFree(*bufs[i]);
       *bufs[i] = nullptr;
       *sizes[i] = 0;
     }
+    for (auto& kv : d.ws) {
+      if (kv.second.ptr) cudaFree(kv.second.ptr);
+      if (kv.second.counters) cudaFree(kv.second.counters);
+    }
+    d.ws.clear();
   }
   cudaSetDevice(prev);
   return rc;

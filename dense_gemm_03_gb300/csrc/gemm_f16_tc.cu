@@ -78,24 +78,41 @@ struct Smem {
 
 struct Unit {
   int m0, n0, kb0, kb1, split;
+  int tail;       // 1 for a K slice of a tail tile
+  int tail_idx;   // index of the tail tile (tail units only)
 };
 
-// Work unit u -> output tile and K range.  Tiles are visited in groups of
-// group_m tile-rows so that concurrently running CTAs share B panels in L2.
+// Work unit u -> output tile and K range.  Units [0, dp_tiles*splits) are
+// whole tiles (or split-K slices); the rest are K slices of the tail tiles.
+// Tiles are visited in groups of group_m tile-rows so that concurrently
+// running CTAs share B panels in L2.
 __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn) {
-  const int split = u % p.splits;
-  const int tile = u / p.splits;
+  Unit x;
+  int tile, kpb;
+  const int dp_units = p.dp_tiles * p.splits;
+  if (u < dp_units) {
+    tile = u / p.splits;
+    x.split = u - tile * p.splits;
+    kpb = p.kb_per_split;
+    x.tail = 0;
+    x.tail_idx = 0;
+  } else {
+    const int v = u - dp_units;
+    x.tail_idx = v / p.tail_splits;
+    x.split = v - x.tail_idx * p.tail_splits;
+    tile = p.dp_tiles + x.tail_idx;
+    kpb = p.tail_kb_per_split;
+    x.tail = 1;
+  }
   const int group = p.group_m * p.tiles_n;
   const int g = tile / group;
   const int first_m = g * p.group_m;
   const int gm = min(p.tiles_m - first_m, p.group_m);
   const int r = tile - g * group;
-  Unit x;
   x.m0 = (first_m + r % gm) * BM;
   x.n0 = (r / gm) * bn;
-  x.kb0 = split * p.kb_per_split;
-  x.kb1 = min(p.kb_total, x.kb0 + p.kb_per_split);
-  x.split = split;
+  x.kb0 = x.split * kpb;
+  x.kb1 = min(p.kb_total, x.kb0 + kpb);
   return x;
 }
 
@@ -373,17 +390,95 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 5)) break;
       tc_fence_after();
       const int row0 = t.m0 + 32 * q;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
       bool ok = true;
-      if (row0 < p.M) {
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
+      bool finish = row0 < p.M;   // this warp produces final values for its rows
+      if (EPI != kEpiPartial && t.tail && finish) {
+        // Publish this slice's partial sums (tile-local rows 32q+lane, all BN
+        // columns), then count the slice in.  The last slice finishes the tile.
+        float* mine = p.tail_ws +
+                      ((static_cast<long long>(t.tail_idx) * p.tail_splits + t.split) * BM +
+                       32 * q + lane) * BN;
+        for (int j = 0; j < Cfg::kChunks; ++j) {
+          if (t.n0 + 64 * j >= p.N) break;
+          uint32_t acc[64];
+          tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
+          tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 64; c += 4)
+            __stcg(reinterpret_cast<float4*>(mine + 64 * j + c),
+                   make_float4(__uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
+                               __uint_as_float(acc[c + 2]), __uint_as_float(acc[c + 3])));
+        }
+        __threadfence();
+        __syncwarp();
+        uint32_t arrived = 0;
+        if (lane == 0) {
+          unsigned long long* cnt = p.tail_counters + t.tail_idx * 4 + q;
+          unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
+          for (;;) {
+            const unsigned long long next =
+                (static_cast<unsigned int>(cur >> 32) == p.epoch)
+                    ? cur + 1ull
+                    : ((static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
+            const unsigned long long prev = atomicCAS(cnt, cur, next);
+            if (prev == cur) {
+              arrived = static_cast<uint32_t>(next & 0xFFFFFFFFull);
+              break;
+            }
+            cur = prev;
+          }
+        }
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        finish = arrived == static_cast<uint32_t>(p.tail_splits);
+        if (finish) __threadfence();
+      }
+      if (finish) {
         for (int j = 0; j < Cfg::kChunks && ok; ++j) {
           const int col0 = t.n0 + 64 * j;
           if (col0 >= p.N) break;
           uint32_t acc[64];
+          if (EPI == kEpiTma) {
+            // wait until the store issued from this buffer two chunks ago has read it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            if (has_c && lane == 0) {
+              const uint32_t b = cc & 1u;
+              const uint32_t sbuf = base + L::kEpiOff + (ew * 2 + b) * kEpiBufBytes;
+              mbar_arrive_expect_tx(cload_bar(ew, b), kEpiBufBytes);
+              tma_load_2d(sbuf, &tmC, cload_bar(ew, b), col0, row0);
+            }
+          }
+          tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
+          tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
+          tmem_wait_ld();
+          if (EPI != kEpiPartial && t.tail) {
+            // acc := sum over slices in slice order (own slice from TMEM)
+            float sum[64];
+            for (int s2 = 0; s2 < p.tail_splits; ++s2) {
+              const float* src = p.tail_ws +
+                                 ((static_cast<long long>(t.tail_idx) * p.tail_splits + s2) * BM +
+                                  32 * q + lane) * BN + 64 * j;
+#pragma unroll
+              for (int c = 0; c < 64; c += 4) {
+                float4 v;
+                if (s2 == t.split)
+                  v = make_float4(__uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
+                                  __uint_as_float(acc[c + 2]), __uint_as_float(acc[c + 3]));
+                else
+                  v = __ldcg(reinterpret_cast<const float4*>(src + c));
+                if (s2 == 0) {
+                  sum[c] = v.x; sum[c + 1] = v.y; sum[c + 2] = v.z; sum[c + 3] = v.w;
+                } else {
+                  sum[c] += v.x; sum[c + 1] += v.y; sum[c + 2] += v.z; sum[c + 3] += v.w;
+                }
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 64; ++c) acc[c] = __float_as_uint(sum[c]);
+          }
           if (EPI == kEpiPartial) {
-            tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
-            tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
-            tmem_wait_ld();
             const int row = row0 + lane;
             if (row < p.M) {
               float* wrow = p.ws + (static_cast<long long>(t.split) * p.M + row) * p.ws_ld;
@@ -407,15 +502,6 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             const int boff = L::kEpiOff + (ew * 2 + static_cast<int>(b)) * kEpiBufBytes;
             const uint32_t sbuf = base + boff;
             uint8_t* const sptr = base_ptr + boff;
-            if (lane == 0) bulk_wait_group_read<1>();   // store from this buffer 2 chunks ago
-            __syncwarp();
-            if (has_c && lane == 0) {
-              mbar_arrive_expect_tx(cload_bar(ew, b), kEpiBufBytes);
-              tma_load_2d(sbuf, &tmC, cload_bar(ew, b), col0, row0);
-            }
-            tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
-            tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
-            tmem_wait_ld();
             if (has_c && !wait_parity(cload_bar(ew, b), (cc >> 1) & 1u, limit, st, 6)) {
               drain_wait(cload_bar(ew, b), (cc >> 1) & 1u, st, 13);
               ok = false;
@@ -438,9 +524,6 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             ++cc;
           } else {  // kEpiManual
             uint8_t* const sptr = base_ptr + L::kEpiOff + (ew * 2) * kEpiBufBytes;
-            tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
-            tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
-            tmem_wait_ld();
             const int cl = 2 * lane;   // this lane's column pair inside the chunk
             if (has_c) {
               for (int r = 0; r < 32; ++r) {

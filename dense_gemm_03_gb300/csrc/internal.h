@@ -27,10 +27,21 @@ struct TcArgs {
   int splits;         // number of K slices (1 = no split)
   int kb_total;       // ceil(K / 64)
   int kb_per_split;   // K blocks per slice (every slice non-empty)
-  int num_units;      // tiles_m * tiles_n * splits
+  int num_units;      // dp_tiles * splits + tail tiles * tail_splits
   int group_m;        // tile-order grouping along M (L2 reuse of B panels)
   float* ws;          // split-K partials [splits][M][ws_ld]
   long long ws_ld;
+  // Tail balancing (splits == 1 only): the first dp_tiles tiles (in visiting
+  // order) are computed whole; each remaining tile is cut into tail_splits
+  // K slices whose fp32 partial sums go to tail_ws; the last slice to finish
+  // (counted in tail_counters under this launch's epoch) adds them up in
+  // slice order and runs the epilogue.
+  int dp_tiles;
+  int tail_splits;
+  int tail_kb_per_split;
+  float* tail_ws;                      // [tail tile][slice][128][BN]
+  unsigned long long* tail_counters;   // [tail tile][4 row quarters]: epoch << 32 | arrivals
+  unsigned int epoch;
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
 };

@@ -132,6 +132,9 @@ extern "C" int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uin
   if (need > static_cast<double>(kScratchFloats) || tiles * s > 0x7fffffffll) return GEMM_ERR_ARG;
   a.num_units = static_cast<int>(tiles * s);
   a.ws = scratch;
+  a.dp_tiles = static_cast<int>(tiles);   // every tile split; no tail balancing
+  a.tail_splits = 1;
+  a.tail_kb_per_split = a.kb_total;
 
   const bool ab_tma = aligned16(A) && aligned16(B) && (1ll * lda * 2) % 16 == 0 &&
                       (1ll * ldb * 2) % 16 == 0;

@@ -35,10 +35,12 @@
  *   Streams    work is enqueued on `stream` (NULL = the legacy default
  *              stream) and the call returns without synchronising.  Calls on
  *              different streams that write the same C race.
- *   Scratch    some shapes (small M*N with a long K) split K over several
- *              thread blocks and need an fp32 workspace; the library owns it,
- *              per device, grows it on first need (that call may allocate
- *              device memory) and frees it in gemm_release().
+ *   Scratch    some shapes split K over several thread blocks and need an
+ *              fp32 workspace: small M*N with a long K, and the tiles of the
+ *              last, partial wave when the tiles outnumber the SMs.  The
+ *              library owns it, per device and stream, grows it on first need
+ *              (that call may allocate device memory) and frees it in
+ *              gemm_release().
  *   Errors     a negative return code (below) and nothing enqueued, except
  *              GEMM_ERR_CUDA, which reports a failed launch.  Kernels never
  *              trap: a wait that runs past its time limit sets a device
@@ -140,7 +142,8 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * 1 = tensor-memory-accelerator operand loads; 2 = predicated element loads
  * (the path taken when strides or pointers are not 16-byte aligned);
  * 3 = split-K over an fp32 workspace; 4 = (fp32 only) FFMA kernel with
- * predicated scalar loads.  A forced path that cannot serve a call (e.g. TMA
+ * predicated scalar loads; 5 = whole tiles only (no K-cutting of the last,
+ * partial wave of tiles).  A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
  */

@@ -180,3 +180,44 @@ def test_streams_are_respected():
         g.gemm_f16(dA2, dB, dC, 1.0, 0.0, M=M, N=N, K=K, stream=s)
     s.synchronize()
     check("f16", dC.cpu().numpy(), A, B, np.zeros((M, N), np.float16), 1.0, 0.0, M, N, K, K, N, N)
+
+
+# ---------------------------------------------------------------- last-wave balancing
+NO_TAIL = 5
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
+    (2000, 3000, 1000, 1000, 3000, 3000),     # 192 tiles: last wave cut into 3 K slices
+    (2000, 3001, 1000, 1000, 3001, 3001),     # N % 8 != 0: predicated epilogue
+    (2000, 3000, 1000, 1001, 3000, 3000),     # odd lda: predicated loads
+    (1300, 4000, 700, 704, 4008, 4000),       # padded operands
+])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
+def test_tail_parity(M, N, K, lda, ldb, ldc, alpha, beta, c_fill):
+    A, B, C0 = operands(40 + M + N + lda, M, N, K, lda, ldb, ldc, np.float16, c_fill=c_fill)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc)
+    assert taken.endswith(".tail"), taken
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc,
+          rows=oracle.sample_rows(M, block=64), cols=oracle.sample_cols(N, block=32))
+    assert padding_untouched(got, C0, N)
+    whole, taken2 = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc, path=NO_TAIL)
+    assert not taken2.endswith(".tail")
+    ref, absd = oracle.gemm(A, B, C0, alpha, beta, M=M, N=N, K=K, lda=lda, ldb=ldb, ldc=ldc,
+                            rows=list(range(0, M, 97)), with_absdot=True)
+    r = oracle.compare(got[::97, :N].astype(np.float64), whole[::97, :N].astype(np.float64),
+                       oracle.tol_f16(ref, absd))
+    assert r["ok"], r
+
+
+def test_tail_deterministic_with_four_slices():
+    """2048 x 4096 tiles: 256 tiles on 152 SMs, the last 104 cut into 4 K
+    slices; whichever slice finishes last, the sum runs in slice order."""
+    M, N, K = 2048, 4096, 4096
+    A, B, C0 = operands(77, M, N, K, K, N, N, np.float16)
+    r1, taken = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    assert taken.endswith(".tail")
+    for _ in range(2):
+        r2, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+        assert np.array_equal(r1.view(np.uint16), r2.view(np.uint16))
+    check("f16", r1, A, B, C0, 1.5, 0.5, M, N, K, K, N, N,
+          rows=oracle.sample_rows(M), cols=oracle.sample_cols(N))
