@@ -164,17 +164,21 @@ int stream_scratch(DevState* d, cudaStream_t stream, size_t bytes, size_t counte
 
 // Tail plan for `tiles` whole tiles on `ctas` persistent CTAs: the number of K
 // slices (1 = none) that minimises the number of tile-times, counting a tile
-// cut into s slices as 1/s of a tile-time per slice.
+// cut into s slices as 1/s of a tile-time per slice plus a small fix-up cost.
 int plan_tail_splits(long long tiles, long long ctas, int kb_total) {
   if (tiles <= ctas || ctas <= 0) return 1;
   const long long full = tiles / ctas, rem = tiles % ctas;
   if (rem == 0) return 1;
   int best = 1;
   double best_t = static_cast<double>(full + 1);
-  for (int s = 2; s <= 4; ++s) {
-    if (kb_total / s < 4) break;
+  // A sliced tile is finished by one extra pass over its partial sums (about
+  // as long as a 32-k-block main loop): only long slices, at most two, pay.
+  for (int s = 2; s <= 2; ++s) {
+    if (kb_total / s < 32) break;
+    // each extra slice costs a little: its partial sums go through L2 once
     const double t = static_cast<double>(full) +
-                     static_cast<double>((rem * s + ctas - 1) / ctas) / static_cast<double>(s);
+                     static_cast<double>((rem * s + ctas - 1) / ctas) / static_cast<double>(s) +
+                     0.03 * (s - 1);
     if (t < best_t - 1e-9) {
       best_t = t;
       best = s;
@@ -184,7 +188,7 @@ int plan_tail_splits(long long tiles, long long ctas, int kb_total) {
 }
 
 int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
-                 int box_cols, int box_rows) {
+                 int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = nullptr;
   if (int rc = encode_fn(&enc)) return rc;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -192,8 +196,8 @@ int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long lon
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -326,7 +330,7 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
       const size_t need = sizeof(float) * static_cast<size_t>(tail_tiles) * ts * kBM * bn;
       std::lock_guard<std::mutex> lk(g_mu);
       StreamWs* w = nullptr;
-      if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tail_tiles) * 4, &w))
+      if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tail_tiles) * 8, &w))
         return rc;
       a.tail_ws = static_cast<float*>(w->ptr);
       a.tail_counters = static_cast<unsigned long long*>(w->counters);
@@ -344,7 +348,8 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
     if (int rc = make_map_f16(&tmB, B, K, N, ldb, 64, 64)) return rc;
   }
   if (epi == kEpiTma) {
-    if (int rc = make_map_f16(&tmC, C, M, N, ldc, 64, 32)) return rc;
+    // epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle
+    if (int rc = make_map_f16(&tmC, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
   }
   const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);

@@ -11,17 +11,25 @@
 // (section on tiling and data movement); on sm_103a they become a
 // multi-stage mbarrier ring fed by TMA and drained by tcgen05.mma.
 //
-// One CTA per SM, persistent over output tiles (BM x BN = 128 x {64,128,256}),
-// warp-specialised:
-//   producer warp(s)  TMA tile loads (or, for unaligned operands, predicated
-//                     element loads written in the same swizzled layout)
+// One CTA per SM, persistent over work units, warp-specialised:
+//   producer warp(s)  TMA tile loads (or, for unaligned operands, 4 warps of
+//                     predicated element loads written in the same layout)
 //   MMA warp          one thread issues tcgen05.mma (M=128, N=BN, K=16) into a
 //                     double-buffered TMEM accumulator (2 x BN fp32 columns)
-//   4 epilogue warps  tcgen05.ld the accumulator (warp w owns TMEM lanes
-//                     32*(w%4) .. +31 = tile rows), apply alpha/beta in fp32,
-//                     round to fp16 and store (TMA, predicated stores, or raw
-//                     fp32 partials for split-K)
-// The epilogue of tile i overlaps the main loop of tile i+1.
+//   8 epilogue warps  warp (q, h) owns TMEM lanes 32q..32q+31 (= tile rows)
+//                     and the h-th half of the tile's columns; in 32-column
+//                     sub-chunks it loads the accumulator (the next sub-chunk's
+//                     load is in flight while the current one is converted),
+//                     applies alpha/beta in fp32 with C prefetched into
+//                     registers, rounds to fp16 and stores through a
+//                     double-buffered 2 KB staging tile by TMA (or with
+//                     predicated stores, or as fp32 split-K partials).
+// The epilogue of one unit overlaps the main loop of the next.
+//
+// A unit is a whole output tile, a split-K slice, or a K slice of one of the
+// tiles of the last, partial wave ("tail"): those write fp32 partial sums and
+// the slice that finishes last (counted per launch) adds them up in slice
+// order and runs the epilogue, so no CTA ever waits for another.
 //
 // Shared-memory operand layouts (128-byte swizzle, 1024-byte aligned):
 //   A stage: 128 rows x 64 halves, K-major; row r at r*128 B, 16-byte chunk c
@@ -29,6 +37,8 @@
 //   B stage: BN/64 column blocks of 64 (k) rows x 64 halves, N-major (MN-major
 //            operand); k-row at k*128 B inside its block, same swizzle.
 //            LBO = 8 KB (next 64 columns), SBO = 1024 B (next 8 k-rows).
+// Epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle: row r at r*64 B,
+//            16-byte chunk c stored at chunk (c ^ ((r / 2) % 4)).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,7 +50,8 @@ constexpr int BK = 64;                       // halves per k-block: one 128-byte
 constexpr int kUmmaK = 16;                   // K of one tcgen05.mma kind::f16
 constexpr int kABytes = BM * BK * 2;         // 16 KB
 constexpr int kBBlockBytes = BK * 128;       // one 64-column block of a B stage: 8 KB
-constexpr int kEpiBufBytes = 32 * 128;       // 32 rows x 64 halves
+constexpr int kSubCols = 32;                 // epilogue sub-chunk width
+constexpr int kEpiBufBytes = 32 * kSubCols * 2;   // 2 KB staging tile
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 
 template <int BN>
@@ -48,28 +59,35 @@ struct TcCfg {
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int kTmemCols = 2 * BN;   // two accumulators
-  static constexpr int kChunks = BN / 64;    // epilogue column chunks
+  static constexpr int kTmemCols = 2 * BN;     // two accumulators
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
 };
 
+// Warp roles.  With TMA loads: 1 producer, 1 MMA and 8 epilogue warps (two
+// per TMEM lane quadrant, each on half of the columns).  With predicated loads:
+// 4 producer warps, 1 MMA and 4 epilogue warps (each on all columns), so that
+// no sub-partition runs more than 3 warps and every thread keeps 168 registers.
 template <int LOAD>
 struct Roles {
   static constexpr int kProdWarps = (LOAD == kLoadTma) ? 1 : 4;
+  static constexpr int kEpiWarps = (LOAD == kLoadTma) ? 8 : 4;
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kProdWarps + 1;
-  static constexpr int kWarps = kProdWarps + 5;
+  static constexpr int kWarps = kProdWarps + 1 + kEpiWarps;
   static constexpr int kThreads = kWarps * 32;
 };
+
+// Counters per tail tile: one per epilogue warp (at most 8).
+constexpr int kTailCounters = 8;
 
 template <int BN, int EPI>
 struct Smem {
   using Cfg = TcCfg<BN>;
   static constexpr int kEpiOff = Cfg::kStages * Cfg::kStageBytes;
-  static constexpr int kEpiBytes = (EPI == kEpiPartial) ? 0 : 4 * 2 * kEpiBufBytes;
+  static constexpr int kEpiBytes = (EPI == kEpiPartial) ? 0 : 8 * 2 * kEpiBufBytes;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
-  // full[S], empty[S], acc_full[2], acc_empty[2], c_load[4][2], mma_done
-  static constexpr int kNumBars = 2 * Cfg::kStages + 2 + 2 + 8 + 1;
+  // full[S], empty[S], acc_full[2], acc_empty[2], mma_done, tmem_free
+  static constexpr int kNumBars = 2 * Cfg::kStages + 2 + 2 + 1 + 1;
   static constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
   static constexpr int kUsed = kTmemPtrOff + 16;
   static constexpr int kAlloc = kUsed + 1024;  // the dynamic base is aligned up to 1024 B
@@ -116,8 +134,16 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn) {
   return x;
 }
 
+// Partial sums of one K slice of a tail tile: BN/4 column quads x 128 rows of
+// float4, so that the 32 lanes of a warp (32 consecutive rows) touch 512
+// contiguous bytes.  Private to this kernel.
+__device__ __forceinline__ float4* tail_partials(const TcArgs& p, int tail_idx, int split, int bn) {
+  return reinterpret_cast<float4*>(p.tail_ws) +
+         (static_cast<long long>(tail_idx) * p.tail_splits + split) * (bn / 4) * BM;
+}
+
 // Waits that must not give up early because another thread failed: used only
-// to let copies already in flight land before the CTA exits.
+// to let copies and MMAs already in flight finish before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, DeviceStatus* st,
                                            int where) {
   if (mbar_try_wait(bar, parity)) return;
@@ -194,9 +220,59 @@ __device__ __forceinline__ uint4 epilogue8(const uint32_t* acc, uint4 cbits, boo
                     float2_to_half2_bits(o[4], o[5]), float2_to_half2_bits(o[6], o[7]));
 }
 
-// Byte offset of (row r, column c) inside a 128-byte-swizzled 32 x 64 half tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + ((((c >> 3) ^ (r & 7)) & 7) << 4) + ((c & 7) << 1));
+// C values of one row for a 32-column sub-chunk (4 groups of 8 halves), read
+// straight into registers with streaming loads; zero outside the matrix.  Used
+// by the TMA epilogue, where rows of C are 16-byte aligned and N % 8 == 0.
+__device__ __forceinline__ void load_c_sub(const TcArgs& p, int row, int col0, uint4 (&dst)[4]) {
+  const bool rok = row < p.M;
+  const uint4* src =
+      reinterpret_cast<const uint4*>(p.C + static_cast<long long>(row) * p.ldc + col0);
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    dst[g] = (rok && col0 + 8 * g < p.N) ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Byte offset of 16-byte chunk c (0..3) of row r in a 64-byte-swizzled staging tile.
+__device__ __forceinline__ uint32_t sw64_chunk(int r, int c) {
+  return static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// Byte offset of column c (0..31) of row r in the same tile.
+__device__ __forceinline__ uint32_t sw64_elem(int r, int c) {
+  return sw64_chunk(r, c >> 3) + static_cast<uint32_t>((c & 7) << 1);
+}
+
+// The 32 registers of an in-flight tcgen05.ld become readable here; listing
+// them as operands keeps every use after this wait.
+__device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// Adds one tail slice's partial sums for a 32-column sub-chunk into acc.
+__device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* src, bool assign) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = __ldcg(src + i * BM);
+    if (assign) {
+      acc[4 * i] = __float_as_uint(v.x);
+      acc[4 * i + 1] = __float_as_uint(v.y);
+      acc[4 * i + 2] = __float_as_uint(v.z);
+      acc[4 * i + 3] = __float_as_uint(v.w);
+    } else {
+      acc[4 * i] = __float_as_uint(__uint_as_float(acc[4 * i]) + v.x);
+      acc[4 * i + 1] = __float_as_uint(__uint_as_float(acc[4 * i + 1]) + v.y);
+      acc[4 * i + 2] = __float_as_uint(__uint_as_float(acc[4 * i + 2]) + v.z);
+      acc[4 * i + 3] = __float_as_uint(__uint_as_float(acc[4 * i + 3]) + v.w);
+    }
+  }
 }
 
 template <int BN, int LOAD, int EPI>
@@ -221,8 +297,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * S + b); };
   auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * S + 2 + b); };
-  auto cload_bar = [&](int w, uint32_t b) { return bars + 8u * (2 * S + 4 + 2 * w + b); };
-  const uint32_t done_bar = bars + 8u * (2 * S + 12);
+  const uint32_t done_bar = bars + 8u * (2 * S + 4);
+  const uint32_t tmem_free_bar = bars + 8u * (2 * S + 5);   // epilogue warps done with TMEM
   auto stage_a = [&](int s) { return base + static_cast<uint32_t>(s * Cfg::kStageBytes); };
   auto stage_b = [&](int s) { return stage_a(s) + kABytes; };
 
@@ -233,11 +309,10 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1u);
-      mbar_init(acce_bar(b), 4u);
+      mbar_init(acce_bar(b), static_cast<uint32_t>(R::kEpiWarps));
     }
-    for (int w = 0; w < 4; ++w)
-      for (uint32_t b = 0; b < 2; ++b) mbar_init(cload_bar(w, b), 1u);
     mbar_init(done_bar, 1u);
+    mbar_init(tmem_free_bar, static_cast<uint32_t>(R::kEpiWarps));
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -275,7 +350,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
             tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
 #pragma unroll
-            for (int c = 0; c < Cfg::kChunks; ++c)
+            for (int c = 0; c < BN / 64; ++c)
               tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage), t.n0 + 64 * c,
                           kb * BK);
             ++issued;
@@ -307,7 +382,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           uint8_t* const sb = sa + kABytes;
           const int k0 = kb * BK;
           // A: 128 rows x 8 chunks of 8 halves.
-#pragma unroll
+#pragma unroll 4
           for (int i = 0; i < 8; ++i) {
             const int id = tp + 128 * i;
             const int r = id >> 3, kc = id & 7;
@@ -373,49 +448,62 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         mma_commit(accf_bar(buf));       // accumulator ready for the epilogue
         ++local;
       }
-      // Every MMA issued above must complete before TMEM is released.
+      // Every MMA issued above must complete, and every epilogue warp must be
+      // done reading, before TMEM is released.
       mma_commit(done_bar);
       drain_wait(done_bar, 0u, st, 12);
+      drain_wait(tmem_free_bar, 0u, st, 14);
     }
     __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - R::kEpiWarp0;   // buffer set 0..3
+    constexpr int kWarpCols = BN * 4 / R::kEpiWarps;   // columns per epilogue warp
+    constexpr int kSubs = kWarpCols / kSubCols;
+    const int ew = warp - R::kEpiWarp0;   // 0 .. kEpiWarps-1
     const int q = warp & 3;               // TMEM lane quadrant -> rows 32q .. 32q+31
+    const int h = ew >> 2;                // column part of the tile
     const bool has_c = p.beta != 0.0f;
-    uint32_t local = 0, cc = 0;
+    const uint32_t sbuf0 = base + L::kEpiOff + ew * 2 * kEpiBufBytes;
+    uint8_t* const sptr0 = base_ptr + L::kEpiOff + ew * 2 * kEpiBufBytes;
+    uint32_t local = 0, nstore = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
       const Unit t = decode_unit(p, u, BN);
       const uint32_t buf = local & 1u, use = local >> 1;
+      const int row0 = t.m0 + 32 * q;
+      const int colw = t.n0 + h * kWarpCols;        // first column of this warp
+      const int row = row0 + lane;                  // this thread's row
+      bool finish = row0 < p.M && colw < p.N;       // this warp has outputs to produce
+      // C of the first sub-chunk is requested before the accumulator is ready.
+      uint4 c_next[4];
+      if (EPI == kEpiTma && has_c && finish && !t.tail) load_c_sub(p, row, colw, c_next);
       if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 5)) break;
       tc_fence_after();
-      const int row0 = t.m0 + 32 * q;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
-      bool ok = true;
-      bool finish = row0 < p.M;   // this warp produces final values for its rows
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * kWarpCols;
+
       if (EPI != kEpiPartial && t.tail && finish) {
-        // Publish this slice's partial sums (tile-local rows 32q+lane, all BN
-        // columns), then count the slice in.  The last slice finishes the tile.
-        float* mine = p.tail_ws +
-                      ((static_cast<long long>(t.tail_idx) * p.tail_splits + t.split) * BM +
-                       32 * q + lane) * BN;
-        for (int j = 0; j < Cfg::kChunks; ++j) {
-          if (t.n0 + 64 * j >= p.N) break;
-          uint32_t acc[64];
-          tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
-          tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
-          tmem_wait_ld();
+        // Publish this slice's partial sums, then count the slice in; the last
+        // slice to arrive finishes the tile.
+        float4* mine = tail_partials(p, t.tail_idx, t.split, BN) + 32 * q + lane;
+        for (int k = 0; k < kSubs; ++k) {
+          if (colw + kSubCols * k >= p.N) break;
+          uint32_t acc[32];
+          tmem_ld_32x32b_x32(tbase + kSubCols * k, acc);
+          tmem_wait_regs(acc);
+          const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4)
-            __stcg(reinterpret_cast<float4*>(mine + 64 * j + c),
-                   make_float4(__uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
-                               __uint_as_float(acc[c + 2]), __uint_as_float(acc[c + 3])));
+          for (int i = 0; i < 8; ++i)
+            __stcg(mine + (cq0 + i) * BM,
+                   make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
+                               __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3])));
         }
         __threadfence();
         __syncwarp();
         uint32_t arrived = 0;
         if (lane == 0) {
-          unsigned long long* cnt = p.tail_counters + t.tail_idx * 4 + q;
+          unsigned long long* cnt = p.tail_counters + t.tail_idx * kTailCounters + h * 4 + q;
           unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
           for (;;) {
             const unsigned long long next =
@@ -432,62 +520,50 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         }
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
         finish = arrived == static_cast<uint32_t>(p.tail_splits);
-        if (finish) __threadfence();
+        if (finish) {
+          __threadfence();
+          if (EPI == kEpiTma && has_c) load_c_sub(p, row, colw, c_next);
+        }
       }
+
       if (finish) {
-        for (int j = 0; j < Cfg::kChunks && ok; ++j) {
-          const int col0 = t.n0 + 64 * j;
+        uint32_t acc_a[32], acc_b[32];
+        if (!t.tail) {
+          tmem_ld_32x32b_x32(tbase, acc_a);
+          tmem_wait_regs(acc_a);
+        }
+#pragma unroll
+        for (int k = 0; k < kSubs; ++k) {
+          uint32_t(&cur)[32] = (k & 1) ? acc_b : acc_a;
+          uint32_t(&nxt)[32] = (k & 1) ? acc_a : acc_b;
+          const int col0 = colw + kSubCols * k;
           if (col0 >= p.N) break;
-          uint32_t acc[64];
+          const bool more = k + 1 < kSubs && col0 + kSubCols < p.N;
+          if (more && !t.tail) tmem_ld_32x32b_x32(tbase + kSubCols * (k + 1), nxt);   // in flight
+          uint4 c_cur[4];
           if (EPI == kEpiTma) {
-            // wait until the store issued from this buffer two chunks ago has read it
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            if (has_c && lane == 0) {
-              const uint32_t b = cc & 1u;
-              const uint32_t sbuf = base + L::kEpiOff + (ew * 2 + b) * kEpiBufBytes;
-              mbar_arrive_expect_tx(cload_bar(ew, b), kEpiBufBytes);
-              tma_load_2d(sbuf, &tmC, cload_bar(ew, b), col0, row0);
-            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) c_cur[g] = c_next[g];
+            if (has_c && more) load_c_sub(p, row, col0 + kSubCols, c_next);
           }
-          tmem_ld_32x32b_x32(tbase + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(acc));
-          tmem_ld_32x32b_x32(tbase + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(acc + 32));
-          tmem_wait_ld();
           if (EPI != kEpiPartial && t.tail) {
-            // acc := sum over slices in slice order (own slice from TMEM)
-            float sum[64];
-            for (int s2 = 0; s2 < p.tail_splits; ++s2) {
-              const float* src = p.tail_ws +
-                                 ((static_cast<long long>(t.tail_idx) * p.tail_splits + s2) * BM +
-                                  32 * q + lane) * BN + 64 * j;
-#pragma unroll
-              for (int c = 0; c < 64; c += 4) {
-                float4 v;
-                if (s2 == t.split)
-                  v = make_float4(__uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
-                                  __uint_as_float(acc[c + 2]), __uint_as_float(acc[c + 3]));
-                else
-                  v = __ldcg(reinterpret_cast<const float4*>(src + c));
-                if (s2 == 0) {
-                  sum[c] = v.x; sum[c + 1] = v.y; sum[c + 2] = v.z; sum[c + 3] = v.w;
-                } else {
-                  sum[c] += v.x; sum[c + 1] += v.y; sum[c + 2] += v.z; sum[c + 3] += v.w;
-                }
-              }
-            }
-#pragma unroll
-            for (int c = 0; c < 64; ++c) acc[c] = __float_as_uint(sum[c]);
+            // cur := sum of every slice's partial sums (this slice's included),
+            // in slice order.
+            const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
+            const float4* part = tail_partials(p, t.tail_idx, 0, BN) + 32 * q + lane + cq0 * BM;
+            const long long slice = static_cast<long long>(BN / 4) * BM;
+            add_partials(cur, part, true);
+            for (int s2 = 1; s2 < p.tail_splits; ++s2) add_partials(cur, part + s2 * slice, false);
           }
           if (EPI == kEpiPartial) {
-            const int row = row0 + lane;
             if (row < p.M) {
               float* wrow = p.ws + (static_cast<long long>(t.split) * p.M + row) * p.ws_ld;
 #pragma unroll
-              for (int c = 0; c < 64; c += 4) {
+              for (int c = 0; c < kSubCols; c += 4) {
                 const int col = col0 + c;
-                const float4 v = make_float4(__uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
-                                             __uint_as_float(acc[c + 2]),
-                                             __uint_as_float(acc[c + 3]));
+                const float4 v = make_float4(__uint_as_float(cur[c]), __uint_as_float(cur[c + 1]),
+                                             __uint_as_float(cur[c + 2]),
+                                             __uint_as_float(cur[c + 3]));
                 if (col + 4 <= p.N) {
                   *reinterpret_cast<float4*>(wrow + col) = v;
                 } else {
@@ -498,85 +574,69 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
               }
             }
           } else if (EPI == kEpiTma) {
-            const uint32_t b = cc & 1u;
-            const int boff = L::kEpiOff + (ew * 2 + static_cast<int>(b)) * kEpiBufBytes;
-            const uint32_t sbuf = base + boff;
-            uint8_t* const sptr = base_ptr + boff;
-            if (has_c && !wait_parity(cload_bar(ew, b), (cc >> 1) & 1u, limit, st, 6)) {
-              drain_wait(cload_bar(ew, b), (cc >> 1) & 1u, st, 13);
-              ok = false;
-              break;
-            }
+            const uint32_t b = nstore & 1u;
+            const uint32_t sbuf = sbuf0 + b * kEpiBufBytes;
+            uint8_t* const sptr = sptr0 + b * kEpiBufBytes;
+            // the store issued from this buffer two sub-chunks ago must have read it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint32_t off = static_cast<uint32_t>(lane * 128 + ((g ^ (lane & 7)) << 4));
-              const uint4 cv = has_c ? *reinterpret_cast<const uint4*>(sptr + off)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(sptr + off) =
-                  epilogue8(acc + 8 * g, cv, has_c, p.alpha, p.beta);
-            }
+            for (int g = 0; g < 4; ++g)
+              *reinterpret_cast<uint4*>(sptr + sw64_chunk(lane, g)) =
+                  epilogue8(cur + 8 * g, c_cur[g], has_c, p.alpha, p.beta);
             fence_proxy_async_smem();   // generic writes -> TMA store reads
             __syncwarp();
             if (lane == 0) {
               tma_store_2d(&tmC, sbuf, col0, row0);
               bulk_commit_group();
             }
-            ++cc;
-          } else {  // kEpiManual
-            uint8_t* const sptr = base_ptr + L::kEpiOff + (ew * 2) * kEpiBufBytes;
-            const int cl = 2 * lane;   // this lane's column pair inside the chunk
+            ++nstore;
+          } else {  // kEpiManual: C through shared memory with predicated accesses
+            uint8_t* const sptr = sptr0;
+            const int col = col0 + lane;   // this lane's column in the row-wise passes
             if (has_c) {
               for (int r = 0; r < 32; ++r) {
-                const int row = row0 + r, col = col0 + cl;
-                uint32_t h0 = 0, h1 = 0;
-                if (row < p.M) {
-                  const uint16_t* crow = p.C + static_cast<long long>(row) * p.ldc;
-                  if (col < p.N) h0 = crow[col];
-                  if (col + 1 < p.N) h1 = crow[col + 1];
-                }
-                *reinterpret_cast<uint32_t*>(sptr + sw128_off(r, cl)) = h0 | (h1 << 16);
+                const int rr = row0 + r;
+                const uint16_t v = (rr < p.M && col < p.N)
+                                       ? p.C[static_cast<long long>(rr) * p.ldc + col]
+                                       : static_cast<uint16_t>(0);
+                *reinterpret_cast<uint16_t*>(sptr + sw64_elem(r, lane)) = v;
               }
               __syncwarp();
             }
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint32_t off = static_cast<uint32_t>(lane * 128 + ((g ^ (lane & 7)) << 4));
+            for (int g = 0; g < 4; ++g) {
+              const uint32_t off = sw64_chunk(lane, g);
               const uint4 cv = has_c ? *reinterpret_cast<const uint4*>(sptr + off)
                                      : make_uint4(0u, 0u, 0u, 0u);
               *reinterpret_cast<uint4*>(sptr + off) =
-                  epilogue8(acc + 8 * g, cv, has_c, p.alpha, p.beta);
+                  epilogue8(cur + 8 * g, cv, has_c, p.alpha, p.beta);
             }
             __syncwarp();
             for (int r = 0; r < 32; ++r) {
-              const int row = row0 + r, col = col0 + cl;
-              if (row < p.M) {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(sptr + sw128_off(r, cl));
-                uint16_t* crow = p.C + static_cast<long long>(row) * p.ldc;
-                if (col < p.N) crow[col] = static_cast<uint16_t>(v & 0xFFFFu);
-                if (col + 1 < p.N) crow[col + 1] = static_cast<uint16_t>(v >> 16);
-              }
+              const int rr = row0 + r;
+              if (rr < p.M && col < p.N)
+                p.C[static_cast<long long>(rr) * p.ldc + col] =
+                    *reinterpret_cast<const uint16_t*>(sptr + sw64_elem(r, lane));
             }
             __syncwarp();
           }
+          if (more && !t.tail) tmem_wait_regs(nxt);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));   // accumulator may be overwritten
       ++local;
-      if (!ok) break;
     }
-    if (EPI == kEpiTma && lane == 0) bulk_wait_group<0>();
+    if (EPI == kEpiTma && lane == 0) bulk_wait_group<0>();   // stores done reading smem
+    tc_fence_before();
     __syncwarp();
+    if (lane == 0) mbar_arrive(tmem_free_bar);
   }
-
-  // ------------------------------------------------------------ teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == R::kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
-  }
+  // No CTA-wide barrier at the end: every role has already waited for its own
+  // asynchronous work (TMA loads, MMAs, TMA stores), and TMEM is released by
+  // the MMA warp only after all epilogue warps have signalled tmem_free.
 }
 
 template <int BN, int LOAD, int EPI>
@@ -636,5 +696,7 @@ int tc_smem_bytes(int bn, int epi_mode) {
 int tc_threads(int load_mode) {
   return load_mode == kLoadTma ? Roles<kLoadTma>::kThreads : Roles<kLoadManual>::kThreads;
 }
+
+int tc_epilogue_tile_cols() { return kSubCols; }
 
 }  // namespace gb300

@@ -40,7 +40,7 @@ struct TcArgs {
   int tail_splits;
   int tail_kb_per_split;
   float* tail_ws;                      // [tail tile][slice][128][BN]
-  unsigned long long* tail_counters;   // [tail tile][4 row quarters]: epoch << 32 | arrivals
+  unsigned long long* tail_counters;   // [tail tile][8 epilogue warps]: epoch << 32 | arrivals
   unsigned int epoch;
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
