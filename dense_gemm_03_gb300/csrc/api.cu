@@ -228,6 +228,11 @@ const char* kTailPathNames[3][2][2] = {
      {"f16.tc.bn256.manual.epi_tma.tail", "f16.tc.bn256.manual.epi_manual.tail"}},
 };
 
+const char* kPairPathNames[2][2] = {
+    {"f16.tc.pair.bn256.tma.epi_tma", "f16.tc.pair.bn256.tma.epi_tma.tail"},
+    {"f16.tc.pair.bn256.tma.epi_manual", "f16.tc.pair.bn256.tma.epi_manual.tail"},
+};
+
 int check_common(const void* A, const void* B, const void* C, int M, int N, int K, long long lda,
                  long long ldb, long long ldc, float alpha) {
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_DIM;
@@ -306,7 +311,20 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   a.splits = splits;
   if (tiles * splits * 4 > 0x7fffffffll) return GEMM_ERR_ARG;
 
-  a.dp_tiles = static_cast<int>(tiles);
+  // CTA pairs (256 x 256 tiles on clusters of 2 sharing each MMA) for the
+  // large aligned shapes: each SM then stages half as much of B per MMA.
+  int pair_slots = 0;
+  const bool pair = splits == 1 && force != 6 && bn == 256 && load == kLoadTma &&
+                    a.tiles_m >= 2 && (pair_slots = tc_pair_max_clusters(epi)) > 0;
+  long long units_tiles = tiles;   // tiles in units of the worker (CTA or pair)
+  long long workers = std::min<long long>(tiles, d->sm_count);
+  if (pair) {
+    a.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
+    units_tiles = 1ll * a.tiles_m * a.tiles_n;
+    workers = std::min<long long>(units_tiles, pair_slots);
+  }
+
+  a.dp_tiles = static_cast<int>(units_tiles);
   a.tail_splits = 1;
   a.tail_kb_per_split = a.kb_total;
   if (splits > 1) {
@@ -319,18 +337,18 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
     a.ws = static_cast<float*>(w->ptr);
   } else if (force != 5) {
     // Balance the last, partial wave: cut its tiles along K.
-    const long long ctas = std::min<long long>(tiles, d->sm_count);
-    int ts = plan_tail_splits(tiles, ctas, a.kb_total);
+    int ts = plan_tail_splits(units_tiles, workers, a.kb_total);
     if (ts > 1) {
-      const long long tail_tiles = tiles % ctas;
+      const long long tail_tiles = units_tiles % workers;
+      const long long parts = tail_tiles * (pair ? 2 : 1);   // 128-row parts with own partials
       a.tail_kb_per_split = (a.kb_total + ts - 1) / ts;
       ts = (a.kb_total + a.tail_kb_per_split - 1) / a.tail_kb_per_split;   // no empty slice
-      a.dp_tiles = static_cast<int>(tiles - tail_tiles);
+      a.dp_tiles = static_cast<int>(units_tiles - tail_tiles);
       a.tail_splits = ts;
-      const size_t need = sizeof(float) * static_cast<size_t>(tail_tiles) * ts * kBM * bn;
+      const size_t need = sizeof(float) * static_cast<size_t>(parts) * ts * kBM * bn;
       std::lock_guard<std::mutex> lk(g_mu);
       StreamWs* w = nullptr;
-      if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tail_tiles) * 8, &w))
+      if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(parts) * 8, &w))
         return rc;
       a.tail_ws = static_cast<float*>(w->ptr);
       a.tail_counters = static_cast<unsigned long long*>(w->counters);
@@ -340,7 +358,7 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
 
   a.num_units = static_cast<int>(a.dp_tiles * static_cast<long long>(splits) +
-                                 (tiles - a.dp_tiles) * a.tail_splits);
+                                 (units_tiles - a.dp_tiles) * a.tail_splits);
 
   CUtensorMap tmA{}, tmB{}, tmC{};
   if (load == kLoadTma) {
@@ -350,6 +368,13 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   if (epi == kEpiTma) {
     // epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle
     if (int rc = make_map_f16(&tmC, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
+  }
+  if (pair) {
+    const int grid = 2 * static_cast<int>(std::min<long long>(a.num_units, workers));
+    t_last_path = a.tail_splits > 1 ? kPairPathNames[epi][1] : kPairPathNames[epi][0];
+    if (launch_gemm_f16_tc_pair(epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_OK;
   }
   const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
@@ -509,7 +534,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 5) return GEMM_ERR_ARG;
+  if (path < 0 || path > 6) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 

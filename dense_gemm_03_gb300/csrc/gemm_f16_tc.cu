@@ -54,13 +54,17 @@ constexpr int kSubCols = 32;                 // epilogue sub-chunk width
 constexpr int kEpiBufBytes = 32 * kSubCols * 2;   // 2 KB staging tile
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 
-template <int BN>
+// PAIR: two CTAs of a cluster share each tcgen05.mma.cta_group::2 (M = 256);
+// each CTA stages its own 128 rows of A and half of the BN columns of B.
+template <int BN, bool PAIR>
 struct TcCfg {
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBLoadCols = PAIR ? BN / 2 : BN;   // B columns staged by this CTA
+  static constexpr int kBBytes = kBLoadCols * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kStages = PAIR ? 6 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int kTmemCols = 2 * BN;     // two accumulators
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+  static_assert(!PAIR || BN == 256, "pairs use 256-wide tiles");
 };
 
 // Warp roles.  With TMA loads: 1 producer, 1 MMA and 8 epilogue warps (two
@@ -80,9 +84,9 @@ struct Roles {
 // Counters per tail tile: one per epilogue warp (at most 8).
 constexpr int kTailCounters = 8;
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 struct Smem {
-  using Cfg = TcCfg<BN>;
+  using Cfg = TcCfg<BN, PAIR>;
   static constexpr int kEpiOff = Cfg::kStages * Cfg::kStageBytes;
   static constexpr int kEpiBytes = (EPI == kEpiPartial) ? 0 : 8 * 2 * kEpiBufBytes;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
@@ -104,7 +108,8 @@ struct Unit {
 // whole tiles (or split-K slices); the rest are K slices of the tail tiles.
 // Tiles are visited in groups of group_m tile-rows so that concurrently
 // running CTAs share B panels in L2.
-__device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn) {
+__device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn, int bm_tile = BM,
+                                           int rank = 0) {
   Unit x;
   int tile, kpb;
   const int dp_units = p.dp_tiles * p.splits;
@@ -127,7 +132,7 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn) {
   const int first_m = g * p.group_m;
   const int gm = min(p.tiles_m - first_m, p.group_m);
   const int r = tile - g * group;
-  x.m0 = (first_m + r % gm) * BM;
+  x.m0 = (first_m + r % gm) * bm_tile + rank * BM;
   x.n0 = (r / gm) * bn;
   x.kb0 = x.split * kpb;
   x.kb1 = min(p.kb_total, x.kb0 + kpb);
@@ -275,15 +280,22 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* 
   }
 }
 
-template <int BN, int LOAD, int EPI>
+template <int BN, int LOAD, int EPI, bool PAIR>
 __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
-  using Cfg = TcCfg<BN>;
+  using Cfg = TcCfg<BN, PAIR>;
   using R = Roles<LOAD>;
-  using L = Smem<BN, EPI>;
+  using L = Smem<BN, EPI, PAIR>;
   constexpr int S = Cfg::kStages;
+  static_assert(!PAIR || (LOAD == kLoadTma && EPI != kEpiPartial), "pair configuration");
+  // Units are handed out per CTA, or per CTA pair (cluster of 2).
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int worker = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int nworkers = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int bm_tile = PAIR ? 2 * BM : BM;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1u);
-      mbar_init(acce_bar(b), static_cast<uint32_t>(R::kEpiWarps));
+      mbar_init(acce_bar(b), static_cast<uint32_t>((PAIR ? 2 : 1) * R::kEpiWarps));
     }
     mbar_init(done_bar, 1u);
     mbar_init(tmem_free_bar, static_cast<uint32_t>(R::kEpiWarps));
@@ -317,8 +329,13 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == R::kMmaWarp) {
-    tmem_alloc(base + L::kTmemPtrOff, Cfg::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(base + L::kTmemPtrOff, Cfg::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(base + L::kTmemPtrOff, Cfg::kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (LOAD == kLoadTma && warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
@@ -326,7 +343,11 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   }
   if (EPI == kEpiTma && warp == R::kEpiWarp0 && lane == 0) prefetch_tensormap(&tmC);
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (PAIR)
+    cluster_sync();   // the peer's barriers are initialised before any remote use
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::kTmemPtrOff);
 
@@ -340,19 +361,32 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-          const Unit t = decode_unit(p, u, BN);
+        for (int u = worker; ok && u < p.num_units; u += nworkers) {
+          const Unit t = decode_unit(p, u, BN, bm_tile, rank);
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
             if (!wait_parity(empty_bar(stage), phase ^ 1u, limit, st, 1)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
-            tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
+            if (PAIR) {
+              // Both CTAs' bytes are counted on the leader's barrier; only the
+              // leader arms it (for the pair's total), the peer's copies just
+              // signal it.
+              const uint32_t fb = map_to_cta(full_bar(stage), 0);
+              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
+              tma_load_2d_pair(stage_a(stage), &tmA, fb, kb * BK, t.m0);
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage), t.n0 + 64 * c,
-                          kb * BK);
+              for (int c = 0; c < Cfg::kBLoadCols / 64; ++c)
+                tma_load_2d_pair(stage_b(stage) + c * kBBlockBytes, &tmB, fb,
+                                 t.n0 + static_cast<int>(rank) * Cfg::kBLoadCols + 64 * c, kb * BK);
+            } else {
+              mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+              tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
+                            t.n0 + 64 * c, kb * BK);
+            }
             ++issued;
             if (++stage == S) {
               stage = 0;
@@ -361,9 +395,16 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           }
         }
         // The last loads (at most one per stage) must land before the CTA exits.
+        // With pairs the completion is counted in the leader, so wait instead for
+        // the MMAs that consumed them (which also guarantees that every commit
+        // the leader multicasts into this CTA's stage barriers has arrived).
         const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
-        for (uint32_t i = issued - n; i < issued; ++i)
-          drain_wait(full_bar(static_cast<int>(i % S)), (i / S) & 1u, st, 11);
+        for (uint32_t i = issued - n; i < issued; ++i) {
+          if (PAIR)
+            drain_wait(empty_bar(static_cast<int>(i % S)), (i / S) & 1u, st, 15);
+          else
+            drain_wait(full_bar(static_cast<int>(i % S)), (i / S) & 1u, st, 11);
+        }
       }
       __syncwarp();
     } else {
@@ -371,8 +412,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit t = decode_unit(p, u, BN);
+      for (int u = worker; ok && u < p.num_units; u += nworkers) {
+        const Unit t = decode_unit(p, u, BN, bm_tile, rank);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!wait_parity(empty_bar(stage), phase ^ 1u, limit, st, 2)) {
             ok = false;
@@ -414,13 +455,13 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     }
   } else if (warp == R::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(0u, BM, BN, 0u, 1u);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc(0u, PAIR ? 2 * BM : BM, BN, 0u, 1u);
       int stage = 0;
       uint32_t phase = 0, local = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const Unit t = decode_unit(p, u, BN);
+      for (int u = worker; ok && u < p.num_units; u += nworkers) {
+        const Unit t = decode_unit(p, u, BN, bm_tile, rank);
         const uint32_t buf = local & 1u, use = local >> 1;
         if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 3)) break;
         tc_fence_after();
@@ -436,27 +477,52 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           for (int kk = 0; kk < BK / kUmmaK; ++kk) {
             const uint64_t ad = smem_desc_sw128(a0 + kk * (kUmmaK * 2), 16u, 1024u);
             const uint64_t bd = smem_desc_sw128(b0 + kk * (kUmmaK * 128), kBBlockBytes, 1024u);
-            mma_f16_ss(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+            if (PAIR)
+              mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+            else
+              mma_f16_ss(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          // frees the stage (in both CTAs of a pair) once these MMAs finish
+          if (PAIR)
+            mma_commit_pair_multicast(empty_bar(stage), 3);
+          else
+            mma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(accf_bar(buf));       // accumulator ready for the epilogue
+        // accumulator ready for the epilogue(s)
+        if (PAIR)
+          mma_commit_pair_multicast(accf_bar(buf), 3);
+        else
+          mma_commit(accf_bar(buf));
         ++local;
       }
-      // Every MMA issued above must complete, and every epilogue warp must be
-      // done reading, before TMEM is released.
-      mma_commit(done_bar);
+      // Every MMA issued above must complete before TMEM is released.
+      if (PAIR)
+        mma_commit_pair_multicast(done_bar, 3);
+      else
+        mma_commit(done_bar);
       drain_wait(done_bar, 0u, st, 12);
-      drain_wait(tmem_free_bar, 0u, st, 14);
+      if (PAIR) {
+        // The last accumulator releases (from both CTAs) must have arrived
+        // before this CTA may leave.
+        const uint32_t first = local > 2u ? local - 2u : 0u;
+        for (uint32_t j = first; j < local; ++j) drain_wait(acce_bar(j & 1u), (j >> 1) & 1u, st, 16);
+      }
+    } else if (PAIR && lane == 0) {
+      drain_wait(done_bar, 0u, st, 12);   // the leader's MMAs also wrote this CTA's TMEM
     }
+    // Every epilogue warp of this CTA must be done reading TMEM before it is released.
+    if (lane == 0) drain_wait(tmem_free_bar, 0u, st, 14);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, Cfg::kTmemCols);
   } else {
     // ------------------------------------------------------------ epilogue
     constexpr int kWarpCols = BN * 4 / R::kEpiWarps;   // columns per epilogue warp
@@ -468,10 +534,12 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     const uint32_t sbuf0 = base + L::kEpiOff + ew * 2 * kEpiBufBytes;
     uint8_t* const sptr0 = base_ptr + L::kEpiOff + ew * 2 * kEpiBufBytes;
     uint32_t local = 0, nstore = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-      const Unit t = decode_unit(p, u, BN);
+    for (int u = worker; u < p.num_units; u += nworkers) {
+      const Unit t = decode_unit(p, u, BN, bm_tile, rank);
       const uint32_t buf = local & 1u, use = local >> 1;
       const int row0 = t.m0 + 32 * q;
+      // tail bookkeeping is per CTA: the rows of one CTA of a pair form their own part
+      const int tail_part = PAIR ? 2 * t.tail_idx + static_cast<int>(rank) : t.tail_idx;
       const int colw = t.n0 + h * kWarpCols;        // first column of this warp
       const int row = row0 + lane;                  // this thread's row
       bool finish = row0 < p.M && colw < p.N;       // this warp has outputs to produce
@@ -486,7 +554,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       if (EPI != kEpiPartial && t.tail && finish) {
         // Publish this slice's partial sums, then count the slice in; the last
         // slice to arrive finishes the tile.
-        float4* mine = tail_partials(p, t.tail_idx, t.split, BN) + 32 * q + lane;
+        float4* mine = tail_partials(p, tail_part, t.split, BN) + 32 * q + lane;
         for (int k = 0; k < kSubs; ++k) {
           if (colw + kSubCols * k >= p.N) break;
           uint32_t acc[32];
@@ -503,7 +571,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         __syncwarp();
         uint32_t arrived = 0;
         if (lane == 0) {
-          unsigned long long* cnt = p.tail_counters + t.tail_idx * kTailCounters + h * 4 + q;
+          unsigned long long* cnt = p.tail_counters + tail_part * kTailCounters + h * 4 + q;
           unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
           for (;;) {
             const unsigned long long next =
@@ -550,7 +618,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             // cur := sum of every slice's partial sums (this slice's included),
             // in slice order.
             const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
-            const float4* part = tail_partials(p, t.tail_idx, 0, BN) + 32 * q + lane + cq0 * BM;
+            const float4* part = tail_partials(p, tail_part, 0, BN) + 32 * q + lane + cq0 * BM;
             const long long slice = static_cast<long long>(BN / 4) * BM;
             add_partials(cur, part, true);
             for (int s2 = 1; s2 < p.tail_splits; ++s2) add_partials(cur, part + s2 * slice, false);
@@ -626,7 +694,13 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(buf));   // accumulator may be overwritten
+      // the accumulator may be overwritten (with pairs: counted on the leader)
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(map_to_cta(acce_bar(buf), 0));
+        else
+          mbar_arrive(acce_bar(buf));
+      }
       ++local;
     }
     if (EPI == kEpiTma && lane == 0) bulk_wait_group<0>();   // stores done reading smem
@@ -634,41 +708,100 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(tmem_free_bar);
   }
+  if (PAIR) {
+    // Neither CTA of a pair leaves while the other may still touch its shared
+    // memory (remote barrier arrivals, multicast commits).
+    __syncwarp();
+    cluster_sync();
+  }
   // No CTA-wide barrier at the end: every role has already waited for its own
   // asynchronous work (TMA loads, MMAs, TMA stores), and TMEM is released by
   // the MMA warp only after all epilogue warps have signalled tmem_free.
 }
 
-template <int BN, int LOAD, int EPI>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                       const TcArgs& args, int grid, cudaStream_t stream) {
-  using L = Smem<BN, EPI>;
-  auto kernel = gemm_f16_tc_kernel<BN, LOAD, EPI>;
+template <int BN, int LOAD, int EPI, bool PAIR>
+cudaError_t configure(int dev) {
+  using L = Smem<BN, EPI, PAIR>;
   static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               L::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  kernel<<<grid, Roles<LOAD>::kThreads, L::kAlloc, stream>>>(tmA, tmB, tmC, args);
+  return cudaSuccess;
+}
+
+template <int BN, int LOAD, int EPI, bool PAIR>
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                       const TcArgs& args, int grid, cudaStream_t stream) {
+  using L = Smem<BN, EPI, PAIR>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = configure<BN, LOAD, EPI, PAIR>(dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(Roles<LOAD>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR>, tmA, tmB, tmC, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Largest number of CTA pairs of this configuration that can be resident at
+// once (pairs must sit in one GPC), cached per device.
+template <int EPI>
+int pair_max_clusters(int dev) {
+  static int cached[64] = {};
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  using L = Smem<256, EPI, true>;
+  if (configure<256, kLoadTma, EPI, true>(dev) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(Roles<kLoadTma>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_tc_kernel<256, kLoadTma, EPI, true>, &cfg) !=
+      cudaSuccess)
+    return 0;
+  cached[dev] = n;
+  return n;
 }
 
 template <int BN>
 cudaError_t launch_bn(int load, int epi, const CUtensorMap& a, const CUtensorMap& b,
                       const CUtensorMap& c, const TcArgs& args, int grid, cudaStream_t s) {
   if (load == kLoadTma) {
-    if (epi == kEpiTma) return launch_one<BN, kLoadTma, kEpiTma>(a, b, c, args, grid, s);
-    if (epi == kEpiManual) return launch_one<BN, kLoadTma, kEpiManual>(a, b, c, args, grid, s);
-    return launch_one<BN, kLoadTma, kEpiPartial>(a, b, c, args, grid, s);
+    if (epi == kEpiTma) return launch_one<BN, kLoadTma, kEpiTma, false>(a, b, c, args, grid, s);
+    if (epi == kEpiManual)
+      return launch_one<BN, kLoadTma, kEpiManual, false>(a, b, c, args, grid, s);
+    return launch_one<BN, kLoadTma, kEpiPartial, false>(a, b, c, args, grid, s);
   }
-  if (epi == kEpiTma) return launch_one<BN, kLoadManual, kEpiTma>(a, b, c, args, grid, s);
-  if (epi == kEpiManual) return launch_one<BN, kLoadManual, kEpiManual>(a, b, c, args, grid, s);
-  return launch_one<BN, kLoadManual, kEpiPartial>(a, b, c, args, grid, s);
+  if (epi == kEpiTma) return launch_one<BN, kLoadManual, kEpiTma, false>(a, b, c, args, grid, s);
+  if (epi == kEpiManual)
+    return launch_one<BN, kLoadManual, kEpiManual, false>(a, b, c, args, grid, s);
+  return launch_one<BN, kLoadManual, kEpiPartial, false>(a, b, c, args, grid, s);
 }
 
 }  // namespace
@@ -684,13 +817,20 @@ cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtens
   }
 }
 
-int tc_smem_bytes(int bn, int epi_mode) {
-  const bool part = epi_mode == kEpiPartial;
-  switch (bn) {
-    case 256: return part ? Smem<256, kEpiPartial>::kAlloc : Smem<256, kEpiTma>::kAlloc;
-    case 128: return part ? Smem<128, kEpiPartial>::kAlloc : Smem<128, kEpiTma>::kAlloc;
-    default: return part ? Smem<64, kEpiPartial>::kAlloc : Smem<64, kEpiTma>::kAlloc;
-  }
+cudaError_t launch_gemm_f16_tc_pair(int epi_mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                    const CUtensorMap& tmC, const TcArgs& args, int grid,
+                                    cudaStream_t stream) {
+  if (epi_mode == kEpiTma)
+    return launch_one<256, kLoadTma, kEpiTma, true>(tmA, tmB, tmC, args, grid, stream);
+  if (epi_mode == kEpiManual)
+    return launch_one<256, kLoadTma, kEpiManual, true>(tmA, tmB, tmC, args, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+int tc_pair_max_clusters(int epi_mode) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return epi_mode == kEpiTma ? pair_max_clusters<kEpiTma>(dev) : pair_max_clusters<kEpiManual>(dev);
 }
 
 int tc_threads(int load_mode) {

@@ -51,8 +51,16 @@ struct TcArgs {
 cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, const CUtensorMap& tmC, const TcArgs& args,
                                int grid, cudaStream_t stream);
-int tc_smem_bytes(int bn, int epi_mode);
 int tc_threads(int load_mode);
+
+// The same GEMM on CTA pairs (clusters of 2 sharing tcgen05.mma.cta_group::2):
+// 256 x 256 output tiles, TMA operand loads only, epilogue kEpiTma or
+// kEpiManual.  tiles_m counts 256-row tiles; grid = 2 x (number of pairs).
+cudaError_t launch_gemm_f16_tc_pair(int epi_mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                    const CUtensorMap& tmC, const TcArgs& args, int grid,
+                                    cudaStream_t stream);
+// Pairs of that configuration that fit on the device at once (0 on error).
+int tc_pair_max_clusters(int epi_mode);
 
 // Split-K reduction: C = half(alpha * sum_s ws[s] + beta * C).
 cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int splits, uint16_t* C,

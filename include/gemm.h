@@ -143,7 +143,8 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * (the path taken when strides or pointers are not 16-byte aligned);
  * 3 = split-K over an fp32 workspace; 4 = (fp32 only) FFMA kernel with
  * predicated scalar loads; 5 = whole tiles only (no K-cutting of the last,
- * partial wave of tiles).  A forced path that cannot serve a call (e.g. TMA
+ * partial wave of tiles); 6 = no CTA pairs (one CTA per 128-row tile).  A
+ * forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
  */

@@ -222,3 +222,57 @@ def test_tail_deterministic():
         assert np.array_equal(r1.view(np.uint16), r2.view(np.uint16))
     check("f16", r1, A, B, C0, 1.5, 0.5, M, N, K, K, N, N,
           rows=oracle.sample_rows(M), cols=oracle.sample_cols(N))
+
+
+# ---------------------------------------------------------------- CTA pairs (cta_group::2)
+NO_PAIR = 6
+
+
+@pytest.mark.parametrize("M,N,K,ldc", [
+    (512, 512, 128, 512),        # one pair tile per cluster
+    (384, 768, 640, 768),        # 1.5 pair rows: the second CTA of the last pair is half empty
+    (300, 1000, 1000, 1000),     # ragged everything
+    (257, 512, 256, 512),        # the second CTA of the last pair has one row
+    (1000, 1001, 700, 1001),     # N % 8 != 0: predicated epilogue on pairs
+    (2048, 2048, 4096, 2048),    # enough tiles for the last-wave split
+])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
+def test_pair_parity(M, N, K, ldc, alpha, beta, c_fill):
+    A, B, C0 = operands(60 + M + N + K, M, N, K, K, N, ldc, np.float16, c_fill=c_fill)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, ldc)
+    if (M + 127) // 128 >= 2 and N > 128 and taken.find("splitk") < 0:
+        assert ".pair." in taken, taken
+    big = M * N * K > 2e9
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, ldc,
+          rows=oracle.sample_rows(M) if big else None, cols=oracle.sample_cols(N) if big else None)
+    assert padding_untouched(got, C0, N)
+
+
+def test_pair_identity_exact():
+    M = K = 768
+    N = 512
+    A = np.eye(M, dtype=np.float16)
+    B = synthetic.uniform(9, 2, (K, N), dtype=np.float16)
+    C0 = np.full((M, N), np.nan, dtype=np.float16)
+    import dense_gemm_03_gb300 as g
+    prev = g.force_splits(1)
+    try:
+        got, taken = run("f16", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    finally:
+        g.force_splits(prev)
+    assert ".pair." in taken or "splitk" in taken
+    assert np.array_equal(got.view(np.uint16), B.view(np.uint16))
+
+
+def test_pair_matches_single_cta_and_is_deterministic():
+    M, N, K = 1536, 2048, 1024
+    A, B, C0 = operands(61, M, N, K, K, N, N, np.float16)
+    p1, t1 = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+    p2, _ = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+    s1, t2 = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N, path=NO_PAIR)
+    assert ".pair." in t1 and ".pair." not in t2
+    assert np.array_equal(p1.view(np.uint16), p2.view(np.uint16))
+    # same products, possibly another summation order inside the tensor core
+    ref, absd = oracle.gemm(A, B, C0, 0.75, -0.25, rows=list(range(0, M, 61)), with_absdot=True)
+    r = oracle.compare(p1[::61].astype(np.float64), s1[::61].astype(np.float64), oracle.tol_f16(ref, absd))
+    assert r["ok"], r
