@@ -43,6 +43,12 @@ METRIC = ("GEMM TFLOPS (2MNK/t) at 4096³ fp16-in/fp32-acc and fp32; "
           "% of tensor/FMA peak")
 F16_CFG = dict(M=4096, N=4096, K=4096, alpha=1.5, beta=0.5)
 F32_CFG = dict(M=4096, N=4096, K=4096, alpha=1.0, beta=0.0)
+# (M, N, K, lda, alpha, beta, name): the fp16 edge shapes, ldb = ldc = N
+EDGE_SHAPES = [
+    (4097, 1023, 777, 780, 0.75, -0.25, "fp16 4097x1023x777, lda=780 (unaligned)"),
+    (16, 8192, 8192, 8192, 0.75, -0.25, "fp16 skinny 16x8192x8192 (HBM-bound)"),
+    (8192, 64, 4096, 4096, 0.75, -0.25, "fp16 tall 8192x64x4096 (HBM-bound)"),
+]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128
@@ -203,6 +209,7 @@ def run_ours(args, rank, world):
     fC = torch.zeros((M, N), dtype=torch.float32, device="cuda")
     f32 = lambda: g.sgemm_f32(fA, fB, fC, 1.0, 0.0, stream=stream)
 
+    peak16_local = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     if world > 1:
         torch.distributed.barrier()
     sampler = ClockSampler(dev).start()
@@ -227,6 +234,28 @@ def run_ours(args, rank, world):
     flops = 2.0 * M * N * K
     tflops16 = flops / (mean16 * 1e-3) / 1e12
     tflops32 = flops / (mean32 * 1e-3) / 1e12
+
+    # the other workloads of the metric, timed the same way (context for the headline)
+    shapes = []
+    if not args.no_shapes:
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        for (sM, sN, sK, slda, alpha, beta, name) in EDGE_SHAPES:
+            seed_e = synthetic.config_seed(4)
+            eA, _ = _fill_device((sM * slda,), np.float16, seed_e, synthetic.STREAM_A)
+            eB, _ = _fill_device((sK, sN), np.float16, seed_e, synthetic.STREAM_B)
+            eC, _ = _fill_device((sM, sN), np.float16, seed_e, synthetic.STREAM_C)
+            fn = lambda: g.gemm_f16(eA, eB, eC, alpha, beta, M=sM, N=sN, K=sK, lda=slda, ldb=sN,
+                                    ldc=sN, stream=stream)
+            ms = timed_replays(fn, max(20, args.steps // 20), 5, stream, flush_bytes)
+            t = sum(ms) / len(ms)
+            byts = 2 * (sM * sK + sK * sN) + 2 * 2 * sM * sN
+            fl = 2.0 * sM * sN * sK
+            tf = fl / (t * 1e-3) / 1e12
+            gbs = byts / (t * 1e-3) / 1e9
+            shapes.append({"workload": name, "us": round(t * 1e3, 2), "tflops": round(tf, 1),
+                           "gb_s": round(gbs, 1), "frac_tensor": round(tf / peak16_local, 3),
+                           "frac_hbm": round(gbs / hbm, 3), "kernel_path": g.last_path()})
+            del eA, eB, eC
 
     # end to end through the host-buffer C-ABI call (copies inside the timed region)
     pA = torch.from_numpy(hA).pin_memory()
@@ -304,6 +333,7 @@ def run_ours(args, rank, world):
             "ms_per_step": round(e2e_mean, 4),
             "api": "gemm_f16_host (pinned host buffers)",
         },
+        "edge_shapes": shapes,
         "gpu_launches": args.steps + f32_steps,
         "clocks": clocks,
         "wall_s_timed": round(t_wall1 - t_wall0, 3),
@@ -456,6 +486,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shapes", action="store_true", help="skip the edge-shape timings")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-out", default=None)
     ap.add_argument("--sweep-sizes", default=None)

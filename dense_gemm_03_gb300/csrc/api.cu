@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -47,6 +48,8 @@ struct StreamWs {
   void* counters = nullptr;     // unsigned long long[]
   size_t counter_bytes = 0;
   unsigned int epoch = 0;       // launches that used the counters
+  void* realigned = nullptr;    // aligned copies of unaligned operands
+  size_t realigned_bytes = 0;
 };
 
 struct DevState {
@@ -234,19 +237,25 @@ const char* kPairPathNames[2][2] = {
 };
 
 int check_common(const void* A, const void* B, const void* C, int M, int N, int K, long long lda,
-                 long long ldb, long long ldc, float alpha) {
+                 long long ldb, long long ldc, float alpha, size_t elem = 1) {
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_DIM;
   if (M == 0 || N == 0) return GEMM_OK;
   if (ldc < N || (K > 0 && (lda < K || ldb < N))) return GEMM_ERR_LD;
   if (C == nullptr) return GEMM_ERR_NULL;
   if (K > 0 && alpha != 0.0f && (A == nullptr || B == nullptr)) return GEMM_ERR_NULL;
+  // element pointers must at least be aligned to their element size
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+                         reinterpret_cast<uintptr_t>(C)) & (elem - 1);
+  if (mis) return GEMM_ERR_ARG;
   return GEMM_OK;
 }
+
+thread_local char t_path_buf[96];
 
 int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
                     long long lda, long long ldb, long long ldc, float alpha, float beta,
                     cudaStream_t stream) {
-  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha)) return rc;
+  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha, 2)) return rc;
   if (M == 0 || N == 0) {
     t_last_path = "noop";
     return GEMM_OK;
@@ -263,6 +272,40 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
 
   const int force = g_force_path.load();
   const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+  const bool a_tma = aligned16(A) && (lda * 2) % 16 == 0;
+  const bool b_tma = aligned16(B) && (ldb * 2) % 16 == 0;
+  // An operand whose rows break the 16-byte rule is first copied into an
+  // aligned layout (one bandwidth-bound pass) unless the predicated-load path
+  // is forced or the copy would be very large.
+  const char* how = "";
+  if ((!a_tma || !b_tma) && force != 2) {
+    const long long lda2 = (K + 7) / 8 * 8, ldb2 = (N + 7) / 8 * 8;
+    const size_t a_bytes = a_tma ? 0 : static_cast<size_t>(M) * lda2 * 2;
+    const size_t b_bytes = b_tma ? 0 : static_cast<size_t>(K) * ldb2 * 2;
+    if (a_bytes + b_bytes <= (static_cast<size_t>(1) << 31)) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      StreamWs& w = d->ws[reinterpret_cast<uintptr_t>(stream)];
+      if (int rc = ensure_buffer(&w.realigned, &w.realigned_bytes, a_bytes + b_bytes + 256))
+        return rc;
+      uint16_t* buf = static_cast<uint16_t*>(w.realigned);
+      if (!a_tma) {
+        if (launch_realign_f16(A, lda, buf, lda2, M, K, scale_grid(*d, 1ll * M * lda2 / 8),
+                               stream) != cudaSuccess)
+          return GEMM_ERR_CUDA;
+        A = buf;
+        lda = lda2;
+        buf += (a_bytes / 2 + 127) / 128 * 128;   // keep the next copy 256-byte aligned
+      }
+      if (!b_tma) {
+        if (launch_realign_f16(B, ldb, buf, ldb2, K, N, scale_grid(*d, 1ll * K * ldb2 / 8),
+                               stream) != cudaSuccess)
+          return GEMM_ERR_CUDA;
+        B = buf;
+        ldb = ldb2;
+      }
+      how = ".realigned";
+    }
+  }
   const bool ab_tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
   // A TMA store writes whole 16-byte pieces of a row: when N is not a multiple
   // of 8 halves it would also write the elements just past column N (measured
@@ -296,9 +339,11 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   int splits = 1;
   const int fs = g_force_splits.load();
   if (force == 3 || (force == 0 && tiles * 2 <= d->sm_count && a.kb_total >= 8)) {
+    // as many K slices as fit in ONE wave of CTAs (a second, partial wave would
+    // double the time of these bandwidth-bound shapes)
     splits = fs > 0 ? fs
                     : static_cast<int>(std::min<long long>(
-                          {(d->sm_count + tiles - 1) / tiles, static_cast<long long>(a.kb_total / 4),
+                          {std::max(1ll, d->sm_count / tiles), static_cast<long long>(a.kb_total / 4),
                            16ll}));
     splits = std::max(1, std::min(splits, a.kb_total));
   }
@@ -371,14 +416,18 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
   if (pair) {
     const int grid = 2 * static_cast<int>(std::min<long long>(a.num_units, workers));
-    t_last_path = a.tail_splits > 1 ? kPairPathNames[epi][1] : kPairPathNames[epi][0];
+    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s",
+             a.tail_splits > 1 ? kPairPathNames[epi][1] : kPairPathNames[epi][0], how);
+    t_last_path = t_path_buf;
     if (launch_gemm_f16_tc_pair(epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     return GEMM_OK;
   }
   const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  t_last_path = a.tail_splits > 1 ? kTailPathNames[bi][load][epi] : kPathNames[bi][load][epi];
+  snprintf(t_path_buf, sizeof(t_path_buf), "%s%s",
+           a.tail_splits > 1 ? kTailPathNames[bi][load][epi] : kPathNames[bi][load][epi], how);
+  t_last_path = t_path_buf;
   if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
   if (splits > 1) {
@@ -392,7 +441,7 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
 
 int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int K, long long lda,
                      long long ldb, long long ldc, float alpha, float beta, cudaStream_t stream) {
-  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha)) return rc;
+  if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha, 4)) return rc;
   if (M == 0 || N == 0) {
     t_last_path = "noop";
     return GEMM_OK;
@@ -600,6 +649,7 @@ int gemm_release(void) {
     for (auto& kv : d.ws) {
       if (kv.second.ptr) cudaFree(kv.second.ptr);
       if (kv.second.counters) cudaFree(kv.second.counters);
+      if (kv.second.realigned) cudaFree(kv.second.realigned);
     }
     d.ws.clear();
   }

@@ -67,6 +67,11 @@ cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int split
                                      long long ldc, int M, int N, float alpha, float beta,
                                      int grid, cudaStream_t stream);
 
+// Copies a rows x cols half matrix with any leading dimension and alignment
+// into a 16-byte-aligned one with ldd = cols rounded up to 8 (zero padding).
+cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
+                               int rows, int cols, int grid, cudaStream_t stream);
+
 // C := beta * C (C := 0 when beta == 0): the alpha == 0 / K == 0 case.
 cudaError_t launch_scale_f16(uint16_t* C, long long ldc, int M, int N, float beta, int grid,
                              cudaStream_t stream);

@@ -84,6 +84,9 @@ extern "C" int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uin
   if (ldc < N || (K > 0 && (lda < K || ldb < N))) return GEMM_ERR_LD;
   if (C == nullptr) return GEMM_ERR_NULL;
   if (K > 0 && alpha != 0.0f && (A == nullptr || B == nullptr)) return GEMM_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 1u)
+    return GEMM_ERR_ARG;   // half pointers must be 2-byte aligned
 
   int sm_count = 0;
   DeviceStatus* status = nullptr;
@@ -122,7 +125,7 @@ extern "C" int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uin
   int s = splits;
   if (s == 0)
     s = static_cast<int>(std::min<long long>(
-        {(sm_count + tiles - 1) / tiles, static_cast<long long>(a.kb_total / 4), 16ll}));
+        {std::max(1ll, sm_count / tiles), static_cast<long long>(a.kb_total / 4), 16ll}));
   s = std::max(1, std::min(s, a.kb_total));
   a.kb_per_split = (a.kb_total + s - 1) / s;
   s = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;   // no empty slice

@@ -20,8 +20,12 @@
  *              beta == 0) and written.  C must not overlap A or B (not
  *              checked; the result is undefined).
  *   Layout     row-major; the non-_ld forms mean lda = K, ldb = N, ldc = N.
- *              Any alignment is accepted: pointers or leading dimensions that
- *              are not 16-byte aligned are served by a slower path.
+ *              Pointers must be aligned to their element (2 bytes for half,
+ *              4 for float; else GEMM_ERR_ARG).  Beyond that any alignment is
+ *              accepted: a half operand whose rows are not 16-byte aligned is
+ *              first copied into an aligned scratch layout (or, with
+ *              gemm_force_path(2), loaded with predicated element loads), and
+ *              such a C is written with predicated element stores.
  *   Types      half = IEEE binary16 (bits in a uint16_t); float = binary32.
  *   Numerics   products accumulate in fp32; the epilogue alpha*acc + beta*c
  *              is evaluated in fp32 and rounded once, to nearest even, to the
@@ -37,9 +41,10 @@
  *              different streams that write the same C race.
  *   Scratch    some shapes split K over several thread blocks and need an
  *              fp32 workspace: small M*N with a long K, and the tiles of the
- *              last, partial wave when the tiles outnumber the SMs.  The
- *              library owns it, per device and stream, grows it on first need
- *              (that call may allocate device memory) and frees it in
+ *              last, partial wave when the tiles outnumber the SMs; unaligned
+ *              half operands need an aligned copy.  The library owns this
+ *              scratch, per device and stream, grows it on first need (that
+ *              call may allocate device memory) and frees it in
  *              gemm_release().
  *   Errors     a negative return code (below) and nothing enqueued, except
  *              GEMM_ERR_CUDA, which reports a failed launch.  Kernels never
