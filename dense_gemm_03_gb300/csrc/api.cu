@@ -271,7 +271,10 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
 
   const int force = g_force_path.load();
-  const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+  int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+  // A single row of 256-wide tiles that cannot fill the SMs: narrower tiles
+  // give more of them, so fewer K slices are needed.
+  if (bn == 256 && M <= kBM && 1ll * ((N + 255) / 256) * 2 <= d->sm_count) bn = 128;
   const bool a_tma = aligned16(A) && (lda * 2) % 16 == 0;
   const bool b_tma = aligned16(B) && (ldb * 2) % 16 == 0;
   // An operand whose rows break the 16-byte rule is first copied into an
@@ -372,14 +375,26 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   a.dp_tiles = static_cast<int>(units_tiles);
   a.tail_splits = 1;
   a.tail_kb_per_split = a.kb_total;
+  const char* cut = "";
   if (splits > 1) {
-    epi = kEpiPartial;
-    a.ws_ld = (N + 3) / 4 * 4;
-    const size_t need = sizeof(float) * static_cast<size_t>(splits) * M * a.ws_ld;
+    // Every tile is cut into `splits` K slices: each slice publishes fp32
+    // partial sums and the last one of a tile to finish adds them up (in slice
+    // order) and runs the epilogue -- no second kernel.
+    a.dp_tiles = 0;
+    a.tail_splits = splits;
+    a.tail_kb_per_split = a.kb_per_split;
+    a.kb_per_split = a.kb_total;
+    splits = 1;
+    a.splits = 1;
+    const size_t need = sizeof(float) * static_cast<size_t>(tiles) * a.tail_splits * kBM * bn;
     std::lock_guard<std::mutex> lk(g_mu);
     StreamWs* w = nullptr;
-    if (int rc = stream_scratch(d, stream, need, 0, &w)) return rc;
-    a.ws = static_cast<float*>(w->ptr);
+    if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tiles) * 8, &w)) return rc;
+    a.tail_ws = static_cast<float*>(w->ptr);
+    a.tail_counters = static_cast<unsigned long long*>(w->counters);
+    a.epoch = ++w->epoch;
+    if (a.epoch == 0) a.epoch = ++w->epoch;
+    cut = ".splitk";
   } else if (force != 5) {
     // Balance the last, partial wave: cut its tiles along K.
     int ts = plan_tail_splits(units_tiles, workers, a.kb_total);
@@ -425,17 +440,13 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
   const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  snprintf(t_path_buf, sizeof(t_path_buf), "%s%s",
-           a.tail_splits > 1 ? kTailPathNames[bi][load][epi] : kPathNames[bi][load][epi], how);
+  snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s",
+           (a.tail_splits > 1 && a.dp_tiles > 0) ? kTailPathNames[bi][load][epi]
+                                                  : kPathNames[bi][load][epi],
+           cut, how);
   t_last_path = t_path_buf;
   if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
-  if (splits > 1) {
-    const long long groups = 1ll * M * ((N + 3) / 4);
-    if (launch_splitk_reduce_f16(a.ws, a.ws_ld, splits, C, ldc, M, N, alpha, beta,
-                                 scale_grid(*d, groups), stream) != cudaSuccess)
-      return GEMM_ERR_CUDA;
-  }
   return GEMM_OK;
 }
 

@@ -280,6 +280,25 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* 
   }
 }
 
+// Adds two slices' partial sums (slice a first, then b) with all 16 loads in
+// flight together.
+__device__ __forceinline__ void add_partials2(uint32_t (&acc)[32], const float4* a,
+                                              const float4* b) {
+  float4 va[8], vb[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    va[i] = __ldcg(a + i * BM);
+    vb[i] = __ldcg(b + i * BM);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    acc[4 * i] = __float_as_uint((__uint_as_float(acc[4 * i]) + va[i].x) + vb[i].x);
+    acc[4 * i + 1] = __float_as_uint((__uint_as_float(acc[4 * i + 1]) + va[i].y) + vb[i].y);
+    acc[4 * i + 2] = __float_as_uint((__uint_as_float(acc[4 * i + 2]) + va[i].z) + vb[i].z);
+    acc[4 * i + 3] = __float_as_uint((__uint_as_float(acc[4 * i + 3]) + va[i].w) + vb[i].w);
+  }
+}
+
 template <int BN, int LOAD, int EPI, bool PAIR>
 __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -621,7 +640,10 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             const float4* part = tail_partials(p, tail_part, 0, BN) + 32 * q + lane + cq0 * BM;
             const long long slice = static_cast<long long>(BN / 4) * BM;
             add_partials(cur, part, true);
-            for (int s2 = 1; s2 < p.tail_splits; ++s2) add_partials(cur, part + s2 * slice, false);
+            int s2 = 1;
+            for (; s2 + 1 < p.tail_splits; s2 += 2)
+              add_partials2(cur, part + s2 * slice, part + (s2 + 1) * slice);
+            if (s2 < p.tail_splits) add_partials(cur, part + s2 * slice, false);
           }
           if (EPI == kEpiPartial) {
             if (row < p.M) {
@@ -662,14 +684,18 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           } else {  // kEpiManual: C through shared memory with predicated accesses
             uint8_t* const sptr = sptr0;
             const int col = col0 + lane;   // this lane's column in the row-wise passes
+            const bool col_ok = col < p.N;
+            const uint16_t* __restrict__ cbase = p.C + static_cast<long long>(row0) * p.ldc + col;
             if (has_c) {
-              for (int r = 0; r < 32; ++r) {
-                const int rr = row0 + r;
-                const uint16_t v = (rr < p.M && col < p.N)
-                                       ? p.C[static_cast<long long>(rr) * p.ldc + col]
-                                       : static_cast<uint16_t>(0);
-                *reinterpret_cast<uint16_t*>(sptr + sw64_elem(r, lane)) = v;
-              }
+              // all 32 loads are issued before any is written to shared memory
+              uint16_t v[32];
+#pragma unroll
+              for (int r = 0; r < 32; ++r)
+                v[r] = (row0 + r < p.M && col_ok) ? __ldg(cbase + static_cast<long long>(r) * p.ldc)
+                                                  : static_cast<uint16_t>(0);
+#pragma unroll
+              for (int r = 0; r < 32; ++r)
+                *reinterpret_cast<uint16_t*>(sptr + sw64_elem(r, lane)) = v[r];
               __syncwarp();
             }
 #pragma unroll
@@ -681,12 +707,14 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
                   epilogue8(cur + 8 * g, cv, has_c, p.alpha, p.beta);
             }
             __syncwarp();
-            for (int r = 0; r < 32; ++r) {
-              const int rr = row0 + r;
-              if (rr < p.M && col < p.N)
-                p.C[static_cast<long long>(rr) * p.ldc + col] =
-                    *reinterpret_cast<const uint16_t*>(sptr + sw64_elem(r, lane));
-            }
+            uint16_t o[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              o[r] = *reinterpret_cast<const uint16_t*>(sptr + sw64_elem(r, lane));
+            uint16_t* const cout = p.C + static_cast<long long>(row0) * p.ldc + col;
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              if (row0 + r < p.M && col_ok) cout[static_cast<long long>(r) * p.ldc] = o[r];
             __syncwarp();
           }
           if (more && !t.tail) tmem_wait_regs(nxt);
