@@ -25,7 +25,7 @@
 #include <mutex>
 #include <unordered_map>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -50,6 +50,8 @@ struct StreamWs {
   unsigned int epoch = 0;       // launches that used the counters
   void* realigned = nullptr;    // aligned copies of unaligned operands
   size_t realigned_bytes = 0;
+  void* split = nullptr;        // big/small tf32 parts of fp32 operands
+  size_t split_bytes = 0;
 };
 
 struct DevState {
@@ -201,6 +203,21 @@ int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long lon
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int make_map_f32(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
+                 int box_cols, int box_rows) {
+  EncodeTiledFn enc = nullptr;
+  if (int rc = encode_fn(&enc)) return rc;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -465,8 +482,65 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
                ? GEMM_OK
                : GEMM_ERR_CUDA;
   }
-  const bool vec = g_force_path.load() != 4 && aligned16(A) && aligned16(B) && aligned16(C) &&
-                   lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0;
+  const int force = g_force_path.load();
+  // 3xTF32 on the tensor cores for shapes with enough work to fill CTA pairs.
+  if (force != 4 && force != 7 && (force == 8 || (M >= 256 && N >= 256 && K >= 64))) {
+    const int pairs = sgemm_3xtf32_max_pairs();
+    const long long K2 = (K + 3) / 4 * 4;
+    const size_t a_part = static_cast<size_t>(M) * K2 * 4, b_part = static_cast<size_t>(N) * K2 * 4;
+    if (pairs > 0 && 2 * (a_part + b_part) <= (static_cast<size_t>(16) << 30)) {
+      float* buf = nullptr;
+      {
+        std::lock_guard<std::mutex> lk(g_mu);
+        StreamWs& w = d->ws[reinterpret_cast<uintptr_t>(stream)];
+        if (int rc = ensure_buffer(&w.split, &w.split_bytes, 2 * (a_part + b_part) + 1024))
+          return rc;
+        buf = static_cast<float*>(w.split);
+      }
+      float* Ab = buf;
+      float* As = Ab + a_part / 4;
+      float* Bb = As + a_part / 4;
+      float* Bs = Bb + b_part / 4;
+      const long long ttiles = ((K2 + 31) / 32) * ((N + 31) / 32);
+      if (launch_split_tf32(A, lda, Ab, As, K2, M, K, scale_grid(*d, 1ll * M * K2 / 4), stream) !=
+              cudaSuccess ||
+          launch_split_tf32_t(B, ldb, Bb, Bs, K2, K, N,
+                              static_cast<int>(std::min<long long>(ttiles, 16ll * d->sm_count)),
+                              stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      CUtensorMap mAb{}, mAs{}, mBb{}, mBs{};
+      if (int rc = make_map_f32(&mAb, Ab, M, K, K2, 32, 128)) return rc;
+      if (int rc = make_map_f32(&mAs, As, M, K, K2, 32, 128)) return rc;
+      if (int rc = make_map_f32(&mBb, Bb, N, K, K2, 32, 128)) return rc;
+      if (int rc = make_map_f32(&mBs, Bs, N, K, K2, 32, 128)) return rc;
+      Tf32Args t{};
+      t.Ab = Ab;
+      t.As = As;
+      t.Bb = Bb;
+      t.Bs = Bs;
+      t.C = C;
+      t.M = M;
+      t.N = N;
+      t.K = K;
+      t.ldc = ldc;
+      t.alpha = alpha;
+      t.beta = beta;
+      t.tiles_m = (M + 255) / 256;
+      t.tiles_n = (N + 255) / 256;
+      t.kb_total = (K + 31) / 32;
+      t.num_units = t.tiles_m * t.tiles_n;
+      t.group_m = 8;
+      t.vec_c = aligned16(C) && ldc % 4 == 0;
+      t.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+      t.status = d->status;
+      const int grid = 2 * std::min(t.num_units, pairs);
+      t_last_path = "f32.3xtf32.pair";
+      return launch_sgemm_3xtf32(mAb, mAs, mBb, mBs, t, grid, stream) == cudaSuccess ? GEMM_OK
+                                                                                     : GEMM_ERR_CUDA;
+    }
+  }
+  const bool vec = force != 4 && aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 &&
+                   ldb % 4 == 0 && ldc % 4 == 0;
   SgemmArgs s{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta};
   t_last_path = vec ? "f32.ffma.vec" : "f32.ffma.scalar";
   return launch_sgemm_ffma(vec, s, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -594,7 +668,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 6) return GEMM_ERR_ARG;
+  if (path < 0 || path > 8) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 
@@ -661,6 +735,7 @@ int gemm_release(void) {
       if (kv.second.ptr) cudaFree(kv.second.ptr);
       if (kv.second.counters) cudaFree(kv.second.counters);
       if (kv.second.realigned) cudaFree(kv.second.realigned);
+      if (kv.second.split) cudaFree(kv.second.split);
     }
     d.ws.clear();
   }

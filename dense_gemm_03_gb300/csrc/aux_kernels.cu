@@ -3,6 +3,7 @@
 //     in ascending order (deterministic), fp32 arithmetic, one rounding;
 //   * realignment of an operand whose rows are not 16-byte aligned into an
 //     aligned copy, so that the tensor-core kernel can load it by TMA;
+//   * the big/small tf32 split of fp32 operands for the 3xTF32 SGEMM;
 //   * scale-only update for alpha == 0 or K == 0: C := beta*C (C := 0 when
 //     beta == 0, without reading C -- the convention of the "LeetGPU GEMM T4"
 //     WMMA sections and the "advanced SGEMM" page for beta == 0).
@@ -129,7 +130,110 @@ __global__ void realign_f16_kernel(const uint16_t* __restrict__ src, long long l
   }
 }
 
+// tf32 value nearest to x (ties away from zero), as fp32 bits with the low 13
+// bits clear.
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// big = x with the low 13 mantissa bits cleared (exactly representable in
+// tf32), small = tf32(x - big); x = big + small up to about 2^-22 |x|.
+// Non-finite x: big carries it, small = 0.
+__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
+  const uint32_t bits = __float_as_uint(x);
+  if (isnan(x)) {
+    big = __uint_as_float(0x7FFFE000u);
+    small = 0.0f;
+  } else if (isinf(x)) {
+    big = x;
+    small = 0.0f;
+  } else {
+    big = __uint_as_float(bits & 0xFFFFE000u);
+    small = round_tf32(x - big);
+  }
+}
+
+// Splits a rows x cols fp32 matrix (any leading dimension, 4-byte aligned)
+// into big and small parts stored densely with leading dimension ldd
+// (ldd % 4 == 0, zero padding), one thread per 4 output columns.
+__global__ void split_tf32_kernel(const float* __restrict__ src, long long lds,
+                                  float* __restrict__ big, float* __restrict__ small, long long ldd,
+                                  int rows, int cols) {
+  const long long groups = ldd / 4;
+  const long long total = static_cast<long long>(rows) * groups;
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (lds & 3) == 0;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(g / groups);
+    const int c0 = static_cast<int>(g % groups) * 4;
+    const float* p = src + static_cast<long long>(r) * lds + c0;
+    float x[4];
+    if (vec && c0 + 4 <= cols) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = (c0 + i < cols) ? __ldg(p + i) : 0.0f;
+    }
+    float b[4], s[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) split_tf32(x[i], b[i], s[i]);
+    const long long o = static_cast<long long>(r) * ldd + c0;
+    *reinterpret_cast<float4*>(big + o) = make_float4(b[0], b[1], b[2], b[3]);
+    *reinterpret_cast<float4*>(small + o) = make_float4(s[0], s[1], s[2], s[3]);
+  }
+}
+
+// Transposing split: src is rows x cols (row-major, 4-byte aligned); writes
+// big/small parts of src^T, i.e. dst[c][r] for c < cols, r < rows, with
+// leading dimension ldd (>= rows, % 4 == 0; zero padding in [rows, ldd)).
+// 32 x 32 tiles through shared memory so that both sides are coalesced.
+__global__ void split_tf32_t_kernel(const float* __restrict__ src, long long lds,
+                                    float* __restrict__ big, float* __restrict__ small,
+                                    long long ldd, int rows, int cols) {
+  __shared__ float tile[32][33];
+  const int tiles_c = (cols + 31) / 32;
+  const int tiles_r = static_cast<int>((ldd + 31) / 32);
+  const long long ntiles = static_cast<long long>(tiles_r) * tiles_c;
+  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int r0 = static_cast<int>(t / tiles_c) * 32, c0 = static_cast<int>(t % tiles_c) * 32;
+    // load: thread (x, y) reads rows r0 + y + 8i, column c0 + x
+    for (int i = 0; i < 4; ++i) {
+      const int rr = r0 + threadIdx.y + 8 * i, cc = c0 + threadIdx.x;
+      tile[threadIdx.y + 8 * i][threadIdx.x] =
+          (rr < rows && cc < cols) ? __ldg(src + static_cast<long long>(rr) * lds + cc) : 0.0f;
+    }
+    __syncthreads();
+    // store: thread (x, y) writes dst row c0 + y + 8i, column r0 + x
+    for (int i = 0; i < 4; ++i) {
+      const int cc = c0 + threadIdx.y + 8 * i, rr = r0 + threadIdx.x;
+      if (cc < cols && rr < ldd) {
+        float b, sm;
+        split_tf32(tile[threadIdx.x][threadIdx.y + 8 * i], b, sm);
+        const long long o = static_cast<long long>(cc) * ldd + rr;
+        big[o] = b;
+        small[o] = sm;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_split_tf32_t(const float* src, long long lds, float* big, float* small,
+                                long long ldd, int rows, int cols, int grid, cudaStream_t stream) {
+  split_tf32_t_kernel<<<grid, dim3(32, 8), 0, stream>>>(src, lds, big, small, ldd, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_tf32(const float* src, long long lds, float* big, float* small,
+                              long long ldd, int rows, int cols, int grid, cudaStream_t stream) {
+  split_tf32_kernel<<<grid, 256, 0, stream>>>(src, lds, big, small, ldd, rows, cols);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
                                int rows, int cols, int grid, cudaStream_t stream) {

@@ -72,6 +72,39 @@ cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int split
 cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
                                int rows, int cols, int grid, cudaStream_t stream);
 
+// big/small tf32 split of an fp32 operand into dense copies (ldd % 4 == 0).
+cudaError_t launch_split_tf32(const float* src, long long lds, float* big, float* small,
+                              long long ldd, int rows, int cols, int grid, cudaStream_t stream);
+
+// The same split of the TRANSPOSE of a rows x cols matrix (dst is cols x ldd).
+cudaError_t launch_split_tf32_t(const float* src, long long lds, float* big, float* small,
+                                long long ldd, int rows, int cols, int grid, cudaStream_t stream);
+
+// 3xTF32 SGEMM on CTA pairs: C = alpha*(Ab*Bb + Ab*Bs + As*Bb) + beta*C with
+// the split operands dense and K-contiguous: A parts M x roundup(K,4), B parts
+// transposed, N x roundup(K,4).
+struct Tf32Args {
+  const float* Ab;
+  const float* As;
+  const float* Bb;
+  const float* Bs;
+  float* C;
+  int M, N, K;
+  long long ldc;
+  float alpha, beta;
+  int tiles_m, tiles_n;   // 256 x 256 pair tiles
+  int kb_total;           // ceil(K / 32)
+  int num_units;
+  int group_m;
+  bool vec_c;             // C 16-byte aligned with ldc % 4 == 0
+  unsigned long long wait_limit_ns;
+  DeviceStatus* status;
+};
+cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,
+                                const CUtensorMap& tmBb, const CUtensorMap& tmBs,
+                                const Tf32Args& args, int grid, cudaStream_t stream);
+int sgemm_3xtf32_max_pairs();
+
 // C := beta * C (C := 0 when beta == 0): the alpha == 0 / K == 0 case.
 cudaError_t launch_scale_f16(uint16_t* C, long long ldc, int M, int N, float beta, int grid,
                              cudaStream_t stream);

@@ -1,0 +1,370 @@
+// sgemm_3xtf32.cu -- fp32 SGEMM on the tensor cores with three tf32 products.
+//
+// C := alpha*A*B + beta*C in fp32.  Each operand is split (by a pre-pass) into
+// a tf32 "big" part (low 13 mantissa bits cleared) and a tf32 "small" part
+// (the remainder, rounded to tf32), so that A = Ab + As and B = Bb + Bs up to
+// about 2^-22 relative.  The product keeps the three largest terms,
+//     A*B ~= Ab*Bb + Ab*Bs + As*Bb;
+// the dropped As*Bs term is below 2^-20 of |A||B|.
+//
+// Accumulation.  The tensor core's fp32 accumulation does not round to
+// nearest: summed over a long K in tensor memory, the result drifts toward
+// zero by a bias that grows like K*|C| (measured: at K = 16384 it exceeds the
+// fp32 error bound).  So the MMA accumulates only chunks of 128 along K into
+// tensor memory (alternating between two buffers), and the epilogue warps add
+// each chunk into fp32 registers with ordinary round-to-nearest adds; the
+// result is then as accurate as the FFMA kernel's.
+//
+// Kernel: CTA pairs (clusters of 2) share tcgen05.mma.cta_group::2.kind::tf32
+// with M = 256 (128 rows of A in each CTA) and N = 256 (each CTA stages 128 of
+// the columns of B); per 32-deep k-block each CTA stages Ab, As (128 x 32) and
+// Bb, Bs (128 columns x 32) by TMA into a 3-stage ring (64 KB per stage), and
+// the leader issues 3 MMAs per 8-deep K step.  Warp roles, barriers and the
+// epilogue (8 warps, fp32 written straight from registers) follow the fp16
+// tensor-core kernel.  Both operands are K-major (the pre-pass stores the B
+// parts transposed): 128-byte swizzle, 32 floats per row, SBO 1024 B.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int BM = 128;                     // rows per CTA
+constexpr int BN = 256;                     // pair tile width
+constexpr int BK = 32;                      // floats per k-block (one 128-byte row)
+constexpr int kMmaK = 8;                    // K of one kind::tf32 MMA
+constexpr int kATile = BM * BK * 4;         // 16 KB per part
+constexpr int kBCols = BN / 2;              // B columns staged by each CTA
+constexpr int kBTile = kBCols * BK * 4;     // 16 KB per part
+constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
+constexpr int kStages = 3;
+constexpr int kEpiWarps = 8;
+constexpr int kCols = BN / 2;               // accumulator columns per epilogue thread
+constexpr int kChunkKb = 4;                 // k-blocks per TMEM accumulation chunk (K = 128)
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kTmemCols = 2 * BN;
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1;   // full, empty, accf, acce, done, tmem_free
+constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
+constexpr int kSmemAlloc = kTmemPtrOff + 16 + 1024;
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, DeviceStatus* st, int where) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return;
+    if (globaltimer_ns() - t0 > kDrainLimitNs) {
+      if (atomicCAS(&st->code, 0, kStatusTimeout) == 0) st->where = where;
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_wait_regs32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAb,
+                        const __grid_constant__ CUtensorMap tmAs,
+                        const __grid_constant__ CUtensorMap tmBb,
+                        const __grid_constant__ CUtensorMap tmBs, const Tf32Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw_addr);
+  const int warp = warp_id_uniform();
+  const int lane = static_cast<int>(lane_id());
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int worker = static_cast<int>(cluster_id_x());
+  const int nworkers = static_cast<int>(cluster_count_x());
+
+  const uint32_t bars = base + kBarOff;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * kStages + b); };
+  auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * kStages + 2 + b); };
+  const uint32_t done_bar = bars + 8u * (2 * kStages + 4);
+  const uint32_t tmem_free_bar = bars + 8u * (2 * kStages + 5);
+  auto stage = [&](int s) { return base + static_cast<uint32_t>(s * kStageBytes); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1u);
+      mbar_init(empty_bar(s), 1u);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1u);
+      mbar_init(acce_bar(b), 2u * kEpiWarps);
+    }
+    mbar_init(done_bar, 1u);
+    mbar_init(tmem_free_bar, static_cast<uint32_t>(kEpiWarps));
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(base + kTmemPtrOff, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmAb);
+    prefetch_tensormap(&tmAs);
+    prefetch_tensormap(&tmBb);
+    prefetch_tensormap(&tmBs);
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + kTmemPtrOff);
+  const unsigned long long limit = p.wait_limit_ns;
+  DeviceStatus* const st = p.status;
+
+  // pair tile -> (m0 of this CTA, n0); groups of group_m tile-rows share B in L2
+  auto tile_of = [&](int u, int& m0, int& n0) {
+    const int group = p.group_m * p.tiles_n;
+    const int g = u / group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.tiles_m - first_m, p.group_m);
+    const int r = u - g * group;
+    m0 = (first_m + r % gm) * (2 * BM) + static_cast<int>(rank) * BM;
+    n0 = (r / gm) * BN;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int u = worker; ok && u < p.num_units; u += nworkers) {
+        int m0, n0;
+        tile_of(u, m0, n0);
+        for (int kb = 0; kb < p.kb_total; ++kb) {
+          if (!wait_parity(empty_bar(s), phase ^ 1u, limit, st, 21)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = map_to_cta(full_bar(s), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+          const uint32_t sa = stage(s);
+          tma_load_2d_pair(sa, &tmAb, fb, kb * BK, m0);
+          tma_load_2d_pair(sa + kATile, &tmAs, fb, kb * BK, m0);
+          const int nb = n0 + static_cast<int>(rank) * kBCols;
+          tma_load_2d_pair(sa + 2 * kATile, &tmBb, fb, kb * BK, nb);
+          tma_load_2d_pair(sa + 2 * kATile + kBTile, &tmBs, fb, kb * BK, nb);
+          ++issued;
+          if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      const uint32_t n = issued < static_cast<uint32_t>(kStages) ? issued : kStages;
+      for (uint32_t i = issued - n; i < issued; ++i)
+        drain(empty_bar(static_cast<int>(i % kStages)), (i / kStages) & 1u, st, 22);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    // Chunks of kChunkKb k-blocks alternate between the two TMEM buffers; each
+    // chunk starts a fresh accumulation and the epilogue folds it into its
+    // fp32 register accumulators.
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc(2u, 2 * BM, BN, 0u, 0u);
+      int s = 0;
+      uint32_t phase = 0, chunk = 0;
+      bool ok = true;
+      for (int u = worker; ok && u < p.num_units; u += nworkers) {
+        for (int kc = 0; ok && kc < p.kb_total; kc += kChunkKb, ++chunk) {
+          const uint32_t buf = chunk & 1u, use = chunk >> 1;
+          if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 23)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + buf * BN;
+          const int kend = min(kc + kChunkKb, p.kb_total);
+          for (int kb = kc; kb < kend; ++kb) {
+            if (!wait_parity(full_bar(s), phase, limit, st, 24)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_big = stage(s), a_small = a_big + kATile;
+            const uint32_t b_big = a_big + 2 * kATile, b_small = b_big + kBTile;
+#pragma unroll
+            for (int kk = 0; kk < BK / kMmaK; ++kk) {
+              const uint64_t adb = smem_desc_sw128(a_big + kk * (kMmaK * 4), 16u, 1024u);
+              const uint64_t ads = smem_desc_sw128(a_small + kk * (kMmaK * 4), 16u, 1024u);
+              const uint64_t bdb = smem_desc_sw128(b_big + kk * (kMmaK * 4), 16u, 1024u);
+              const uint64_t bds = smem_desc_sw128(b_small + kk * (kMmaK * 4), 16u, 1024u);
+              // the two small terms first, then the big one
+              mma_tf32_ss_pair(d, ads, bdb, idesc, (kb > kc || kk > 0) ? 1u : 0u);
+              mma_tf32_ss_pair(d, adb, bds, idesc, 1u);
+              mma_tf32_ss_pair(d, adb, bdb, idesc, 1u);
+            }
+            mma_commit_pair_multicast(empty_bar(s), 3);
+            if (++s == kStages) {
+              s = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair_multicast(accf_bar(buf), 3);
+        }
+      }
+      mma_commit_pair_multicast(done_bar, 3);
+      drain(done_bar, 0u, st, 25);
+      const uint32_t first = chunk > 2u ? chunk - 2u : 0u;
+      for (uint32_t j = first; j < chunk; ++j) drain(acce_bar(j & 1u), (j >> 1) & 1u, st, 26);
+    } else if (lane == 0) {
+      drain(done_bar, 0u, st, 25);
+    }
+    if (lane == 0) drain(tmem_free_bar, 0u, st, 27);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Warp (q, h) owns TMEM lanes 32q..32q+31 (rows) and columns h*128..+127;
+    // each thread keeps its row's 128 sums in fp32 registers.
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int h = ew >> 2;
+    const bool has_c = p.beta != 0.0f;
+    uint32_t chunk = 0;
+    bool ok = true;
+    for (int u = worker; ok && u < p.num_units; u += nworkers) {
+      int m0, n0;
+      tile_of(u, m0, n0);
+      const int row0 = m0 + 32 * q;
+      const int row = row0 + lane;
+      const int colw = n0 + h * kCols;
+      const bool active = row0 < p.M && colw < p.N;   // warp-uniform
+      float acc[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
+      for (int kc = 0; kc < p.kb_total; kc += kChunkKb, ++chunk) {
+        const uint32_t buf = chunk & 1u, use = chunk >> 1;
+        if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 28)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (active) {
+          const uint32_t tbase =
+              tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * kCols;
+#pragma unroll
+          for (int k = 0; k < kCols / 32; ++k) {
+            uint32_t t[32];
+            tmem_ld_32x32b_x32(tbase + 32 * k, t);
+            tmem_wait_regs32(t);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * k + j] += __uint_as_float(t[j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(buf), 0));
+      }
+      if (!ok || !active || row >= p.M) continue;
+      float* crow = p.C + static_cast<long long>(row) * p.ldc;
+#pragma unroll
+      for (int g = 0; g < kCols / 4; ++g) {
+        const int col = colw + 4 * g;
+        if (col >= p.N) break;
+        float o[4] = {acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]};
+        if (p.vec_c && col + 4 <= p.N) {
+          float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (has_c) c = __ldcs(reinterpret_cast<const float4*>(crow + col));
+          const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[j] = has_c ? fmaf(p.alpha, o[j], p.beta * cv[j]) : p.alpha * o[j];
+          __stcs(reinterpret_cast<float4*>(crow + col), make_float4(o[0], o[1], o[2], o[3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (col + j < p.N)
+              crow[col + j] =
+                  has_c ? fmaf(p.alpha, o[j], p.beta * crow[col + j]) : p.alpha * o[j];
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tmem_free_bar);
+  }
+  __syncwarp();
+  cluster_sync();
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+cudaError_t configure(int dev) {
+  static bool done[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        sgemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int sgemm_3xtf32_max_pairs() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || configure(dev) != cudaSuccess) return 0;
+  static int cached[64] = {};
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, sgemm_3xtf32_kernel, &cfg) != cudaSuccess) return 0;
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,
+                                const CUtensorMap& tmBb, const CUtensorMap& tmBs,
+                                const Tf32Args& args, int grid, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = configure(dev)) != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, tmAb, tmAs, tmBb, tmBs, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -30,7 +30,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "internal.h"
 
 namespace gb300 {

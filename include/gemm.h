@@ -87,7 +87,12 @@ int gemm_f16_ld(const uint16_t* A, const uint16_t* B, uint16_t* C,
                 int M, int N, int K, int lda, int ldb, int ldc,
                 float alpha, float beta, cudaStream_t stream);
 
-/* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 everywhere. */
+/* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 operands and
+ * result.  Shapes of at least 256 x 256 x 64 run on the tensor cores as three
+ * tf32 products of split operands (A = Ab + As, B = Bb + Bs; the As*Bs term,
+ * about 2^-22 of |A||B|, is dropped) with fp32 accumulation, after a pre-pass
+ * that writes the split operands to library-owned scratch; smaller shapes use
+ * an FFMA kernel (exact fp32 products). */
 int sgemm_f32(const float* A, const float* B, float* C,
               int M, int N, int K, float alpha, float beta, cudaStream_t stream);
 
@@ -148,8 +153,9 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * (the path taken when strides or pointers are not 16-byte aligned);
  * 3 = split-K over an fp32 workspace; 4 = (fp32 only) FFMA kernel with
  * predicated scalar loads; 5 = whole tiles only (no K-cutting of the last,
- * partial wave of tiles); 6 = no CTA pairs (one CTA per 128-row tile).  A
- * forced path that cannot serve a call (e.g. TMA
+ * partial wave of tiles); 6 = no CTA pairs (one CTA per 128-row tile);
+ * 7 = (fp32) FFMA kernel only, no tensor cores; 8 = (fp32) 3xTF32 tensor-core
+ * kernel whatever the shape.  A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
  */

@@ -75,3 +75,66 @@ def test_deterministic():
     r1, _ = run("f32", A, B, C0, 1.0, 1.0, M, N, K, K, N, N)
     r2, _ = run("f32", A, B, C0, 1.0, 1.0, M, N, K, K, N, N)
     assert np.array_equal(r1, r2)
+
+
+# ---------------------------------------------------------------- 3xTF32 tensor-core path
+FFMA_ONLY, TF32_FORCED = 7, 8
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 520, 200), (129, 257, 65), (7, 9, 13),
+                                   (1000, 1000, 1000), (513, 1025, 4100), (64, 2000, 33)])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(1.0, 0.0, "nan"), (1.5, 0.5, "uniform"),
+                                               (0.75, -0.25, "uniform")])
+def test_3xtf32_parity(M, N, K, alpha, beta, c_fill):
+    A, B, C0 = operands(900 + M + N + K, M, N, K, K, N, N, np.float32, c_fill=c_fill)
+    got, taken = run("f32", A, B, C0, alpha, beta, M, N, K, K, N, N, path=TF32_FORCED)
+    assert taken == "f32.3xtf32.pair"
+    check("f32", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 700, 1000)])
+def test_3xtf32_small_integers_bit_exact(M, N, K):
+    """Integers in {-3..3} are tf32 values: the small parts are zero and every
+    partial sum is exact."""
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=TF32_FORCED)
+    assert taken == "f32.3xtf32.pair"
+    assert np.array_equal(got.astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0))
+
+
+def test_3xtf32_close_to_ffma_and_split_pins():
+    """The split keeps enough bits: at K = 1024 both the tensor-core and the
+    FFMA product stay below an eighth of the fp32 bound (a single tf32 product,
+    with its 2^-11 relative rounding per term, lands near or above the whole
+    bound)."""
+    M = N = K = 1024
+    A, B, C0 = operands(77, M, N, K, K, N, N, np.float32)
+    tc, t1 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    ff, t2 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=FFMA_ONLY)
+    assert t1 == "f32.3xtf32.pair" and t2.startswith("f32.ffma")
+    ref = oracle.gemm(A, B, None, 1.0, 0.0)
+    err_tc = np.abs(tc - ref).max()
+    err_ff = np.abs(ff - ref).max()
+    bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
+    assert err_tc < bound / 8 and err_ff < bound / 8, (err_tc, err_ff, bound)
+
+
+def test_3xtf32_long_k_no_drift():
+    """Long K: the tensor core's own fp32 accumulation drifts toward zero by a
+    bias growing like K*|C| (past the bound by K = 16384); the kernel folds
+    128-deep chunks into round-to-nearest register sums, so the error stays a
+    small fraction of the bound and shows no systematic sign."""
+    M, N, K = 256, 256, 16384
+    A, B, C0 = operands(4242, M, N, K, K, N, N, np.float32)
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=TF32_FORCED)
+    assert taken == "f32.3xtf32.pair"
+    ref = oracle.gemm(A, B, None, 1.0, 0.0)
+    err = got.astype(np.float64) - ref
+    bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
+    assert np.abs(err).max() < bound / 10, (np.abs(err).max(), bound)
+    # drift toward zero would make err * sign(ref) consistently negative
+    bias = np.mean(err * np.sign(ref))
+    assert abs(bias) < bound / 100, (bias, bound)
