@@ -72,6 +72,7 @@ DevState g_dev[kMaxDevices];
 std::atomic<int> g_force_path{0};
 std::atomic<int> g_force_splits{0};
 std::atomic<long long> g_wait_limit_ns{2000000000ll};
+std::atomic<long long> g_launches{0};
 thread_local const char* t_last_path = "none";
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -610,6 +611,8 @@ int encode_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long l
   return make_map_f16(map, ptr, rows, cols, ld, box_cols, box_rows);
 }
 
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace gb300
 
 using namespace gb300;
@@ -695,6 +698,8 @@ int gemm_debug_status(void) {
 }
 
 const char* gemm_last_path(void) { return t_last_path; }
+
+long long gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* gemm_strerror(int code) {
   switch (code) {

@@ -226,38 +226,38 @@ __global__ void split_tf32_t_kernel(const float* __restrict__ src, long long lds
 cudaError_t launch_split_tf32_t(const float* src, long long lds, float* big, float* small,
                                 long long ldd, int rows, int cols, int grid, cudaStream_t stream) {
   split_tf32_t_kernel<<<grid, dim3(32, 8), 0, stream>>>(src, lds, big, small, ldd, rows, cols);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 cudaError_t launch_split_tf32(const float* src, long long lds, float* big, float* small,
                               long long ldd, int rows, int cols, int grid, cudaStream_t stream) {
   split_tf32_kernel<<<grid, 256, 0, stream>>>(src, lds, big, small, ldd, rows, cols);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
                                int rows, int cols, int grid, cudaStream_t stream) {
   realign_f16_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, rows, cols);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int splits, uint16_t* C,
                                      long long ldc, int M, int N, float alpha, float beta,
                                      int grid, cudaStream_t stream) {
   splitk_reduce_f16_kernel<<<grid, 256, 0, stream>>>(ws, ws_ld, splits, C, ldc, M, N, alpha, beta);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 cudaError_t launch_scale_f16(uint16_t* C, long long ldc, int M, int N, float beta, int grid,
                              cudaStream_t stream) {
   scale_f16_kernel<<<grid, 256, 0, stream>>>(C, ldc, M, N, beta);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 cudaError_t launch_scale_f32(float* C, long long ldc, int M, int N, float beta, int grid,
                              cudaStream_t stream) {
   scale_f32_kernel<<<grid, 256, 0, stream>>>(C, ldc, M, N, beta);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 }  // namespace gb300

@@ -786,7 +786,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   }
   e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR>, tmA, tmB, tmC, args);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 // Largest number of CTA pairs of this configuration that can be resident at

@@ -8,6 +8,14 @@
 
 namespace gb300 {
 
+// Every kernel launch of the library goes through counted_launch: a
+// successful launch adds one to a process-wide counter (gemm_launch_count).
+void note_launch();
+inline cudaError_t counted_launch(cudaError_t e) {
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
 struct DeviceStatus;
 
 // Operand-load modes of the tensor-core kernel.

@@ -364,7 +364,7 @@ cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs
   cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
   e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, tmAb, tmAs, tmBb, tmBs, args);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 }  // namespace gb300

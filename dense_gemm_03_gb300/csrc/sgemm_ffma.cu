@@ -167,7 +167,7 @@ cudaError_t launch_sgemm_ffma(bool vec, const SgemmArgs& args, cudaStream_t stre
     sgemm_ffma_kernel<true><<<grid, 256, 0, stream>>>(args);
   else
     sgemm_ffma_kernel<false><<<grid, 256, 0, stream>>>(args);
-  return cudaGetLastError();
+  return counted_launch(cudaGetLastError());
 }
 
 }  // namespace gb300

@@ -179,6 +179,11 @@ int gemm_debug_status(void);
 /* Describes the path the last call on this thread took (static string). */
 const char* gemm_last_path(void);
 
+/* Number of kernels the library has launched in this process (all threads,
+ * all devices; launches that failed are not counted).  Nothing else --
+ * memset, copies, L2 flushes -- is counted. */
+long long gemm_launch_count(void);
+
 /* Text for a return code (static string). */
 const char* gemm_strerror(int code);
 
