@@ -17,7 +17,7 @@ import threading
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16", "sgemm_f32", "gemm_f16_host",
     "sgemm_f32_host", "gemm_f16_splitk_noalloc", "l2_flush", "force_path", "force_splits", "set_wait_limit_ns",
-    "debug_status", "last_path", "launch_count", "release", "EXPORTS",
+    "debug_status", "last_path", "launch_count", "plan_stream_k", "release", "EXPORTS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,7 @@ EXPORTS = (
     "gemm_f16", "gemm_f16_ld", "sgemm_f32", "sgemm_f32_ld", "gemm_f16_host", "sgemm_f32_host",
     "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
     "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
-    "gemm_f16_splitk_noalloc", "gemm_launch_count",
+    "gemm_f16_splitk_noalloc", "gemm_launch_count", "gemm_plan_stream_k",
 )
 
 PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
@@ -77,6 +77,9 @@ def lib():
             L.gemm_set_wait_limit_ns.argtypes = [ctypes.c_longlong]
             L.gemm_debug_status.restype = i
             L.gemm_debug_status.argtypes = []
+            L.gemm_plan_stream_k.restype = i
+            L.gemm_plan_stream_k.argtypes = [ctypes.c_longlong, ctypes.c_longlong, i, i,
+                                             ctypes.POINTER(ctypes.c_longlong)]
             L.gemm_launch_count.restype = ctypes.c_longlong
             L.gemm_launch_count.argtypes = []
             L.gemm_last_path.restype = ctypes.c_char_p
@@ -222,6 +225,13 @@ def debug_status() -> int:
 
 def last_path() -> str:
     return lib().gemm_last_path().decode()
+
+
+def plan_stream_k(tiles: int, slots: int, kb: int, all_tiles: bool = False) -> dict:
+    """The stream-K plan of the half-precision path (host-side query)."""
+    out = (ctypes.c_longlong * 4)()
+    _check(lib().gemm_plan_stream_k(tiles, slots, kb, int(bool(all_tiles)), out), "gemm_plan_stream_k")
+    return {"dp_tiles": out[0], "sk_tiles": out[1], "workers": out[2], "max_pieces": out[3]}
 
 
 def launch_count() -> int:

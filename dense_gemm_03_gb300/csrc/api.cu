@@ -193,6 +193,46 @@ int plan_tail_splits(long long tiles, long long ctas, int kb_total) {
   return best;
 }
 
+// Stream-K plan for `tiles` tiles of kb k-blocks on at most `slots`
+// concurrent workers (CTAs or CTA pairs).
+//  * all_tiles (few tiles, many SMs): every tile's k-blocks are shared out,
+//    at least kSkMinKb per worker;
+//  * otherwise, when the tiles do not fill a whole number of waves, the
+//    last partial wave and the full wave before it are shared out, so every
+//    worker ends at the same k-block count; the earlier waves stay whole
+//    tiles.  Taken only when it beats whole tiles by more than the cost of
+//    finishing a shared tile (about kSkFixKb k-blocks of main loop).
+// A worker's range then spans at most ceil(kb / range) + 1 tiles' pieces.
+struct SkPlan {
+  long long dp_tiles = 0, sk_tiles = 0, workers = 0, max_pieces = 0;
+};
+constexpr long long kSkMinKb = 4;
+constexpr long long kSkFixKb = 8;
+
+SkPlan plan_stream_k(long long tiles, long long slots, int kb, bool all_tiles) {
+  SkPlan p;
+  if (tiles <= 0 || slots <= 0 || kb <= 0) return p;
+  long long dp = 0;
+  if (!all_tiles) {
+    if (tiles <= slots || tiles % slots == 0) return p;
+    const long long full = tiles / slots;
+    dp = (full - 1) * slots;
+    const long long whole = (full + 1) * kb;
+    const long long shared = (full - 1) * kb + ((tiles - dp) * kb + slots - 1) / slots + kSkFixKb;
+    if (shared >= whole) return p;
+  }
+  const long long iters = (tiles - dp) * kb;
+  if (iters >= (1ll << 31)) return p;   // the kernel counts k-blocks in 32 bits
+  const long long workers = std::min(slots, iters / kSkMinKb);
+  if (workers < 2) return p;
+  const long long range = iters / workers;   // shortest range
+  p.dp_tiles = dp;
+  p.sk_tiles = tiles - dp;
+  p.workers = workers;
+  p.max_pieces = (kb + range - 1) / range + 1;
+  return p;
+}
+
 int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
                  int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = nullptr;
@@ -240,19 +280,8 @@ const char* kPathNames[3][3][3] = {
       "f16.tc.bn256.manual.splitk"}},
 };
 
-const char* kTailPathNames[3][2][2] = {
-    {{"f16.tc.bn64.tma.epi_tma.tail", "f16.tc.bn64.tma.epi_manual.tail"},
-     {"f16.tc.bn64.manual.epi_tma.tail", "f16.tc.bn64.manual.epi_manual.tail"}},
-    {{"f16.tc.bn128.tma.epi_tma.tail", "f16.tc.bn128.tma.epi_manual.tail"},
-     {"f16.tc.bn128.manual.epi_tma.tail", "f16.tc.bn128.manual.epi_manual.tail"}},
-    {{"f16.tc.bn256.tma.epi_tma.tail", "f16.tc.bn256.tma.epi_manual.tail"},
-     {"f16.tc.bn256.manual.epi_tma.tail", "f16.tc.bn256.manual.epi_manual.tail"}},
-};
-
-const char* kPairPathNames[2][2] = {
-    {"f16.tc.pair.bn256.tma.epi_tma", "f16.tc.pair.bn256.tma.epi_tma.tail"},
-    {"f16.tc.pair.bn256.tma.epi_manual", "f16.tc.pair.bn256.tma.epi_manual.tail"},
-};
+const char* kPairPathNames[2] = {"f16.tc.pair.bn256.tma.epi_tma",
+                                 "f16.tc.pair.bn256.tma.epi_manual"};
 
 int check_common(const void* A, const void* B, const void* C, int M, int N, int K, long long lda,
                  long long ldb, long long ldc, float alpha, size_t elem = 1) {
@@ -355,11 +384,14 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   a.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
   a.status = d->status;
 
-  // Split-K when the tiles alone leave most SMs idle.
   const long long tiles = 1ll * a.tiles_m * a.tiles_n;
   int splits = 1;
   const int fs = g_force_splits.load();
-  if (force == 3 || (force == 0 && tiles * 2 <= d->sm_count && a.kb_total >= 8)) {
+  // Few tiles for many SMs: the k-blocks of all tiles are shared out evenly
+  // over the SMs (stream-K); the forced split-K path cuts every tile into
+  // equal K slices instead.
+  const bool few = tiles * 2 <= d->sm_count && a.kb_total >= 8;
+  if (force == 3) {
     // as many K slices as fit in ONE wave of CTAs (a second, partial wave would
     // double the time of these bandwidth-bound shapes)
     splits = fs > 0 ? fs
@@ -380,20 +412,34 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   // CTA pairs (256 x 256 tiles on clusters of 2 sharing each MMA) for the
   // large aligned shapes: each SM then stages half as much of B per MMA.
   int pair_slots = 0;
-  const bool pair = splits == 1 && force != 6 && bn == 256 && load == kLoadTma &&
-                    a.tiles_m >= 2 && (pair_slots = tc_pair_max_clusters(epi)) > 0;
+  const bool pair = splits == 1 && !(force == 0 && few) && force != 6 && bn == 256 &&
+                    load == kLoadTma && a.tiles_m >= 2 &&
+                    (pair_slots = tc_pair_max_clusters(epi)) > 0;
   long long units_tiles = tiles;   // tiles in units of the worker (CTA or pair)
-  long long workers = std::min<long long>(tiles, d->sm_count);
+  long long slots = d->sm_count;   // workers that can run at once
   if (pair) {
     a.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
     units_tiles = 1ll * a.tiles_m * a.tiles_n;
-    workers = std::min<long long>(units_tiles, pair_slots);
+    slots = pair_slots;
   }
+  long long workers = std::min<long long>(units_tiles, slots);
 
   a.dp_tiles = static_cast<int>(units_tiles);
   a.tail_splits = 1;
   a.tail_kb_per_split = a.kb_total;
   const char* cut = "";
+  // scratch for partial sums: `parts` 128-row tile parts x `pieces` each
+  auto take_scratch = [&](long long parts, long long pieces) -> int {
+    const size_t need = sizeof(float) * static_cast<size_t>(parts) * pieces * kBM * bn;
+    std::lock_guard<std::mutex> lk(g_mu);
+    StreamWs* w = nullptr;
+    if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(parts) * 8, &w)) return rc;
+    a.tail_ws = static_cast<float*>(w->ptr);
+    a.tail_counters = static_cast<unsigned long long*>(w->counters);
+    a.epoch = ++w->epoch;
+    if (a.epoch == 0) a.epoch = ++w->epoch;   // 0 marks never-used counters
+    return GEMM_OK;
+  };
   if (splits > 1) {
     // Every tile is cut into `splits` K slices: each slice publishes fp32
     // partial sums and the last one of a tile to finish adds them up (in slice
@@ -404,39 +450,64 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
     a.kb_per_split = a.kb_total;
     splits = 1;
     a.splits = 1;
-    const size_t need = sizeof(float) * static_cast<size_t>(tiles) * a.tail_splits * kBM * bn;
-    std::lock_guard<std::mutex> lk(g_mu);
-    StreamWs* w = nullptr;
-    if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tiles) * 8, &w)) return rc;
-    a.tail_ws = static_cast<float*>(w->ptr);
-    a.tail_counters = static_cast<unsigned long long*>(w->counters);
-    a.epoch = ++w->epoch;
-    if (a.epoch == 0) a.epoch = ++w->epoch;
+    if (int rc = take_scratch(tiles, a.tail_splits)) return rc;
     cut = ".splitk";
-  } else if (force != 5) {
-    // Balance the last, partial wave: cut its tiles along K.
+  } else if (force == 9) {
+    // Two equal K slices for each tile of the last, partial wave.
     int ts = plan_tail_splits(units_tiles, workers, a.kb_total);
     if (ts > 1) {
       const long long tail_tiles = units_tiles % workers;
-      const long long parts = tail_tiles * (pair ? 2 : 1);   // 128-row parts with own partials
       a.tail_kb_per_split = (a.kb_total + ts - 1) / ts;
       ts = (a.kb_total + a.tail_kb_per_split - 1) / a.tail_kb_per_split;   // no empty slice
       a.dp_tiles = static_cast<int>(units_tiles - tail_tiles);
       a.tail_splits = ts;
-      const size_t need = sizeof(float) * static_cast<size_t>(parts) * ts * kBM * bn;
-      std::lock_guard<std::mutex> lk(g_mu);
-      StreamWs* w = nullptr;
-      if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(parts) * 8, &w))
-        return rc;
-      a.tail_ws = static_cast<float*>(w->ptr);
-      a.tail_counters = static_cast<unsigned long long*>(w->counters);
-      a.epoch = ++w->epoch;
-      if (a.epoch == 0) a.epoch = ++w->epoch;   // 0 marks never-used counters
+      if (int rc = take_scratch(tail_tiles * (pair ? 2 : 1), ts)) return rc;
+      cut = ".tail";
+    }
+  } else if (force == 10) {
+    // stream-K over the last waves (k-block ranges shared out evenly)
+    const SkPlan sk = plan_stream_k(units_tiles, slots, a.kb_total, false);
+    if (sk.sk_tiles > 0) {
+      a.dp_tiles = static_cast<int>(sk.dp_tiles);
+      a.sk_tile0 = static_cast<int>(sk.dp_tiles);
+      a.sk_tiles = static_cast<int>(sk.sk_tiles);
+      a.sk_workers = static_cast<int>(sk.workers);
+      a.sk_iters = sk.sk_tiles * a.kb_total;
+      a.tail_splits = static_cast<int>(sk.max_pieces);
+      workers = sk.workers;
+      if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
+      cut = ".sk";
+    }
+  } else if (force != 5 && !(few && force == 0)) {
+    // The tiles of the last, partial wave become two half-width units each
+    // (whole K, no partial sums) when the halves fit in one wave.
+    const long long rem = units_tiles % slots;
+    if (load == kLoadTma && bn >= 128 && rem > 0 && 2 * rem <= slots) {
+      a.dp_tiles = static_cast<int>(units_tiles - rem);
+      a.tail_splits = 2;
+      a.tail_halves = 1;
+      workers = std::min<long long>(slots, a.dp_tiles > 0 ? slots : 2 * rem);
+      cut = ".halves";
+    }
+  } else if (force != 5) {
+    const SkPlan sk = plan_stream_k(units_tiles, slots, a.kb_total, true);
+    if (sk.sk_tiles > 0) {
+      a.dp_tiles = static_cast<int>(sk.dp_tiles);
+      a.sk_tile0 = static_cast<int>(sk.dp_tiles);
+      a.sk_tiles = static_cast<int>(sk.sk_tiles);
+      a.sk_workers = static_cast<int>(sk.workers);
+      a.sk_iters = sk.sk_tiles * a.kb_total;
+      a.tail_splits = static_cast<int>(sk.max_pieces);
+      workers = sk.workers;
+      if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
+      cut = ".sk";
     }
   }
 
-  a.num_units = static_cast<int>(a.dp_tiles * static_cast<long long>(splits) +
-                                 (units_tiles - a.dp_tiles) * a.tail_splits);
+  a.num_units = a.sk_tiles > 0
+                    ? a.dp_tiles
+                    : static_cast<int>(a.dp_tiles * static_cast<long long>(splits) +
+                                       (units_tiles - a.dp_tiles) * a.tail_splits);
 
   CUtensorMap tmA{}, tmB{}, tmC{};
   if (load == kLoadTma) {
@@ -447,21 +518,19 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
     // epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle
     if (int rc = make_map_f16(&tmC, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
   }
+  // one CTA (pair) per worker; with stream-K exactly sk_workers of them
+  const long long nw = a.sk_tiles > 0 ? a.sk_workers : std::min<long long>(a.num_units, workers);
   if (pair) {
-    const int grid = 2 * static_cast<int>(std::min<long long>(a.num_units, workers));
-    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s",
-             a.tail_splits > 1 ? kPairPathNames[epi][1] : kPairPathNames[epi][0], how);
+    const int grid = 2 * static_cast<int>(nw);
+    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s", kPairPathNames[epi], cut, how);
     t_last_path = t_path_buf;
     if (launch_gemm_f16_tc_pair(epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     return GEMM_OK;
   }
-  const int grid = static_cast<int>(std::min<long long>(a.num_units, d->sm_count));
+  const int grid = static_cast<int>(nw);
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s",
-           (a.tail_splits > 1 && a.dp_tiles > 0) ? kTailPathNames[bi][load][epi]
-                                                  : kPathNames[bi][load][epi],
-           cut, how);
+  snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s", kPathNames[bi][load][epi], cut, how);
   t_last_path = t_path_buf;
   if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
@@ -671,7 +740,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 8) return GEMM_ERR_ARG;
+  if (path < 0 || path > 10) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 
@@ -698,6 +767,16 @@ int gemm_debug_status(void) {
 }
 
 const char* gemm_last_path(void) { return t_last_path; }
+
+int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, long long* out) {
+  if (out == nullptr) return GEMM_ERR_NULL;
+  const SkPlan p = plan_stream_k(tiles, slots, kb, all_tiles != 0);
+  out[0] = p.dp_tiles;
+  out[1] = p.sk_tiles;
+  out[2] = p.workers;
+  out[3] = p.max_pieces;
+  return GEMM_OK;
+}
 
 long long gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

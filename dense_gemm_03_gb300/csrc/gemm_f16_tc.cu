@@ -53,15 +53,19 @@ constexpr int kBBlockBytes = BK * 128;       // one 64-column block of a B stage
 constexpr int kSubCols = 32;                 // epilogue sub-chunk width
 constexpr int kEpiBufBytes = 32 * kSubCols * 2;   // 2 KB staging tile
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
+// C staging tiles per epilogue warp in the CTA-pair kernel (2: six stages of
+// A/B fit beside them; 4: the warp's whole C part, five stages).
+constexpr int kCsBufs = 2;
 
 // PAIR: two CTAs of a cluster share each tcgen05.mma.cta_group::2 (M = 256);
 // each CTA stages its own 128 rows of A and half of the BN columns of B.
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool CS = false>
 struct TcCfg {
   static constexpr int kBLoadCols = PAIR ? BN / 2 : BN;   // B columns staged by this CTA
   static constexpr int kBBytes = kBLoadCols * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = PAIR ? 6 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+  static constexpr int kStages =
+      PAIR ? ((CS && kCsBufs > 2) ? 5 : 6) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int kTmemCols = 2 * BN;     // two accumulators
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(!PAIR || BN == 256, "pairs use 256-wide tiles");
@@ -86,12 +90,19 @@ constexpr int kTailCounters = 8;
 
 template <int BN, int EPI, bool PAIR>
 struct Smem {
-  using Cfg = TcCfg<BN, PAIR>;
+  // C read by TMA into the epilogue's staging tiles: the CTA-pair kernel with
+  // TMA stores
+  static constexpr bool kCs = PAIR && EPI == kEpiTma;
+  using Cfg = TcCfg<BN, PAIR, kCs>;
+  // 32 x 32 staging tiles per epilogue warp
+  static constexpr int kBufs = kCs ? kCsBufs : 2;
+  static constexpr int kWarpEpiBytes = kBufs * kEpiBufBytes;
   static constexpr int kEpiOff = Cfg::kStages * Cfg::kStageBytes;
-  static constexpr int kEpiBytes = (EPI == kEpiPartial) ? 0 : 8 * 2 * kEpiBufBytes;
+  static constexpr int kEpiBytes = (EPI == kEpiPartial) ? 0 : 8 * kWarpEpiBytes;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
-  // full[S], empty[S], acc_full[2], acc_empty[2], mma_done, tmem_free
-  static constexpr int kNumBars = 2 * Cfg::kStages + 2 + 2 + 1 + 1;
+  // full[S], empty[S], acc_full[2], acc_empty[2], mma_done, tmem_free,
+  // c_full[8 warps][kBufs staging tiles]
+  static constexpr int kNumBars = 2 * Cfg::kStages + 2 + 2 + 1 + 1 + 8 * kBufs;
   static constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
   static constexpr int kUsed = kTmemPtrOff + 16;
   static constexpr int kAlloc = kUsed + 1024;  // the dynamic base is aligned up to 1024 B
@@ -100,14 +111,28 @@ struct Smem {
 
 struct Unit {
   int m0, n0, kb0, kb1, split;
-  int tail;       // 1 for a K slice of a tail tile
+  int tail;       // 1 for a K slice of a tail tile (or a piece of a shared stream-K tile)
   int tail_idx;   // index of the tail tile (tail units only)
+  int npieces;    // slices or pieces the tile is cut into (tail units only)
+  int ncols;      // columns of the unit: BN, or BN/2 for a half-width tail unit
 };
+
+// Output tile index (in visiting order) -> first row and column.  Tiles are
+// visited in groups of group_m tile-rows so that concurrently running CTAs
+// share B panels in L2.
+__device__ __forceinline__ void tile_origin(const TcArgs& p, int tile, int bn, int bm_tile,
+                                            int rank, Unit& x) {
+  const int group = p.group_m * p.tiles_n;
+  const int g = tile / group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.tiles_m - first_m, p.group_m);
+  const int r = tile - g * group;
+  x.m0 = (first_m + r % gm) * bm_tile + rank * BM;
+  x.n0 = (r / gm) * bn;
+}
 
 // Work unit u -> output tile and K range.  Units [0, dp_tiles*splits) are
 // whole tiles (or split-K slices); the rest are K slices of the tail tiles.
-// Tiles are visited in groups of group_m tile-rows so that concurrently
-// running CTAs share B panels in L2.
 __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn, int bm_tile = BM,
                                            int rank = 0) {
   Unit x;
@@ -119,6 +144,22 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn, int 
     kpb = p.kb_per_split;
     x.tail = 0;
     x.tail_idx = 0;
+    x.npieces = 1;
+    x.ncols = bn;
+  } else if (p.tail_halves) {
+    // two half-width units per tail tile, each over the whole K
+    const int v = u - dp_units;
+    tile = p.dp_tiles + (v >> 1);
+    tile_origin(p, tile, bn, bm_tile, rank, x);
+    x.n0 += (v & 1) * (bn / 2);
+    x.ncols = bn / 2;
+    x.split = 0;
+    x.tail = 0;
+    x.tail_idx = 0;
+    x.npieces = 1;
+    x.kb0 = 0;
+    x.kb1 = p.kb_total;
+    return x;
   } else {
     const int v = u - dp_units;
     x.tail_idx = v / p.tail_splits;
@@ -126,17 +167,66 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn, int 
     tile = p.dp_tiles + x.tail_idx;
     kpb = p.tail_kb_per_split;
     x.tail = 1;
+    x.npieces = p.tail_splits;
+    x.ncols = bn;
   }
-  const int group = p.group_m * p.tiles_n;
-  const int g = tile / group;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.tiles_m - first_m, p.group_m);
-  const int r = tile - g * group;
-  x.m0 = (first_m + r % gm) * bm_tile + rank * BM;
-  x.n0 = (r / gm) * bn;
+  tile_origin(p, tile, bn, bm_tile, rank, x);
   x.kb0 = x.split * kpb;
   x.kb1 = min(p.kb_total, x.kb0 + kpb);
   return x;
+}
+
+// Stream-K: first k-block of worker w's range, and the worker whose range
+// holds k-block x (the largest w with sk_begin(w) <= x).
+__device__ __forceinline__ int sk_begin(const TcArgs& p, int w) {
+  return static_cast<int>(static_cast<long long>(w) * p.sk_iters / p.sk_workers);
+}
+__device__ __forceinline__ int sk_owner(const TcArgs& p, int x) {
+  return static_cast<int>((static_cast<long long>(x + 1) * p.sk_workers - 1) / p.sk_iters);
+}
+
+// Position of one worker in its sequence of units: first the units
+// worker, worker + nworkers, ... below num_units, then the pieces of its
+// stream-K range [x, x_end).
+struct UnitCursor {
+  int u, x, x_end;   // the host keeps sk_iters below 2^31
+};
+
+__device__ __forceinline__ UnitCursor first_unit(const TcArgs& p, int worker) {
+  UnitCursor c;
+  c.u = worker;
+  if (p.sk_tiles > 0 && worker < p.sk_workers) {
+    c.x = sk_begin(p, worker);
+    c.x_end = sk_begin(p, worker + 1);
+  } else {
+    c.x = c.x_end = 0;
+  }
+  return c;
+}
+
+// The worker's next unit into t; false when it has none left.
+__device__ __forceinline__ bool next_unit(const TcArgs& p, UnitCursor& c, int worker,
+                                          int nworkers, int bn, int bm_tile, int rank, Unit& t) {
+  if (c.u < p.num_units) {
+    t = decode_unit(p, c.u, bn, bm_tile, rank);
+    c.u += nworkers;
+    return true;
+  }
+  if (c.x >= c.x_end) return false;
+  const int kb = p.kb_total;
+  const int s = c.x / kb;   // stream-K tile
+  t.kb0 = c.x - s * kb;
+  t.kb1 = min(kb, t.kb0 + (c.x_end - c.x));
+  c.x += t.kb1 - t.kb0;
+  const int first = sk_owner(p, s * kb);
+  const int last = sk_owner(p, (s + 1) * kb - 1);
+  t.npieces = last - first + 1;
+  t.split = worker - first;
+  t.tail = t.npieces > 1 ? 1 : 0;
+  t.tail_idx = s;
+  t.ncols = bn;
+  tile_origin(p, p.sk_tile0 + s, bn, bm_tile, rank, t);
+  return true;
 }
 
 // Partial sums of one K slice of a tail tile: BN/4 column quads x 128 rows of
@@ -280,33 +370,15 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* 
   }
 }
 
-// Adds two slices' partial sums (slice a first, then b) with all 16 loads in
-// flight together.
-__device__ __forceinline__ void add_partials2(uint32_t (&acc)[32], const float4* a,
-                                              const float4* b) {
-  float4 va[8], vb[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    va[i] = __ldcg(a + i * BM);
-    vb[i] = __ldcg(b + i * BM);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    acc[4 * i] = __float_as_uint((__uint_as_float(acc[4 * i]) + va[i].x) + vb[i].x);
-    acc[4 * i + 1] = __float_as_uint((__uint_as_float(acc[4 * i + 1]) + va[i].y) + vb[i].y);
-    acc[4 * i + 2] = __float_as_uint((__uint_as_float(acc[4 * i + 2]) + va[i].z) + vb[i].z);
-    acc[4 * i + 3] = __float_as_uint((__uint_as_float(acc[4 * i + 3]) + va[i].w) + vb[i].w);
-  }
-}
-
 template <int BN, int LOAD, int EPI, bool PAIR>
 __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
-  using Cfg = TcCfg<BN, PAIR>;
   using R = Roles<LOAD>;
   using L = Smem<BN, EPI, PAIR>;
+  using Cfg = typename L::Cfg;
+  constexpr bool kCs = L::kCs;
   constexpr int S = Cfg::kStages;
   static_assert(!PAIR || (LOAD == kLoadTma && EPI != kEpiPartial), "pair configuration");
   // Units are handed out per CTA, or per CTA pair (cluster of 2).
@@ -330,6 +402,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * S + 2 + b); };
   const uint32_t done_bar = bars + 8u * (2 * S + 4);
   const uint32_t tmem_free_bar = bars + 8u * (2 * S + 5);   // epilogue warps done with TMEM
+  // C sub-tile landed in staging tile b of epilogue warp w
+  auto cfull_bar = [&](int w, int b) { return bars + 8u * (2 * S + 6 + L::kBufs * w + b); };
   auto stage_a = [&](int s) { return base + static_cast<uint32_t>(s * Cfg::kStageBytes); };
   auto stage_b = [&](int s) { return stage_a(s) + kABytes; };
 
@@ -344,6 +418,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     }
     mbar_init(done_bar, 1u);
     mbar_init(tmem_free_bar, static_cast<uint32_t>(R::kEpiWarps));
+    for (int w = 0; w < 8; ++w)
+      for (int b = 0; b < L::kBufs; ++b) mbar_init(cfull_bar(w, b), 1u);
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -380,31 +456,37 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0;
         bool ok = true;
-        for (int u = worker; ok && u < p.num_units; u += nworkers) {
-          const Unit t = decode_unit(p, u, BN, bm_tile, rank);
+        UnitCursor cur = first_unit(p, worker);
+        Unit t;
+        while (ok && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t)) {
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
             if (!wait_parity(empty_bar(stage), phase ^ 1u, limit, st, 1)) {
               ok = false;
               break;
             }
+            // B columns this CTA stages: a half-width unit needs half of them
+            const int bcols = PAIR ? t.ncols / 2 : t.ncols;
+            const uint32_t bytes = static_cast<uint32_t>(kABytes + bcols * BK * 2);
             if (PAIR) {
               // Both CTAs' bytes are counted on the leader's barrier; only the
               // leader arms it (for the pair's total), the peer's copies just
               // signal it.
               const uint32_t fb = map_to_cta(full_bar(stage), 0);
-              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
+              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
               tma_load_2d_pair(stage_a(stage), &tmA, fb, kb * BK, t.m0);
 #pragma unroll
               for (int c = 0; c < Cfg::kBLoadCols / 64; ++c)
-                tma_load_2d_pair(stage_b(stage) + c * kBBlockBytes, &tmB, fb,
-                                 t.n0 + static_cast<int>(rank) * Cfg::kBLoadCols + 64 * c, kb * BK);
+                if (64 * c < bcols)
+                  tma_load_2d_pair(stage_b(stage) + c * kBBlockBytes, &tmB, fb,
+                                   t.n0 + static_cast<int>(rank) * bcols + 64 * c, kb * BK);
             } else {
-              mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+              mbar_arrive_expect_tx(full_bar(stage), bytes);
               tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
-                tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
-                            t.n0 + 64 * c, kb * BK);
+                if (64 * c < bcols)
+                  tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
+                              t.n0 + 64 * c, kb * BK);
             }
             ++issued;
             if (++stage == S) {
@@ -431,8 +513,9 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = worker; ok && u < p.num_units; u += nworkers) {
-        const Unit t = decode_unit(p, u, BN, bm_tile, rank);
+      UnitCursor cur = first_unit(p, worker);
+      Unit t;
+      while (ok && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t)) {
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!wait_parity(empty_bar(stage), phase ^ 1u, limit, st, 2)) {
             ok = false;
@@ -475,15 +558,18 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   } else if (warp == R::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = make_idesc(0u, PAIR ? 2 * BM : BM, BN, 0u, 1u);
+      constexpr uint32_t idesc_full = make_idesc(0u, PAIR ? 2 * BM : BM, BN, 0u, 1u);
+      constexpr uint32_t idesc_half = make_idesc(0u, PAIR ? 2 * BM : BM, BN / 2, 0u, 1u);
       int stage = 0;
       uint32_t phase = 0, local = 0;
       bool ok = true;
-      for (int u = worker; ok && u < p.num_units; u += nworkers) {
-        const Unit t = decode_unit(p, u, BN, bm_tile, rank);
+      UnitCursor cur = first_unit(p, worker);
+      Unit t;
+      while (ok && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t)) {
         const uint32_t buf = local & 1u, use = local >> 1;
         if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 3)) break;
         tc_fence_after();
+        const uint32_t idesc = t.ncols == BN ? idesc_full : idesc_half;
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!wait_parity(full_bar(stage), phase, limit, st, 4)) {
@@ -544,75 +630,150 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       tmem_dealloc(tmem_base, Cfg::kTmemCols);
   } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int kWarpCols = BN * 4 / R::kEpiWarps;   // columns per epilogue warp
+    constexpr int kWarpCols = BN * 4 / R::kEpiWarps;   // columns per epilogue warp (whole tile)
     constexpr int kSubs = kWarpCols / kSubCols;
     const int ew = warp - R::kEpiWarp0;   // 0 .. kEpiWarps-1
     const int q = warp & 3;               // TMEM lane quadrant -> rows 32q .. 32q+31
     const int h = ew >> 2;                // column part of the tile
     const bool has_c = p.beta != 0.0f;
-    const uint32_t sbuf0 = base + L::kEpiOff + ew * 2 * kEpiBufBytes;
-    uint8_t* const sptr0 = base_ptr + L::kEpiOff + ew * 2 * kEpiBufBytes;
+    const uint32_t sbuf0 = base + L::kEpiOff + ew * L::kWarpEpiBytes;
+    uint8_t* const sptr0 = base_ptr + L::kEpiOff + ew * L::kWarpEpiBytes;
     uint32_t local = 0, nstore = 0;
-    for (int u = worker; u < p.num_units; u += nworkers) {
-      const Unit t = decode_unit(p, u, BN, bm_tile, rank);
+    // kCs: C sub-tiles (32 rows x 32 columns) are read by TMA into the
+    // staging tiles, where the result replaces them and is stored by TMA.
+    // The first kBufs sub-tiles of a unit are requested while its main loop
+    // runs; sub-tile k + kBufs as soon as the store of sub-tile k has read its
+    // tile.  c_loads[b] counts the loads into tile b (the parity of its
+    // barrier).
+    constexpr int NB = L::kBufs;
+    uint32_t c_loads[NB];
+    bool c_pending[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      c_loads[b] = 0u;
+      c_pending[b] = false;
+    }
+    auto load_c_sub_tma = [&](int b, int col, int r0) {
+      if (lane == 0) {
+        bulk_wait_group_read<0>();   // stores issued from the staging tiles have read them
+        mbar_arrive_expect_tx(cfull_bar(ew, b), static_cast<uint32_t>(kEpiBufBytes));
+        tma_load_2d(sbuf0 + b * kEpiBufBytes, &tmC, cfull_bar(ew, b), col, r0);
+      }
+      ++c_loads[b];
+      c_pending[b] = true;
+    };
+    auto wait_c_sub = [&](int b) -> bool {
+      if (!c_pending[b]) return true;
+      // on failure the load stays pending and is drained before the CTA exits
+      if (!wait_parity(cfull_bar(ew, b), (c_loads[b] - 1u) & 1u, limit, st, 9)) return false;
+      c_pending[b] = false;
+      return true;
+    };
+    auto load_c_head = [&](const Unit& u2) {   // the first NB sub-tiles of a unit
+      const int wc = u2.ncols * 4 / R::kEpiWarps;
+      const int r0 = u2.m0 + 32 * q, cw = u2.n0 + h * wc;
+      if (!has_c || r0 >= p.M || cw >= p.N) return;
+#pragma unroll
+      for (int k = 0; k < NB && k < kSubs; ++k)
+        if (kSubCols * k < wc && cw + kSubCols * k < p.N) load_c_sub_tma(k, cw + kSubCols * k, r0);
+    };
+    UnitCursor cur = first_unit(p, worker);
+    Unit t, tn;
+    bool have = next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t);
+    if (kCs && have) load_c_head(t);
+    while (have) {
+      // kCs looks one unit ahead (its C tile is loaded during the next main loop)
+      const bool have_next = kCs && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, tn);
       const uint32_t buf = local & 1u, use = local >> 1;
       const int row0 = t.m0 + 32 * q;
       // tail bookkeeping is per CTA: the rows of one CTA of a pair form their own part
       const int tail_part = PAIR ? 2 * t.tail_idx + static_cast<int>(rank) : t.tail_idx;
-      const int colw = t.n0 + h * kWarpCols;        // first column of this warp
+      const int wcols = t.ncols * 4 / R::kEpiWarps;  // this warp's columns of the unit
+      const int nsub = wcols / kSubCols;
+      const int colw = t.n0 + h * wcols;            // first column of this warp
       const int row = row0 + lane;                  // this thread's row
       bool finish = row0 < p.M && colw < p.N;       // this warp has outputs to produce
+      if (EPI != kEpiPartial && has_c && finish && row < p.M) {
+        // While this unit's main loop runs, bring this row's part of C into
+        // L2, so that the epilogue's reads of C wait on L2 and not on DRAM.
+        const uint16_t* c0 = p.C + static_cast<long long>(row) * p.ldc + colw;
+        const int ncols = min(wcols, p.N - colw);
+        const uintptr_t first = reinterpret_cast<uintptr_t>(c0) & ~static_cast<uintptr_t>(127);
+        const uintptr_t last = reinterpret_cast<uintptr_t>(c0 + ncols - 1);
+        for (uintptr_t a = first; a <= last; a += 128) prefetch_l2(reinterpret_cast<const void*>(a));
+      }
       // C of the first sub-chunk is requested before the accumulator is ready.
       uint4 c_next[4];
-      if (EPI == kEpiTma && has_c && finish && !t.tail) load_c_sub(p, row, colw, c_next);
+      if (!kCs && EPI == kEpiTma && has_c && finish && !t.tail) load_c_sub(p, row, colw, c_next);
       if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 5)) break;
       tc_fence_after();
       const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * kWarpCols;
+          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * wcols;
 
       if (EPI != kEpiPartial && t.tail && finish) {
-        // Publish this slice's partial sums, then count the slice in; the last
-        // slice to arrive finishes the tile.
-        float4* mine = tail_partials(p, tail_part, t.split, BN) + 32 * q + lane;
-        for (int k = 0; k < kSubs; ++k) {
-          if (colw + kSubCols * k >= p.N) break;
-          uint32_t acc[32];
-          tmem_ld_32x32b_x32(tbase + kSubCols * k, acc);
-          tmem_wait_regs(acc);
-          const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            __stcg(mine + (cq0 + i) * BM,
-                   make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
-                               __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3])));
-        }
-        __threadfence();
-        __syncwarp();
-        uint32_t arrived = 0;
+        unsigned long long* cnt = p.tail_counters + tail_part * kTailCounters + h * 4 + q;
+        // If every other slice of the tile has already published, this one
+        // finishes the tile straight from TMEM and need not publish.
+        uint32_t before = 0;
         if (lane == 0) {
-          unsigned long long* cnt = p.tail_counters + tail_part * kTailCounters + h * 4 + q;
-          unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
-          for (;;) {
-            const unsigned long long next =
-                (static_cast<unsigned int>(cur >> 32) == p.epoch)
-                    ? cur + 1ull
-                    : ((static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
-            const unsigned long long prev = atomicCAS(cnt, cur, next);
-            if (prev == cur) {
-              arrived = static_cast<uint32_t>(next & 0xFFFFFFFFull);
-              break;
-            }
-            cur = prev;
-          }
+          const unsigned long long c0 = ld_acquire_gpu_u64(cnt);
+          before = (static_cast<unsigned int>(c0 >> 32) == p.epoch)
+                       ? static_cast<uint32_t>(c0 & 0xFFFFFFFFull)
+                       : 0u;
         }
-        arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        finish = arrived == static_cast<uint32_t>(p.tail_splits);
-        if (finish) {
+        before = __shfl_sync(0xffffffffu, before, 0);
+        if (before + 1u == static_cast<uint32_t>(t.npieces)) {
           __threadfence();
-          if (EPI == kEpiTma && has_c) load_c_sub(p, row, colw, c_next);
+          if (!kCs && EPI == kEpiTma && has_c) load_c_sub(p, row, colw, c_next);
+        } else {
+          // Publish this slice's partial sums, then count the slice in; the last
+          // slice to arrive finishes the tile.
+          float4* mine = tail_partials(p, tail_part, t.split, BN) + 32 * q + lane;
+          for (int k = 0; k < kSubs; ++k) {
+            if (colw + kSubCols * k >= p.N) break;
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tbase + kSubCols * k, acc);
+            tmem_wait_regs(acc);
+            const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              __stcg(mine + (cq0 + i) * BM,
+                     make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
+                                 __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3])));
+          }
+          __threadfence();
+          __syncwarp();
+          uint32_t arrived = 0;
+          if (lane == 0) {
+            unsigned long long cv = *reinterpret_cast<volatile unsigned long long*>(cnt);
+            for (;;) {
+              const unsigned long long next =
+                  (static_cast<unsigned int>(cv >> 32) == p.epoch)
+                      ? cv + 1ull
+                      : ((static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
+              const unsigned long long prev = atomicCAS(cnt, cv, next);
+              if (prev == cv) {
+                arrived = static_cast<uint32_t>(next & 0xFFFFFFFFull);
+                break;
+              }
+              cv = prev;
+            }
+          }
+          arrived = __shfl_sync(0xffffffffu, arrived, 0);
+          finish = arrived == static_cast<uint32_t>(t.npieces);
+          if (finish) {
+            __threadfence();
+            if (!kCs && EPI == kEpiTma && has_c) load_c_sub(p, row, colw, c_next);
+          }
         }
       }
 
+      if (kCs && !finish) {   // unused C retired
+        bool ok_c = true;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) ok_c = wait_c_sub(b) && ok_c;
+        if (!ok_c) break;
+      }
       if (finish) {
         uint32_t acc_a[32], acc_b[32];
         if (!t.tail) {
@@ -624,26 +785,39 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           uint32_t(&cur)[32] = (k & 1) ? acc_b : acc_a;
           uint32_t(&nxt)[32] = (k & 1) ? acc_a : acc_b;
           const int col0 = colw + kSubCols * k;
-          if (col0 >= p.N) break;
-          const bool more = k + 1 < kSubs && col0 + kSubCols < p.N;
+          if (k >= nsub || col0 >= p.N) break;
+          const bool more = k + 1 < nsub && col0 + kSubCols < p.N;
           if (more && !t.tail) tmem_ld_32x32b_x32(tbase + kSubCols * (k + 1), nxt);   // in flight
           uint4 c_cur[4];
-          if (EPI == kEpiTma) {
+          if (!kCs && EPI == kEpiTma) {
 #pragma unroll
             for (int g = 0; g < 4; ++g) c_cur[g] = c_next[g];
             if (has_c && more) load_c_sub(p, row, col0 + kSubCols, c_next);
           }
           if (EPI != kEpiPartial && t.tail) {
-            // cur := sum of every slice's partial sums (this slice's included),
-            // in slice order.
+            // cur := sum of every slice's partial sums in slice order; this
+            // slice's own term is still in TMEM (bit-identical to what it
+            // published), so only the other slices are read back.
             const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
             const float4* part = tail_partials(p, tail_part, 0, BN) + 32 * q + lane + cq0 * BM;
             const long long slice = static_cast<long long>(BN / 4) * BM;
-            add_partials(cur, part, true);
-            int s2 = 1;
-            for (; s2 + 1 < p.tail_splits; s2 += 2)
-              add_partials2(cur, part + s2 * slice, part + (s2 + 1) * slice);
-            if (s2 < p.tail_splits) add_partials(cur, part + s2 * slice, false);
+            if (t.split == 0) {
+              tmem_ld_32x32b_x32(tbase + kSubCols * k, cur);
+              tmem_wait_regs(cur);
+            } else {
+              add_partials(cur, part, true);
+            }
+            for (int s2 = 1; s2 < t.npieces; ++s2) {
+              if (s2 == t.split) {
+                tmem_ld_32x32b_x32(tbase + kSubCols * k, nxt);
+                tmem_wait_regs(nxt);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  cur[i] = __float_as_uint(__uint_as_float(cur[i]) + __uint_as_float(nxt[i]));
+              } else {
+                add_partials(cur, part + s2 * slice, false);
+              }
+            }
           }
           if (EPI == kEpiPartial) {
             if (row < p.M) {
@@ -663,6 +837,32 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
                 }
               }
             }
+          } else if (kCs) {
+            // C sub-tile k in staging tile k % NB -> result in place -> TMA store
+            const int b = k % NB;
+            uint8_t* const sptr = sptr0 + b * kEpiBufBytes;
+            if (has_c) {
+              if (!wait_c_sub(b)) break;
+            } else {
+              // the store issued from this tile NB sub-chunks ago must have read it
+              if (lane == 0) bulk_wait_group_read<NB - 1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint8_t* const e = sptr + sw64_chunk(lane, g);
+              const uint4 cv =
+                  has_c ? *reinterpret_cast<const uint4*>(e) : make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(e) = epilogue8(cur + 8 * g, cv, has_c, p.alpha, p.beta);
+            }
+            fence_proxy_async_smem();   // generic writes -> TMA store reads
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, sbuf0 + b * kEpiBufBytes, col0, row0);
+              bulk_commit_group();
+            }
+            if (has_c && k + NB < nsub && col0 + NB * kSubCols < p.N)
+              load_c_sub_tma(b, col0 + NB * kSubCols, row0);
           } else if (EPI == kEpiTma) {
             const uint32_t b = nstore & 1u;
             const uint32_t sbuf = sbuf0 + b * kEpiBufBytes;
@@ -730,7 +930,18 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           mbar_arrive(acce_bar(buf));
       }
       ++local;
+      if (kCs) {
+        if (have_next) load_c_head(tn);
+        t = tn;
+        have = have_next;
+      } else {
+        have = next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t);
+      }
     }
+    // C loads still in flight (a wait above gave up) must land before exit
+    for (int b = 0; b < NB; ++b)
+      if (kCs && c_pending[b] && lane == 0)
+        drain_wait(cfull_bar(ew, b), (c_loads[b] - 1u) & 1u, st, 17);
     if (EPI == kEpiTma && lane == 0) bulk_wait_group<0>();   // stores done reading smem
     tc_fence_before();
     __syncwarp();

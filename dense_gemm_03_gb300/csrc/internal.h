@@ -50,6 +50,19 @@ struct TcArgs {
   float* tail_ws;                      // [tail tile][slice][128][BN]
   unsigned long long* tail_counters;   // [tail tile][8 epilogue warps]: epoch << 32 | arrivals
   unsigned int epoch;
+  // Stream-K region (sk_tiles > 0, after the units above): the tiles
+  // sk_tile0 .. sk_tile0 + sk_tiles - 1 (in visiting order) are treated as
+  // sk_iters = sk_tiles * kb_total k-blocks, and worker w of sk_workers takes
+  // k-blocks [w*sk_iters/sk_workers, (w+1)*sk_iters/sk_workers), cut at tile
+  // boundaries into pieces.  A tile covered by several pieces is finished like
+  // a tail tile; tail_splits is then the most pieces any tile can have (the
+  // stride of tail_ws).
+  int sk_tile0, sk_tiles, sk_workers;
+  long long sk_iters;
+  // tail_halves != 0 (TMA loads, BN >= 128): the tiles after dp_tiles are
+  // computed as two units of BN/2 columns each (whole K, an MMA of N = BN/2)
+  // instead of K slices.
+  int tail_halves;
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
 };

@@ -151,11 +151,15 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * Kernel path selection, for tests and benchmarks.  0 = automatic (default);
  * 1 = tensor-memory-accelerator operand loads; 2 = predicated element loads
  * (the path taken when strides or pointers are not 16-byte aligned);
- * 3 = split-K over an fp32 workspace; 4 = (fp32 only) FFMA kernel with
- * predicated scalar loads; 5 = whole tiles only (no K-cutting of the last,
- * partial wave of tiles); 6 = no CTA pairs (one CTA per 128-row tile);
- * 7 = (fp32) FFMA kernel only, no tensor cores; 8 = (fp32) 3xTF32 tensor-core
- * kernel whatever the shape.  A forced path that cannot serve a call (e.g. TMA
+ * 3 = split-K (every tile cut into equal K slices); 4 = (fp32 only) FFMA
+ * kernel with predicated scalar loads; 5 = whole tiles only (no stream-K, no
+ * splitting of the last wave); 6 = no CTA pairs (one
+ * CTA per 128-row tile); 7 = (fp32) FFMA kernel only, no tensor cores;
+ * 8 = (fp32) 3xTF32 tensor-core kernel whatever the shape; 9 = the last,
+ * partial wave of tiles cut into two equal K slices (instead of two
+ * half-width units); 10 = stream-K over the last waves of tiles (k-block
+ * ranges shared out evenly; automatic only when there are few tiles).
+ * A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
  */
@@ -178,6 +182,18 @@ int gemm_debug_status(void);
 
 /* Describes the path the last call on this thread took (static string). */
 const char* gemm_last_path(void);
+
+/*
+ * The stream-K plan the half-precision path would use for `tiles` output
+ * tiles of `kb` k-blocks on at most `slots` concurrent workers (CTAs or CTA
+ * pairs); `all_tiles` != 0 asks for the few-tiles form (every tile's k-blocks
+ * shared out).  Writes out[0] = whole tiles computed first, out[1] = tiles
+ * whose k-blocks are shared out (0 = no stream-K), out[2] = workers sharing
+ * them, out[3] = most pieces one tile can be cut into.  Worker w of W takes
+ * k-blocks [w*I/W, (w+1)*I/W) of the I = out[1]*kb shared ones.  Host-only
+ * (no device call); returns GEMM_OK, or GEMM_ERR_NULL for a null `out`.
+ */
+int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, long long* out);
 
 /* Number of kernels the library has launched in this process (all threads,
  * all devices; launches that failed are not counted).  Nothing else --

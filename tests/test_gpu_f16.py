@@ -11,6 +11,7 @@ from helpers import check, operands, padding_untouched, run, to_dev, torch
 pytestmark = pytest.mark.gpu
 
 AUTO, MANUAL, SPLITK = 0, 2, 3
+NO_TAIL, NO_PAIR, TAIL2, SK = 5, 6, 9, 10
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -183,9 +184,7 @@ def test_streams_are_respected():
 
 
 # ---------------------------------------------------------------- last-wave balancing
-NO_TAIL = 5
-
-
+@pytest.mark.parametrize("path,mark", [(AUTO, ".halves"), (TAIL2, ".tail"), (SK, ".sk")])
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
     (2000, 2600, 4096, 4096, 2600, 2600),     # 176 tiles: the last 24 cut into 2 K slices
     (2000, 2600, 4100, 4104, 2600, 2600),     # ragged last k-block
@@ -194,15 +193,18 @@ NO_TAIL = 5
     (1300, 4000, 4096, 4104, 4008, 4000),     # padded operands
 ])
 @pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
-def test_tail_parity(M, N, K, lda, ldb, ldc, alpha, beta, c_fill):
+def test_tail_parity(path, mark, M, N, K, lda, ldb, ldc, alpha, beta, c_fill):
+    """The last wave balanced by half-width units, by two K slices per tile or
+    by stream-K (shared k-block ranges); against the oracle and against whole
+    tiles."""
     A, B, C0 = operands(40 + M + N + lda, M, N, K, lda, ldb, ldc, np.float16, c_fill=c_fill)
-    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc)
-    assert ".tail" in taken, taken
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc, path=path)
+    assert mark in taken, taken
     check("f16", got, A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc,
           rows=oracle.sample_rows(M, block=64), cols=oracle.sample_cols(N, block=32))
     assert padding_untouched(got, C0, N)
     whole, taken2 = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc, path=NO_TAIL)
-    assert ".tail" not in taken2
+    assert ".tail" not in taken2 and ".sk" not in taken2
     ref, absd = oracle.gemm(A, B, C0, alpha, beta, M=M, N=N, K=K, lda=lda, ldb=ldb, ldc=ldc,
                             rows=list(range(0, M, 97)), with_absdot=True)
     r = oracle.compare(got[::97, :N].astype(np.float64), whole[::97, :N].astype(np.float64),
@@ -210,22 +212,50 @@ def test_tail_parity(M, N, K, lda, ldb, ldc, alpha, beta, c_fill):
     assert r["ok"], r
 
 
-def test_tail_deterministic():
-    """192 tiles on 152 SMs: the last 40 are cut into two K slices; whichever
-    slice finishes last, the result is the same bits."""
+@pytest.mark.parametrize("path,mark", [(AUTO, ".halves"), (TAIL2, ".tail"), (SK, ".sk")])
+def test_tail_deterministic(path, mark):
+    """Shared tiles are summed in k order whichever piece finishes last (and
+    whether or not the finishing piece published its own partial sums), so
+    repeated calls give the same bits."""
     M, N, K = 2000, 3000, 4096
     A, B, C0 = operands(77, M, N, K, K, N, N, np.float16)
-    r1, taken = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
-    assert ".tail" in taken
-    for _ in range(2):
-        r2, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    r1, taken = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=path)
+    assert mark in taken
+    for _ in range(3):
+        r2, _ = run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=path)
         assert np.array_equal(r1.view(np.uint16), r2.view(np.uint16))
     check("f16", r1, A, B, C0, 1.5, 0.5, M, N, K, K, N, N,
           rows=oracle.sample_rows(M), cols=oracle.sample_cols(N))
 
 
+@pytest.mark.parametrize("M,N,K,path,mark", [
+    (2000, 2600, 4096, SK, ".pair.bn256.tma.epi_tma.sk"),    # CTA pairs, last waves shared
+    (2000, 2601, 2048, SK, ".epi_manual.sk"),                # N % 8 != 0, predicated epilogue
+    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 88 pair tiles: 12 halved
+    (2560, 2560, 1024, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 100 pair tiles: 24 halved
+    (2560, 2560, 1024, NO_PAIR, ".bn256.tma.epi_tma.halves"),     # 200 CTA tiles, halved tail
+    (3300, 2001, 700, AUTO, ".epi_manual.halves"),                # predicated epilogue, halved
+    (16, 8192, 4096, AUTO, ".bn128.tma.epi_tma.sk"),     # skinny: every tile shared
+    (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma.sk"),      # tall: every tile shared
+    (64, 128, 4096, AUTO, ".sk"),                        # one tile cut into many pieces
+    (100, 300, 1000, AUTO, ".sk"),                       # ragged, small
+])
+def test_balanced_schedules_integers_exact(M, N, K, path, mark):
+    """Entries in {-1, 0, 1}: partial sums are integers below 2^24, exact in
+    fp32 however the k-blocks are shared out, so C is exactly the oracle's
+    value rounded once to half."""
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A = rng.integers(-1, 2, size=(M, K)).astype(np.float16)
+    B = rng.integers(-1, 2, size=(K, N)).astype(np.float16)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float16)
+    got, taken = run("f16", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=path)
+    assert mark in taken, taken
+    rows = list(range(M)) if M * N * K <= 4e9 else oracle.sample_rows(M, block=32)
+    ref = oracle.gemm(A, B, C0, 2.0, -1.0, rows=rows)
+    assert np.array_equal(got[rows].view(np.uint16), _exact16(ref).view(np.uint16))
+
+
 # ---------------------------------------------------------------- CTA pairs (cta_group::2)
-NO_PAIR = 6
 
 
 @pytest.mark.parametrize("M,N,K,ldc", [
@@ -234,13 +264,15 @@ NO_PAIR = 6
     (300, 1000, 1000, 1000),     # ragged everything
     (257, 512, 256, 512),        # the second CTA of the last pair has one row
     (1000, 1001, 700, 1001),     # N % 8 != 0: predicated epilogue on pairs
-    (2048, 2048, 4096, 2048),    # enough tiles for the last-wave split
+    (2048, 2048, 4096, 2048),    # 64 pair tiles, one partial wave
 ])
 @pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
 def test_pair_parity(M, N, K, ldc, alpha, beta, c_fill):
+    """Whole tiles forced (no stream-K), so that even the shapes with few tiles
+    run on CTA pairs."""
     A, B, C0 = operands(60 + M + N + K, M, N, K, K, N, ldc, np.float16, c_fill=c_fill)
-    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, ldc)
-    if (M + 127) // 128 >= 2 and N > 128 and taken.find("splitk") < 0:
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, ldc, path=NO_TAIL)
+    if (M + 127) // 128 >= 2 and N > 128:
         assert ".pair." in taken, taken
     big = M * N * K > 2e9
     check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, ldc,
@@ -255,12 +287,8 @@ def test_pair_identity_exact():
     B = synthetic.uniform(9, 2, (K, N), dtype=np.float16)
     C0 = np.full((M, N), np.nan, dtype=np.float16)
     import dense_gemm_03_gb300 as g
-    prev = g.force_splits(1)
-    try:
-        got, taken = run("f16", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
-    finally:
-        g.force_splits(prev)
-    assert ".pair." in taken or "splitk" in taken
+    got, taken = run("f16", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=NO_TAIL)
+    assert ".pair." in taken
     assert np.array_equal(got.view(np.uint16), B.view(np.uint16))
 
 
