@@ -15,7 +15,8 @@ import os
 import threading
 
 __all__ = [
-    "GemmError", "lib", "library_path", "gemm_f16", "sgemm_f32", "gemm_f16_host",
+    "GemmError", "lib", "library_path", "gemm_f16", "gemm_f16_f32out", "f32_to_f16",
+    "sgemm_f32", "gemm_f16_host",
     "sgemm_f32_host", "gemm_f16_splitk_noalloc", "l2_flush", "force_path", "force_splits", "set_wait_limit_ns",
     "debug_status", "last_path", "launch_count", "plan_stream_k", "release", "EXPORTS",
 ]
@@ -30,7 +31,8 @@ EXPORTS = (
     "gemm_f16", "gemm_f16_ld", "sgemm_f32", "sgemm_f32_ld", "gemm_f16_host", "sgemm_f32_host",
     "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
     "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
-    "gemm_f16_splitk_noalloc", "gemm_launch_count", "gemm_plan_stream_k",
+    "gemm_f16_splitk_noalloc", "gemm_launch_count", "gemm_plan_stream_k", "gemm_f16_f32out",
+    "gemm_f32_to_f16",
 )
 
 PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
@@ -65,6 +67,10 @@ def lib():
                 fn = getattr(L, name)
                 fn.restype = i
                 fn.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, vp]
+            L.gemm_f16_f32out.restype = i
+            L.gemm_f16_f32out.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, vp]
+            L.gemm_f32_to_f16.restype = i
+            L.gemm_f32_to_f16.argtypes = [vp, vp, ctypes.c_longlong, vp]
             L.gemm_f16_splitk_noalloc.restype = i
             L.gemm_f16_splitk_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, i, vp]
             L.gemm_l2_flush.restype = i
@@ -146,6 +152,25 @@ def gemm_f16(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb
                            int(K if lda is None else lda), int(N if ldb is None else ldb),
                            int(N if ldc is None else ldc), float(alpha), float(beta), s)
     _check(rc, "gemm_f16")
+
+
+def gemm_f16_f32out(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None,
+                    ldc=None, stream=None):
+    """C := alpha*A*B + beta*C with device fp16 A, B and an fp32 C."""
+    M, N, K = _dims(A, B, M, N, K)
+    rc = lib().gemm_f16_f32out(_addr(A), _addr(B), _addr(C), M, N, K,
+                               int(K if lda is None else lda), int(N if ldb is None else ldb),
+                               int(N if ldc is None else ldc), float(alpha), float(beta),
+                               _stream(stream))
+    _check(rc, "gemm_f16_f32out")
+
+
+def f32_to_f16(src, dst, n=None, stream=None):
+    """dst := src rounded to half (nearest, ties to even), n elements."""
+    if n is None:
+        n = src.numel() if hasattr(src, "numel") else src.size
+    _check(lib().gemm_f32_to_f16(_addr(src), _addr(dst), int(n), _stream(stream)),
+           "gemm_f32_to_f16")
 
 
 def sgemm_f32(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None, ldc=None,

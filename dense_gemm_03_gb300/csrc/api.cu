@@ -299,10 +299,13 @@ int check_common(const void* A, const void* B, const void* C, int M, int N, int 
 
 thread_local char t_path_buf[96];
 
-int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
-                    long long lda, long long ldb, long long ldc, float alpha, float beta,
-                    cudaStream_t stream) {
+// Half-precision operands, fp32 accumulation; C is half (c_f32 false) or
+// float (c_f32 true).
+int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int M, int N, int K,
+                  long long lda, long long ldb, long long ldc, float alpha, float beta,
+                  cudaStream_t stream) {
   if (int rc = check_common(A, B, C, M, N, K, lda, ldb, ldc, alpha, 2)) return rc;
+  if (c_f32 && (reinterpret_cast<uintptr_t>(C) & 3u)) return GEMM_ERR_ARG;
   if (M == 0 || N == 0) {
     t_last_path = "noop";
     return GEMM_OK;
@@ -311,10 +314,12 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   if (int rc = device_state(&d, nullptr)) return rc;
 
   if (alpha == 0.0f || K == 0) {
-    t_last_path = "f16.scale";
-    return launch_scale_f16(C, ldc, M, N, beta, scale_grid(*d, 1ll * M * N), stream) == cudaSuccess
-               ? GEMM_OK
-               : GEMM_ERR_CUDA;
+    t_last_path = c_f32 ? "f16f32.scale" : "f16.scale";
+    const int g = scale_grid(*d, 1ll * M * N);
+    const cudaError_t e =
+        c_f32 ? launch_scale_f32(static_cast<float*>(C), ldc, M, N, beta, g, stream)
+              : launch_scale_f16(static_cast<uint16_t*>(C), ldc, M, N, beta, g, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
 
   const int force = g_force_path.load();
@@ -361,14 +366,16 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   // of 8 halves it would also write the elements just past column N (measured
   // on GB300), which may belong to the caller.  Such shapes take the predicated
   // epilogue.
-  const bool c_tma = aligned16(C) && (ldc * 2) % 16 == 0 && N % 8 == 0;
+  const bool c_tma = !c_f32 && aligned16(C) && (ldc * 2) % 16 == 0 && N % 8 == 0;
   int load = (ab_tma && force != 2) ? kLoadTma : kLoadManual;
-  int epi = (c_tma && force != 2) ? kEpiTma : kEpiManual;
+  int epi = c_f32 ? kEpiF32 : ((c_tma && force != 2) ? kEpiTma : kEpiManual);
 
   TcArgs a{};
   a.A = A;
   a.B = B;
-  a.C = C;
+  a.C = c_f32 ? nullptr : static_cast<uint16_t*>(C);
+  a.Cf = c_f32 ? static_cast<float*>(C) : nullptr;
+  a.vec_c = c_f32 && aligned16(C) && ldc % 4 == 0;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -516,13 +523,14 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
   if (epi == kEpiTma) {
     // epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle
-    if (int rc = make_map_f16(&tmC, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
+    if (int rc = make_map_f16(&tmC, a.C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
   }
   // one CTA (pair) per worker; with stream-K exactly sk_workers of them
   const long long nw = a.sk_tiles > 0 ? a.sk_workers : std::min<long long>(a.num_units, workers);
   if (pair) {
     const int grid = 2 * static_cast<int>(nw);
-    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s", kPairPathNames[epi], cut, how);
+    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s",
+             c_f32 ? "f16.tc.pair.bn256.tma.epi_f32" : kPairPathNames[epi], cut, how);
     t_last_path = t_path_buf;
     if (launch_gemm_f16_tc_pair(epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
@@ -530,11 +538,21 @@ int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, in
   }
   const int grid = static_cast<int>(nw);
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s", kPathNames[bi][load][epi], cut, how);
+  if (c_f32)
+    snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.bn%d.%s.epi_f32%s%s", bn,
+             load == kLoadTma ? "tma" : "manual", cut, how);
+  else
+    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s", kPathNames[bi][load][epi], cut, how);
   t_last_path = t_path_buf;
   if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return GEMM_OK;
+}
+
+int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,
+                    long long lda, long long ldb, long long ldc, float alpha, float beta,
+                    cudaStream_t stream) {
+  return gemm_f16_impl(A, B, C, false, M, N, K, lda, ldb, ldc, alpha, beta, stream);
 }
 
 int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int K, long long lda,
@@ -696,6 +714,25 @@ int gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, in
 int gemm_f16_ld(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, int lda,
                 int ldb, int ldc, float alpha, float beta, cudaStream_t stream) {
   return gemm_f16_device(A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, stream);
+}
+
+int gemm_f16_f32out(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int lda,
+                    int ldb, int ldc, float alpha, float beta, cudaStream_t stream) {
+  return gemm_f16_impl(A, B, C, true, M, N, K, lda, ldb, ldc, alpha, beta, stream);
+}
+
+int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t stream) {
+  if (n < 0) return GEMM_ERR_DIM;
+  if (n == 0) return GEMM_OK;
+  if (src == nullptr || dst == nullptr) return GEMM_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(src) & 3u) || (reinterpret_cast<uintptr_t>(dst) & 1u))
+    return GEMM_ERR_ARG;
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  t_last_path = "f32_to_f16";
+  return launch_f32_to_f16(src, dst, n, scale_grid(*d, (n + 7) / 8), stream) == cudaSuccess
+             ? GEMM_OK
+             : GEMM_ERR_CUDA;
 }
 
 int sgemm_f32(const float* A, const float* B, float* C, int M, int N, int K, float alpha,

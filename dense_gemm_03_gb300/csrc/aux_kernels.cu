@@ -221,7 +221,44 @@ __global__ void split_tf32_t_kernel(const float* __restrict__ src, long long lds
   }
 }
 
+// dst[i] = src[i] rounded to the nearest half (ties to even), eight elements
+// per thread and step: two 16-byte loads and one 16-byte store when both
+// pointers are 16-byte aligned (VEC), element accesses otherwise.
+template <bool VEC>
+__global__ void f32_to_f16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
+                                  long long n) {
+  const long long groups = (n + 7) / 8;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < groups;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long i = 8 * g;
+    if (VEC && i + 8 <= n) {
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(src + i));
+      const float4 b = __ldcs(reinterpret_cast<const float4*>(src + i) + 1);
+      const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
+      const __half2 h2 = __floats2half2_rn(b.x, b.y), h3 = __floats2half2_rn(b.z, b.w);
+      uint4 o;
+      memcpy(&o.x, &h0, 4);
+      memcpy(&o.y, &h1, 4);
+      memcpy(&o.z, &h2, 4);
+      memcpy(&o.w, &h3, 4);
+      __stcs(reinterpret_cast<uint4*>(dst + i), o);
+    } else {
+      for (long long j = i; j < n && j < i + 8; ++j) dst[j] = __half_as_ushort(__float2half_rn(src[j]));
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int grid,
+                              cudaStream_t stream) {
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0;
+  if (vec)
+    f32_to_f16_kernel<true><<<grid, 256, 0, stream>>>(src, dst, n);
+  else
+    f32_to_f16_kernel<false><<<grid, 256, 0, stream>>>(src, dst, n);
+  return counted_launch(cudaGetLastError());
+}
 
 cudaError_t launch_split_tf32_t(const float* src, long long lds, float* big, float* small,
                                 long long ldd, int rows, int cols, int grid, cudaStream_t stream) {

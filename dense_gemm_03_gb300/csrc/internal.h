@@ -22,7 +22,7 @@ struct DeviceStatus;
 enum LoadMode : int { kLoadTma = 0, kLoadManual = 1 };
 // Epilogue modes: TMA load/store of C, predicated element access of C, or
 // raw fp32 partial sums to the split-K workspace.
-enum EpiMode : int { kEpiTma = 0, kEpiManual = 1, kEpiPartial = 2 };
+enum EpiMode : int { kEpiTma = 0, kEpiManual = 1, kEpiPartial = 2, kEpiF32 = 3 };
 
 struct TcArgs {
   const uint16_t* A;
@@ -59,6 +59,11 @@ struct TcArgs {
   // stride of tail_ws).
   int sk_tile0, sk_tiles, sk_workers;
   long long sk_iters;
+  // kEpiF32: C is fp32 (Cf, ldc in floats) and written straight from
+  // registers, with 16-byte accesses when vec_c (Cf and ldc 16-byte aligned)
+  // and predicated element accesses otherwise.
+  float* Cf;
+  int vec_c;
   // tail_halves != 0 (TMA loads, BN >= 128): the tiles after dp_tiles are
   // computed as two units of BN/2 columns each (whole K, an MMA of N = BN/2)
   // instead of K slices.
@@ -73,6 +78,18 @@ cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtens
                                const CUtensorMap& tmB, const CUtensorMap& tmC, const TcArgs& args,
                                int grid, cudaStream_t stream);
 int tc_threads(int load_mode);
+
+// The same GEMM with an fp32 C (epilogue kEpiF32; gemm_f16_f32out.cu).
+cudaError_t launch_gemm_f16_tc_f32(int bn, int load_mode, const CUtensorMap& tmA,
+                                   const CUtensorMap& tmB, const TcArgs& args, int grid,
+                                   cudaStream_t stream);
+cudaError_t launch_gemm_f16_tc_pair_f32(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                        const TcArgs& args, int grid, cudaStream_t stream);
+int tc_pair_max_clusters_f32();
+
+// fp32 -> fp16 conversion of n elements, round to nearest even.
+cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int grid,
+                              cudaStream_t stream);
 
 // The same GEMM on CTA pairs (clusters of 2 sharing tcgen05.mma.cta_group::2):
 // 256 x 256 output tiles, TMA operand loads only, epilogue kEpiTma or

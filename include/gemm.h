@@ -87,6 +87,30 @@ int gemm_f16_ld(const uint16_t* A, const uint16_t* B, uint16_t* C,
                 int M, int N, int K, int lda, int ldb, int ldc,
                 float alpha, float beta, cudaStream_t stream);
 
+/*
+ * C := alpha*A*B + beta*C with half A and B and a FLOAT C: fp32 accumulation
+ * and an fp32 epilogue, with no rounding to half.  This is the WMMA kernel of
+ * the "Tensorcore_wmma_vs_fp32 test code" page (section on the WMMA tensor
+ * core GEMM kernel), which stores its fp32 accumulator fragment to a float C;
+ * alpha = 1, beta = 0 gives exactly that product.  Leading dimensions in
+ * elements (lda >= K, ldb >= N, ldc >= N).  C must be 4-byte aligned
+ * (GEMM_ERR_ARG otherwise); with beta == 0 C is not read.  Otherwise the
+ * rules of gemm_f16_ld apply (same kernels and scheduling).
+ */
+int gemm_f16_f32out(const uint16_t* A, const uint16_t* B, float* C,
+                    int M, int N, int K, int lda, int ldb, int ldc,
+                    float alpha, float beta, cudaStream_t stream);
+
+/*
+ * dst[i] := src[i] rounded to the nearest half, ties to even, for 0 <= i < n
+ * (the float-to-half kernel of the same page, section on the float - half
+ * conversion kernel): values beyond the half range become +-Inf, NaN stays
+ * NaN.  Device pointers, src 4-byte and dst 2-byte aligned (GEMM_ERR_ARG
+ * otherwise); 16-byte aligned pointers take the vectorised path.  n < 0 is
+ * GEMM_ERR_DIM, n == 0 a no-op.  Asynchronous on `stream`.
+ */
+int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t stream);
+
 /* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 operands and
  * result.  Shapes of at least 256 x 256 x 64 run on the tensor cores as three
  * tf32 products of split operands (A = Ab + As, B = Bb + Bs; the As*Bs term,

@@ -6,9 +6,12 @@ links or runs this package, and this package imports nothing from it.
 
 The arithmetic lives in ``gemm_oracle.c`` (plain triple loop, double, k
 ascending).  This module builds and loads it, widens half operands to float32
-(exact), and holds the parity tolerances:
+(exact), holds the parity tolerances, and gives the float-to-half rounding
+that the conversion entry point must reproduce bit for bit:
 
 * fp16 path: |gpu - ref| <= 2e-3 * sum_k |a_ik||b_kj| + ulp16(ref), per element;
+* fp16 operands with an fp32 C: the same bound with the output rounding term
+  of binary32, 2e-3 * sum_k |a_ik||b_kj| + ulp32(ref);
 * fp32 path: |gpu - ref| <= 1e-6 * K * max|A| * max|B| + ulp32(ref), per element.
 
 ulp16/ulp32 are the spacings of binary16/binary32 at |ref| (the subnormal
@@ -218,6 +221,20 @@ def tol_f16(ref, absdot) -> np.ndarray:
 
 def tol_f32(ref, K: int, max_a: float, max_b: float) -> np.ndarray:
     return 1e-6 * float(K) * float(max_a) * float(max_b) + ulp32(ref)
+
+
+def tol_f16_f32out(ref, absdot) -> np.ndarray:
+    return 2e-3 * np.asarray(absdot, dtype=np.float64) + ulp32(ref)
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """binary32 -> binary16, round to nearest with ties to even, overflow to
+    +-Inf, NaN to NaN (IEEE 754 conversion; numpy's cast implements it).
+    The float-to-half kernel of the "Tensorcore_wmma_vs_fp32 test code" page
+    (section on the float - half conversion kernel) applies __float2half,
+    which rounds the same way."""
+    with np.errstate(over="ignore", invalid="ignore"):   # overflow to Inf is the rule
+        return np.asarray(x, dtype=np.float32).astype(np.float16)
 
 
 def compare(got, ref, tol):

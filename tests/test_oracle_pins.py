@@ -285,6 +285,33 @@ def test_tol_f16_accepts_rounded_reference():
     assert oracle.compare(rounded, ref, oracle.tol_f16(ref, absd))["ok"]
 
 
+def test_tol_f16_f32out_is_the_fp16_bound_with_binary32_rounding():
+    ref = np.array([1.0, -3.0, 1000.0, 0.0])
+    absd = np.array([10.0, 0.0, 5.0, 0.0])
+    want = 2e-3 * absd + np.array([2.0 ** -23, 2.0 ** -22, 2.0 ** -14, 2.0 ** -149])
+    assert np.array_equal(oracle.tol_f16_f32out(ref, absd), want)
+
+
+# ---------------------------------------------------------------- float -> half rounding
+
+def test_f32_to_f16_worked_values():
+    """IEEE binary16 facts: the largest finite half is 65504 (0x7BFF); values
+    at or beyond 65520 (halfway to the next binade step) overflow to Inf; the
+    smallest subnormal is 2^-24 (0x0001); ties round to the even neighbour
+    (2049 -> 2048, 2051 -> 2052 = 0x6802 since the spacing above 2048 is 2,
+    2^-25 -> 0, 3*2^-25 -> 2*2^-24)."""
+    cases = [
+        (1.0 / 3.0, 0x3555), (1.0, 0x3C00), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+        (65504.0, 0x7BFF), (65519.0, 0x7BFF), (65520.0, 0x7C00), (-1e6, 0xFC00),
+        (2049.0, 0x6800), (2051.0, 0x6802), (2.0 ** -24, 0x0001), (2.0 ** -25, 0x0000),
+        (3 * 2.0 ** -25, 0x0002), (2.0 ** -14, 0x0400), (float("inf"), 0x7C00),
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float32)
+    got = oracle.f32_to_f16(x).view(np.uint16)
+    assert [int(v) for v in got] == [c[1] for c in cases]
+    assert np.isnan(oracle.f32_to_f16(np.array([np.nan], np.float32))).all()
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def test_compare_flags_planted_error_and_nan():
