@@ -247,6 +247,36 @@ def run_ours(args, rank, world):
     tflops16 = flops / (mean16 * 1e-3) / 1e12
     tflops32 = flops / (mean32 * 1e-3) / 1e12
 
+    # fp16 operands with an fp32 C, and the fp32 -> fp16 conversion of C
+    f32c = torch.from_numpy(synthetic.uniform(seed, synthetic.STREAM_C, (M, N),
+                                              dtype=np.float32)).cuda()
+    fo = lambda: g.gemm_f16_f32out(dA, dB, f32c, F16_CFG["alpha"], F16_CFG["beta"], stream=stream)
+    ms_fo = timed_replays(fo, max(20, args.steps // 20), 5, stream, flush_bytes)
+    path_fo = g.last_path()
+    conv_dst = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    cv = lambda: g.f32_to_f16(f32c, conv_dst, stream=stream)
+    ms_cv = timed_replays(cv, max(20, args.steps // 20), 5, stream, flush_bytes)
+    t_fo = sum(ms_fo) / len(ms_fo)
+    t_cv = sum(ms_cv) / len(ms_cv)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    extra = {
+        "f16_f32out": {
+            "workload": "fp16 A, B -> fp32 C = 1.5*A*B + 0.5*C, M=N=K=4096",
+            "us": round(t_fo * 1e3, 2),
+            "tflops": round(2.0 * M * N * K / (t_fo * 1e-3) / 1e12, 1),
+            "frac_tensor": round(2.0 * M * N * K / (t_fo * 1e-3) / 1e12 / peak16_local, 4),
+            "kernel_path": path_fo,
+        },
+        "f32_to_f16": {
+            "workload": "fp32 -> fp16 conversion of a 4096 x 4096 matrix",
+            "us": round(t_cv * 1e3, 2),
+            "gb_s": round(6.0 * M * N / (t_cv * 1e-3) / 1e9, 1),
+            "frac_hbm": round(6.0 * M * N / (t_cv * 1e-3) / 1e9 / hbm_peak, 4),
+            "algorithmic_bytes": 6 * M * N,
+        },
+    }
+    del f32c, conv_dst
+
     # the other workloads of the metric, timed the same way (context for the headline)
     shapes = []
     if not args.no_shapes:
@@ -366,6 +396,7 @@ def run_ours(args, rank, world):
             "api": "gemm_f16_host (pinned host buffers)",
         },
         "edge_shapes": shapes,
+        **extra,
         "gpu_launches": LaunchTally.total,
         "clocks": clocks,
         "wall_s_timed": round(t_wall1 - t_wall0, 3),
