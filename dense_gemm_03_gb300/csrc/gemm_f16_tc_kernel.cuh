@@ -11,25 +11,28 @@
 // (section on tiling and data movement); on sm_103a they become a
 // multi-stage mbarrier ring fed by TMA and drained by tcgen05.mma.
 //
-// One CTA per SM, persistent over work units, warp-specialised:
+// One CTA per SM (or one CTA pair per two SMs), persistent over work units,
+// warp-specialised:
 //   producer warp(s)  TMA tile loads (or, for unaligned operands, 4 warps of
 //                     predicated element loads written in the same layout)
-//   MMA warp          one thread issues tcgen05.mma (M=128, N=BN, K=16) into a
-//                     double-buffered TMEM accumulator (2 x BN fp32 columns)
+//   MMA warp          one thread issues tcgen05.mma (M=128, or M=256 on a CTA
+//                     pair; N=BN or BN/2; K=16) into a double-buffered TMEM
+//                     accumulator (2 x BN fp32 columns)
 //   8 epilogue warps  warp (q, h) owns TMEM lanes 32q..32q+31 (= tile rows)
-//                     and the h-th half of the tile's columns; in 32-column
+//                     and the h-th half of the unit's columns; in 32-column
 //                     sub-chunks it loads the accumulator (the next sub-chunk's
-//                     load is in flight while the current one is converted),
-//                     applies alpha/beta in fp32 with C prefetched into
-//                     registers, rounds to fp16 and stores through a
-//                     double-buffered 2 KB staging tile by TMA (or with
-//                     predicated stores, or as fp32 split-K partials).
+//                     load in flight), applies alpha/beta in fp32, rounds to
+//                     fp16 and stores by TMA through 2 KB staging tiles (on
+//                     CTA pairs C itself is TMA-loaded into those tiles during
+//                     the main loop), or stores fp16/fp32 from registers with
+//                     predicated accesses, or publishes fp32 partial sums.
 // The epilogue of one unit overlaps the main loop of the next.
 //
-// A unit is a whole output tile, a split-K slice, or a K slice of one of the
-// tiles of the last, partial wave ("tail"): those write fp32 partial sums and
-// the slice that finishes last (counted per launch) adds them up in slice
-// order and runs the epilogue, so no CTA ever waits for another.
+// A unit is a whole output tile, half of one (its columns split in two, for
+// the last partial wave), a split-K slice, or a piece of a stream-K range.
+// Pieces of a shared tile publish fp32 partial sums; the piece that finishes
+// last (counted per launch) adds them up in k order and runs the epilogue, so
+// no CTA ever waits for another.
 //
 // Shared-memory operand layouts (128-byte swizzle, 1024-byte aligned):
 //   A stage: 128 rows x 64 halves, K-major; row r at r*128 B, 16-byte chunk c
