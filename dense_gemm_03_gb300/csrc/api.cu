@@ -516,9 +516,12 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
                     : static_cast<int>(a.dp_tiles * static_cast<long long>(splits) +
                                        (units_tiles - a.dp_tiles) * a.tail_splits);
 
+  // At most 64 rows on 128-wide single-CTA tiles: stage only the A rows that
+  // exist (32 or 64), which leaves room for more stages of B.
+  const int am = (load == kLoadTma && !pair && bn == 128 && M <= 64) ? (M <= 32 ? 32 : 64) : kBM;
   CUtensorMap tmA{}, tmB{}, tmC{};
   if (load == kLoadTma) {
-    if (int rc = make_map_f16(&tmA, A, M, K, lda, 64, kBM)) return rc;
+    if (int rc = make_map_f16(&tmA, A, M, K, lda, 64, am)) return rc;
     if (int rc = make_map_f16(&tmB, B, K, N, ldb, 64, 64)) return rc;
   }
   if (epi == kEpiTma) {
@@ -538,15 +541,18 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   }
   const int grid = static_cast<int>(nw);
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
+  const char* rows = am == 32 ? ".a32" : (am == 64 ? ".a64" : "");
   if (c_f32)
-    snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.bn%d.%s.epi_f32%s%s", bn,
-             load == kLoadTma ? "tma" : "manual", cut, how);
+    snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.bn%d.%s.epi_f32%s%s%s", bn,
+             load == kLoadTma ? "tma" : "manual", rows, cut, how);
   else
-    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s", kPathNames[bi][load][epi], cut, how);
+    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s%s", kPathNames[bi][load][epi], rows, cut,
+             how);
   t_last_path = t_path_buf;
-  if (launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
-    return GEMM_ERR_CUDA;
-  return GEMM_OK;
+  const cudaError_t e = am < kBM
+                            ? launch_gemm_f16_tc_skinny(am, epi, tmA, tmB, tmC, a, grid, stream)
+                            : launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream);
+  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,

@@ -63,16 +63,25 @@ constexpr int kCsBufs = 2;
 
 // PAIR: two CTAs of a cluster share each tcgen05.mma.cta_group::2 (M = 256);
 // each CTA stages its own 128 rows of A and half of the BN columns of B.
-template <int BN, bool PAIR, bool CS = false>
+// AM: rows of A staged per k-block.  128 normally; 32 or 64 for shapes with
+// M <= AM, whose stages then hold more of B (the MMA still reads 128 rows of
+// A: the rows past AM come from the stage's B region and only produce
+// accumulator rows >= M, which are never stored).
+template <int BN, bool PAIR, bool CS = false, int AM = 128>
 struct TcCfg {
   static constexpr int kBLoadCols = PAIR ? BN / 2 : BN;   // B columns staged by this CTA
   static constexpr int kBBytes = kBLoadCols * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kAStageBytes = AM * BK * 2;
+  static constexpr int kStageBytes = kAStageBytes + kBBytes;
+  // skinny stages: as many as fit beside the epilogue tiles, at most 16
+  static constexpr int kSkinnyStages = (232448 - 1024 - 1024 - 8 * 2 * kEpiBufBytes) / kStageBytes;
   static constexpr int kStages =
-      PAIR ? ((CS && kCsBufs > 2) ? 5 : 6) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+      AM < 128 ? (kSkinnyStages < 16 ? kSkinnyStages : 16)
+               : (PAIR ? ((CS && kCsBufs > 2) ? 5 : 6) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)));
   static constexpr int kTmemCols = 2 * BN;     // two accumulators
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(!PAIR || BN == 256, "pairs use 256-wide tiles");
+  static_assert(AM == 128 || (!PAIR && kStageBytes >= kABytes), "skinny stages span 128 A rows");
 };
 
 // Warp roles.  With TMA loads: 1 producer, 1 MMA and 8 epilogue warps (two
@@ -92,12 +101,12 @@ struct Roles {
 // Counters per tail tile: one per epilogue warp (at most 8).
 constexpr int kTailCounters = 8;
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, int AM = 128>
 struct Smem {
   // C read by TMA into the epilogue's staging tiles: the CTA-pair kernel with
   // TMA stores
   static constexpr bool kCs = PAIR && EPI == kEpiTma;
-  using Cfg = TcCfg<BN, PAIR, kCs>;
+  using Cfg = TcCfg<BN, PAIR, kCs, AM>;
   // 32 x 32 staging tiles per epilogue warp
   static constexpr int kBufs = kCs ? kCsBufs : 2;
   static constexpr int kWarpEpiBytes = kBufs * kEpiBufBytes;
@@ -374,15 +383,17 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* 
   }
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128>
 __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
   using R = Roles<LOAD>;
-  using L = Smem<BN, EPI, PAIR>;
+  using L = Smem<BN, EPI, PAIR, AM>;
   using Cfg = typename L::Cfg;
   constexpr bool kCs = L::kCs;
+  constexpr int kAB = Cfg::kAStageBytes;   // A bytes per stage
+  static_assert(AM == 128 || LOAD == kLoadTma, "skinny stages take TMA loads");
   constexpr int S = Cfg::kStages;
   static_assert(!PAIR || (LOAD == kLoadTma && EPI != kEpiPartial), "pair configuration");
   // Units are handed out per CTA, or per CTA pair (cluster of 2).
@@ -409,7 +420,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   // C sub-tile landed in staging tile b of epilogue warp w
   auto cfull_bar = [&](int w, int b) { return bars + 8u * (2 * S + 6 + L::kBufs * w + b); };
   auto stage_a = [&](int s) { return base + static_cast<uint32_t>(s * Cfg::kStageBytes); };
-  auto stage_b = [&](int s) { return stage_a(s) + kABytes; };
+  auto stage_b = [&](int s) { return stage_a(s) + kAB; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -470,7 +481,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             }
             // B columns this CTA stages: a half-width unit needs half of them
             const int bcols = PAIR ? t.ncols / 2 : t.ncols;
-            const uint32_t bytes = static_cast<uint32_t>(kABytes + bcols * BK * 2);
+            const uint32_t bytes = static_cast<uint32_t>(kAB + bcols * BK * 2);
             if (PAIR) {
               // Both CTAs' bytes are counted on the leader's barrier; only the
               // leader arms it (for the pair's total), the peer's copies just
@@ -526,7 +537,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             break;
           }
           uint8_t* const sa = base_ptr + stage * Cfg::kStageBytes;
-          uint8_t* const sb = sa + kABytes;
+          uint8_t* const sb = sa + kAB;
           const int k0 = kb * BK;
           // A: 128 rows x 8 chunks of 8 halves.
 #pragma unroll 4
@@ -998,13 +1009,13 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   // the MMA warp only after all epilogue warps have signalled tmem_free.
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128>
 cudaError_t configure(int dev) {
-  using L = Smem<BN, EPI, PAIR>;
+  using L = Smem<BN, EPI, PAIR, AM>;
   static bool configured[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1013,14 +1024,14 @@ cudaError_t configure(int dev) {
   return cudaSuccess;
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                        const TcArgs& args, int grid, cudaStream_t stream) {
-  using L = Smem<BN, EPI, PAIR>;
+  using L = Smem<BN, EPI, PAIR, AM>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if ((e = configure<BN, LOAD, EPI, PAIR>(dev)) != cudaSuccess) return e;
+  if ((e = configure<BN, LOAD, EPI, PAIR, AM>(dev)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(Roles<LOAD>::kThreads, 1, 1);
@@ -1035,7 +1046,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR>, tmA, tmB, tmC, args);
+  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM>, tmA, tmB, tmC, args);
   if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());
 }

@@ -87,6 +87,12 @@ cudaError_t launch_gemm_f16_tc_pair_f32(const CUtensorMap& tmA, const CUtensorMa
                                         const TcArgs& args, int grid, cudaStream_t stream);
 int tc_pair_max_clusters_f32();
 
+// The same GEMM (128-wide tiles, TMA loads, one CTA per tile) for M <= am,
+// staging am = 32 or 64 rows of A per k-block (gemm_f16_skinny.cu).
+cudaError_t launch_gemm_f16_tc_skinny(int am, int epi_mode, const CUtensorMap& tmA,
+                                      const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                      const TcArgs& args, int grid, cudaStream_t stream);
+
 // fp32 -> fp16 conversion of n elements, round to nearest even.
 cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int grid,
                               cudaStream_t stream);

@@ -235,7 +235,7 @@ def test_tail_deterministic(path, mark):
     (2560, 2560, 1024, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 100 pair tiles: 24 halved
     (2560, 2560, 1024, NO_PAIR, ".bn256.tma.epi_tma.halves"),     # 200 CTA tiles, halved tail
     (3300, 2001, 700, AUTO, ".epi_manual.halves"),                # predicated epilogue, halved
-    (16, 8192, 4096, AUTO, ".bn128.tma.epi_tma.sk"),     # skinny: every tile shared
+    (16, 8192, 4096, AUTO, ".bn128.tma.epi_tma.a32.sk"),   # skinny: every tile shared
     (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma.sk"),      # tall: every tile shared
     (64, 128, 4096, AUTO, ".sk"),                        # one tile cut into many pieces
     (100, 300, 1000, AUTO, ".sk"),                       # ragged, small
@@ -339,3 +339,23 @@ def test_odd_pointers_are_rejected():
     f = t.zeros(4096, dtype=t.float32, device="cuda")
     with pytest.raises(g.GemmError):
         g.sgemm_f32(f, f.data_ptr() + 2, f[1024:], 1.0, 0.0, M=8, N=8, K=8)
+
+
+# ---------------------------------------------------------------- skinny shapes (A rows staged: 32 or 64)
+@pytest.mark.parametrize("M,N,K,mark", [
+    (1, 300, 2000, ".a32"),
+    (16, 8192, 2048, ".a32.sk"),
+    (31, 1000, 700, ".a32"),
+    (32, 1000, 700, ".a32"),
+    (33, 1000, 700, ".a64"),
+    (64, 4096, 1024, ".a64"),
+    (17, 1001, 513, ".epi_manual.a32"),     # N % 8 != 0: predicated epilogue
+])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
+def test_skinny_parity(M, N, K, mark, alpha, beta, c_fill):
+    """At most 64 rows: only the rows of A that exist are staged; the MMA's
+    other rows read the stage's B region and must never reach C."""
+    A, B, C0 = operands(900 + M + N, M, N, K, K, N, N, np.float16, c_fill=c_fill)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, N)
+    assert mark in taken, taken
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
