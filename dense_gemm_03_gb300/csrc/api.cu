@@ -602,11 +602,13 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
                               static_cast<int>(std::min<long long>(ttiles, 16ll * d->sm_count)),
                               stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
-      CUtensorMap mAb{}, mAs{}, mBb{}, mBs{};
+      CUtensorMap mAb{}, mAs{}, mBb{}, mBs{}, mBbh{}, mBsh{};
       if (int rc = make_map_f32(&mAb, Ab, M, K, K2, 32, 128)) return rc;
       if (int rc = make_map_f32(&mAs, As, M, K, K2, 32, 128)) return rc;
       if (int rc = make_map_f32(&mBb, Bb, N, K, K2, 32, 128)) return rc;
       if (int rc = make_map_f32(&mBs, Bs, N, K, K2, 32, 128)) return rc;
+      if (int rc = make_map_f32(&mBbh, Bb, N, K, K2, 32, 64)) return rc;
+      if (int rc = make_map_f32(&mBsh, Bs, N, K, K2, 32, 64)) return rc;
       Tf32Args t{};
       t.Ab = Ab;
       t.As = As;
@@ -622,15 +624,22 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       t.tiles_m = (M + 255) / 256;
       t.tiles_n = (N + 255) / 256;
       t.kb_total = (K + 31) / 32;
-      t.num_units = t.tiles_m * t.tiles_n;
+      // the tiles of the last, partial wave run as two half-width units each
+      // when the halves fit in one wave
+      const int tiles = t.tiles_m * t.tiles_n;
+      const int rem = tiles % pairs;
+      const bool halves = force != 5 && rem > 0 && 2 * rem <= pairs;
+      t.dp_tiles = halves ? tiles - rem : tiles;
+      t.num_units = t.dp_tiles + 2 * (tiles - t.dp_tiles);
       t.group_m = 8;
       t.vec_c = aligned16(C) && ldc % 4 == 0;
       t.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
       t.status = d->status;
       const int grid = 2 * std::min(t.num_units, pairs);
-      t_last_path = "f32.3xtf32.pair";
-      return launch_sgemm_3xtf32(mAb, mAs, mBb, mBs, t, grid, stream) == cudaSuccess ? GEMM_OK
-                                                                                     : GEMM_ERR_CUDA;
+      t_last_path = halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair";
+      return launch_sgemm_3xtf32(mAb, mAs, mBb, mBs, mBbh, mBsh, t, grid, stream) == cudaSuccess
+                 ? GEMM_OK
+                 : GEMM_ERR_CUDA;
     }
   }
   const bool vec = force != 4 && aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 &&

@@ -138,14 +138,19 @@ struct Tf32Args {
   float alpha, beta;
   int tiles_m, tiles_n;   // 256 x 256 pair tiles
   int kb_total;           // ceil(K / 32)
+  // units [0, dp_tiles) are whole tiles; each tile after them (the last,
+  // partial wave) runs as two half-width units of 128 columns
+  int dp_tiles;
   int num_units;
   int group_m;
   bool vec_c;             // C 16-byte aligned with ldc % 4 == 0
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
 };
+// tmBbh / tmBsh: the B parts with 64-row boxes, for the half-width units.
 cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,
                                 const CUtensorMap& tmBb, const CUtensorMap& tmBs,
+                                const CUtensorMap& tmBbh, const CUtensorMap& tmBsh,
                                 const Tf32Args& args, int grid, cudaStream_t stream);
 int sgemm_3xtf32_max_pairs();
 

@@ -78,7 +78,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAb,
                         const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBb,
-                        const __grid_constant__ CUtensorMap tmBs, const Tf32Args p) {
+                        const __grid_constant__ CUtensorMap tmBs,
+                        const __grid_constant__ CUtensorMap tmBbh,
+                        const __grid_constant__ CUtensorMap tmBsh, const Tf32Args p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -122,6 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmAs);
     prefetch_tensormap(&tmBb);
     prefetch_tensormap(&tmBs);
+    prefetch_tensormap(&tmBbh);
+    prefetch_tensormap(&tmBsh);
   }
   tc_fence_before();
   __syncwarp();
@@ -131,15 +135,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const unsigned long long limit = p.wait_limit_ns;
   DeviceStatus* const st = p.status;
 
-  // pair tile -> (m0 of this CTA, n0); groups of group_m tile-rows share B in L2
-  auto tile_of = [&](int u, int& m0, int& n0) {
+  // unit -> (m0 of this CTA, n0, columns); groups of group_m tile-rows share B
+  // in L2; units past dp_tiles are the two column halves of a tile
+  auto tile_of = [&](int u, int& m0, int& n0, int& ncols) {
+    int tile = u, half = -1;
+    if (u >= p.dp_tiles) {
+      tile = p.dp_tiles + ((u - p.dp_tiles) >> 1);
+      half = (u - p.dp_tiles) & 1;
+    }
     const int group = p.group_m * p.tiles_n;
-    const int g = u / group;
+    const int g = tile / group;
     const int first_m = g * p.group_m;
     const int gm = min(p.tiles_m - first_m, p.group_m);
-    const int r = u - g * group;
+    const int r = tile - g * group;
     m0 = (first_m + r % gm) * (2 * BM) + static_cast<int>(rank) * BM;
-    n0 = (r / gm) * BN;
+    n0 = (r / gm) * BN + (half > 0 ? BN / 2 : 0);
+    ncols = half < 0 ? BN : BN / 2;
   };
 
   if (warp == 0) {
@@ -149,21 +160,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int u = worker; ok && u < p.num_units; u += nworkers) {
-        int m0, n0;
-        tile_of(u, m0, n0);
+        int m0, n0, ncols;
+        tile_of(u, m0, n0, ncols);
+        // B rows (columns of B) this CTA stages: half of the unit's
+        const int bcols = ncols / 2;
+        const uint32_t bytes = static_cast<uint32_t>(2 * kATile + 2 * bcols * BK * 4);
+        const CUtensorMap* mb = bcols == kBCols ? &tmBb : &tmBbh;
+        const CUtensorMap* ms = bcols == kBCols ? &tmBs : &tmBsh;
         for (int kb = 0; kb < p.kb_total; ++kb) {
           if (!wait_parity(empty_bar(s), phase ^ 1u, limit, st, 21)) {
             ok = false;
             break;
           }
           const uint32_t fb = map_to_cta(full_bar(s), 0);
-          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
           const uint32_t sa = stage(s);
           tma_load_2d_pair(sa, &tmAb, fb, kb * BK, m0);
           tma_load_2d_pair(sa + kATile, &tmAs, fb, kb * BK, m0);
-          const int nb = n0 + static_cast<int>(rank) * kBCols;
-          tma_load_2d_pair(sa + 2 * kATile, &tmBb, fb, kb * BK, nb);
-          tma_load_2d_pair(sa + 2 * kATile + kBTile, &tmBs, fb, kb * BK, nb);
+          const int nb = n0 + static_cast<int>(rank) * bcols;
+          tma_load_2d_pair(sa + 2 * kATile, mb, fb, kb * BK, nb);
+          tma_load_2d_pair(sa + 2 * kATile + kBTile, ms, fb, kb * BK, nb);
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -182,11 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk starts a fresh accumulation and the epilogue folds it into its
     // fp32 register accumulators.
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = make_idesc(2u, 2 * BM, BN, 0u, 0u);
+      constexpr uint32_t idesc_full = make_idesc(2u, 2 * BM, BN, 0u, 0u);
+      constexpr uint32_t idesc_half = make_idesc(2u, 2 * BM, BN / 2, 0u, 0u);
       int s = 0;
       uint32_t phase = 0, chunk = 0;
       bool ok = true;
       for (int u = worker; ok && u < p.num_units; u += nworkers) {
+        const uint32_t idesc = u < p.dp_tiles ? idesc_full : idesc_half;
         for (int kc = 0; ok && kc < p.kb_total; kc += kChunkKb, ++chunk) {
           const uint32_t buf = chunk & 1u, use = chunk >> 1;
           if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 23)) {
@@ -247,11 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t chunk = 0;
     bool ok = true;
     for (int u = worker; ok && u < p.num_units; u += nworkers) {
-      int m0, n0;
-      tile_of(u, m0, n0);
+      int m0, n0, ncols;
+      tile_of(u, m0, n0, ncols);
+      const int wcols = ncols / 2;   // this warp's columns of the unit
       const int row0 = m0 + 32 * q;
       const int row = row0 + lane;
-      const int colw = n0 + h * kCols;
+      const int colw = n0 + h * wcols;
       const bool active = row0 < p.M && colw < p.N;   // warp-uniform
       float acc[kCols];
 #pragma unroll
@@ -265,9 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (active) {
           const uint32_t tbase =
-              tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * kCols;
+              tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * wcols;
 #pragma unroll
           for (int k = 0; k < kCols / 32; ++k) {
+            if (32 * k >= wcols) break;
             uint32_t t[32];
             tmem_ld_32x32b_x32(tbase + 32 * k, t);
             tmem_wait_regs32(t);
@@ -284,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < kCols / 4; ++g) {
         const int col = colw + 4 * g;
-        if (col >= p.N) break;
+        if (4 * g >= wcols || col >= p.N) break;
         float o[4] = {acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]};
         if (p.vec_c && col + 4 <= p.N) {
           float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -355,6 +375,7 @@ int sgemm_3xtf32_max_pairs() {
 
 cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,
                                 const CUtensorMap& tmBb, const CUtensorMap& tmBs,
+                                const CUtensorMap& tmBbh, const CUtensorMap& tmBsh,
                                 const Tf32Args& args, int grid, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -362,7 +383,7 @@ cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs
   if ((e = configure(dev)) != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, tmAb, tmAs, tmBb, tmBs, args);
+  e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, tmAb, tmAs, tmBb, tmBs, tmBbh, tmBsh, args);
   if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());
 }

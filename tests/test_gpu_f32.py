@@ -88,7 +88,7 @@ FFMA_ONLY, TF32_FORCED = 7, 8
 def test_3xtf32_parity(M, N, K, alpha, beta, c_fill):
     A, B, C0 = operands(900 + M + N + K, M, N, K, K, N, N, np.float32, c_fill=c_fill)
     got, taken = run("f32", A, B, C0, alpha, beta, M, N, K, K, N, N, path=TF32_FORCED)
-    assert taken == "f32.3xtf32.pair"
+    assert taken.startswith("f32.3xtf32.pair")
     check("f32", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
 
 
@@ -101,7 +101,7 @@ def test_3xtf32_small_integers_bit_exact(M, N, K):
     B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
     C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
     got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=TF32_FORCED)
-    assert taken == "f32.3xtf32.pair"
+    assert taken.startswith("f32.3xtf32.pair")
     assert np.array_equal(got.astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0))
 
 
@@ -114,7 +114,7 @@ def test_3xtf32_close_to_ffma_and_split_pins():
     A, B, C0 = operands(77, M, N, K, K, N, N, np.float32)
     tc, t1 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
     ff, t2 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=FFMA_ONLY)
-    assert t1 == "f32.3xtf32.pair" and t2.startswith("f32.ffma")
+    assert t1.startswith("f32.3xtf32.pair") and t2.startswith("f32.ffma")
     ref = oracle.gemm(A, B, None, 1.0, 0.0)
     err_tc = np.abs(tc - ref).max()
     err_ff = np.abs(ff - ref).max()
@@ -130,7 +130,7 @@ def test_3xtf32_long_k_no_drift():
     M, N, K = 256, 256, 16384
     A, B, C0 = operands(4242, M, N, K, K, N, N, np.float32)
     got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=TF32_FORCED)
-    assert taken == "f32.3xtf32.pair"
+    assert taken.startswith("f32.3xtf32.pair")
     ref = oracle.gemm(A, B, None, 1.0, 0.0)
     err = got.astype(np.float64) - ref
     bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
@@ -138,3 +138,24 @@ def test_3xtf32_long_k_no_drift():
     # drift toward zero would make err * sign(ref) consistently negative
     bias = np.mean(err * np.sign(ref))
     assert abs(bias) < bound / 100, (bias, bound)
+
+
+@pytest.mark.parametrize("M,N,K", [(2560, 2560, 512), (2500, 2000, 300)])
+def test_3xtf32_half_width_tail(M, N, K):
+    """The last, partial wave of pair tiles runs as half-width units: exact on
+    integers, and within the fp32 bound of both the oracle and whole tiles."""
+    rng = np.random.default_rng(M + K)
+    A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N)
+    assert taken == "f32.3xtf32.pair.halves", taken
+    rows = oracle.sample_rows(M, block=64)
+    assert np.array_equal(got[rows].astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0, rows=rows))
+    A, B, C0 = operands(55 + M, M, N, K, K, N, N, np.float32)
+    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=5)
+    assert t2 == "f32.3xtf32.pair"
+    check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N, rows=rows)
+    bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
+    assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
