@@ -595,12 +595,12 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       float* As = Ab + a_part / 4;
       float* Bb = As + a_part / 4;
       float* Bs = Bb + b_part / 4;
+      // one launch splits both operands, the blocks shared in proportion to the bytes
       const long long ttiles = ((K2 + 31) / 32) * ((N + 31) / 32);
-      if (launch_split_tf32(A, lda, Ab, As, K2, M, K, scale_grid(*d, 1ll * M * K2 / 4), stream) !=
-              cudaSuccess ||
-          launch_split_tf32_t(B, ldb, Bb, Bs, K2, K, N,
-                              static_cast<int>(std::min<long long>(ttiles, 16ll * d->sm_count)),
-                              stream) != cudaSuccess)
+      const int grid_a = scale_grid(*d, 1ll * M * K2 / 4);
+      const int grid_b = static_cast<int>(std::min<long long>(ttiles, 8ll * d->sm_count));
+      if (launch_split_tf32_ab(A, lda, Ab, As, B, ldb, Bb, Bs, K2, M, N, K, grid_a, grid_b,
+                               stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
       CUtensorMap mAb{}, mAs{}, mBb{}, mBs{}, mBbh{}, mBsh{};
       if (int rc = make_map_f32(&mAb, Ab, M, K, K2, 32, 128)) return rc;

@@ -157,15 +157,16 @@ __device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
 
 // Splits a rows x cols fp32 matrix (any leading dimension, 4-byte aligned)
 // into big and small parts stored densely with leading dimension ldd
-// (ldd % 4 == 0, zero padding), one thread per 4 output columns.
-__global__ void split_tf32_kernel(const float* __restrict__ src, long long lds,
-                                  float* __restrict__ big, float* __restrict__ small, long long ldd,
-                                  int rows, int cols) {
+// (ldd % 4 == 0, zero padding), one thread per 4 output columns; `block` and
+// `nblocks` number the blocks that share the work.
+__device__ __forceinline__ void split_rows(const float* __restrict__ src, long long lds,
+                                           float* __restrict__ big, float* __restrict__ small,
+                                           long long ldd, int rows, int cols, long long block,
+                                           long long nblocks) {
   const long long groups = ldd / 4;
   const long long total = static_cast<long long>(rows) * groups;
   const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (lds & 3) == 0;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+  for (long long g = block * blockDim.x + threadIdx.x; g < total; g += nblocks * blockDim.x) {
     const int r = static_cast<int>(g / groups);
     const int c0 = static_cast<int>(g % groups) * 4;
     const float* p = src + static_cast<long long>(r) * lds + c0;
@@ -186,39 +187,66 @@ __global__ void split_tf32_kernel(const float* __restrict__ src, long long lds,
   }
 }
 
-// Transposing split: src is rows x cols (row-major, 4-byte aligned); writes
-// big/small parts of src^T, i.e. dst[c][r] for c < cols, r < rows, with
-// leading dimension ldd (>= rows, % 4 == 0; zero padding in [rows, ldd)).
-// 32 x 32 tiles through shared memory so that both sides are coalesced.
-__global__ void split_tf32_t_kernel(const float* __restrict__ src, long long lds,
-                                    float* __restrict__ big, float* __restrict__ small,
-                                    long long ldd, int rows, int cols) {
-  __shared__ float tile[32][33];
+// Transposing split of 32 x 32 tiles through shared memory (256 threads):
+// src is rows x cols; dst rows are src columns (leading dimension ldd >= rows,
+// % 4 == 0, zero padding in [rows, ldd)).  Thread t loads the 16 bytes at
+// columns 4*(t % 8) of tile row t / 8 and stores the 16 bytes at columns
+// 4*(t % 8) of tile row t / 8 of the transpose; tile[32][33] keeps the
+// column reads of the store phase free of bank conflicts.  Element accesses
+// when src or lds is not 16-byte aligned.
+__device__ __forceinline__ void split_transpose(const float* __restrict__ src, long long lds,
+                                                float* __restrict__ big, float* __restrict__ small,
+                                                long long ldd, int rows, int cols, long long block,
+                                                long long nblocks, float (*tile)[33]) {
   const int tiles_c = (cols + 31) / 32;
   const int tiles_r = static_cast<int>((ldd + 31) / 32);
   const long long ntiles = static_cast<long long>(tiles_r) * tiles_c;
-  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (lds & 3) == 0;
+  const int tr = static_cast<int>(threadIdx.x) >> 3, tq = (static_cast<int>(threadIdx.x) & 7) * 4;
+  for (long long t = block; t < ntiles; t += nblocks) {
     const int r0 = static_cast<int>(t / tiles_c) * 32, c0 = static_cast<int>(t % tiles_c) * 32;
-    // load: thread (x, y) reads rows r0 + y + 8i, column c0 + x
-    for (int i = 0; i < 4; ++i) {
-      const int rr = r0 + threadIdx.y + 8 * i, cc = c0 + threadIdx.x;
-      tile[threadIdx.y + 8 * i][threadIdx.x] =
-          (rr < rows && cc < cols) ? __ldg(src + static_cast<long long>(rr) * lds + cc) : 0.0f;
+    {
+      const int rr = r0 + tr, cc = c0 + tq;
+      const float* p = src + static_cast<long long>(rr) * lds + cc;
+      float x[4];
+      if (vec && rr < rows && cc + 4 <= cols) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = (rr < rows && cc + i < cols) ? __ldg(p + i) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tile[tr][tq + i] = x[i];
     }
     __syncthreads();
-    // store: thread (x, y) writes dst row c0 + y + 8i, column r0 + x
-    for (int i = 0; i < 4; ++i) {
-      const int cc = c0 + threadIdx.y + 8 * i, rr = r0 + threadIdx.x;
+    {
+      const int cc = c0 + tr, rr = r0 + tq;   // destination row cc, columns rr .. rr+3
       if (cc < cols && rr < ldd) {
-        float b, sm;
-        split_tf32(tile[threadIdx.x][threadIdx.y + 8 * i], b, sm);
+        float b[4], sm[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_tf32(tile[tq + i][tr], b[i], sm[i]);
         const long long o = static_cast<long long>(cc) * ldd + rr;
-        big[o] = b;
-        small[o] = sm;
+        *reinterpret_cast<float4*>(big + o) = make_float4(b[0], b[1], b[2], b[3]);
+        *reinterpret_cast<float4*>(small + o) = make_float4(sm[0], sm[1], sm[2], sm[3]);
       }
     }
     __syncthreads();
   }
+}
+
+// Both splits of a 3xTF32 product in one launch: blocks [0, grid_a) split A
+// (M x K), the others split B^T (B is K x N).
+__global__ void split_tf32_ab_kernel(const float* __restrict__ A, long long lda,
+                                     float* __restrict__ Ab, float* __restrict__ As,
+                                     const float* __restrict__ B, long long ldb,
+                                     float* __restrict__ Bb, float* __restrict__ Bs, long long ld2,
+                                     int M, int N, int K, int grid_a) {
+  __shared__ float tile[32][33];
+  if (static_cast<int>(blockIdx.x) < grid_a)
+    split_rows(A, lda, Ab, As, ld2, M, K, blockIdx.x, grid_a);
+  else
+    split_transpose(B, ldb, Bb, Bs, ld2, K, N, blockIdx.x - grid_a, gridDim.x - grid_a, tile);
 }
 
 // dst[i] = src[i] rounded to the nearest half (ties to even), eight elements
@@ -260,17 +288,14 @@ cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int 
   return counted_launch(cudaGetLastError());
 }
 
-cudaError_t launch_split_tf32_t(const float* src, long long lds, float* big, float* small,
-                                long long ldd, int rows, int cols, int grid, cudaStream_t stream) {
-  split_tf32_t_kernel<<<grid, dim3(32, 8), 0, stream>>>(src, lds, big, small, ldd, rows, cols);
+cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float* As,
+                                 const float* B, long long ldb, float* Bb, float* Bs, long long ld2,
+                                 int M, int N, int K, int grid_a, int grid_b, cudaStream_t stream) {
+  split_tf32_ab_kernel<<<grid_a + grid_b, 256, 0, stream>>>(A, lda, Ab, As, B, ldb, Bb, Bs, ld2, M,
+                                                            N, K, grid_a);
   return counted_launch(cudaGetLastError());
 }
 
-cudaError_t launch_split_tf32(const float* src, long long lds, float* big, float* small,
-                              long long ldd, int rows, int cols, int grid, cudaStream_t stream) {
-  split_tf32_kernel<<<grid, 256, 0, stream>>>(src, lds, big, small, ldd, rows, cols);
-  return counted_launch(cudaGetLastError());
-}
 
 cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
                                int rows, int cols, int grid, cudaStream_t stream) {

@@ -116,13 +116,12 @@ cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int split
 cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
                                int rows, int cols, int grid, cudaStream_t stream);
 
-// big/small tf32 split of an fp32 operand into dense copies (ldd % 4 == 0).
-cudaError_t launch_split_tf32(const float* src, long long lds, float* big, float* small,
-                              long long ldd, int rows, int cols, int grid, cudaStream_t stream);
-
-// The same split of the TRANSPOSE of a rows x cols matrix (dst is cols x ldd).
-cudaError_t launch_split_tf32_t(const float* src, long long lds, float* big, float* small,
-                                long long ldd, int rows, int cols, int grid, cudaStream_t stream);
+// Both splits of a 3xTF32 product in one launch: A (M x K) into Ab, As and
+// B^T (B is K x N) into Bb, Bs, all with leading dimension ld2 (>= K, % 4 == 0);
+// grid_a blocks work on A, grid_b on B^T.
+cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float* As,
+                                 const float* B, long long ldb, float* Bb, float* Bs, long long ld2,
+                                 int M, int N, int K, int grid_a, int grid_b, cudaStream_t stream);
 
 // 3xTF32 SGEMM on CTA pairs: C = alpha*(Ab*Bb + Ab*Bs + As*Bb) + beta*C with
 // the split operands dense and K-contiguous: A parts M x roundup(K,4), B parts
