@@ -32,7 +32,7 @@ EXPORTS = (
     "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
     "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
     "gemm_f16_splitk_noalloc", "gemm_launch_count", "gemm_plan_stream_k", "gemm_f16_f32out",
-    "gemm_f32_to_f16",
+    "gemm_f32_to_f16", "gemm_debug_wait_probe",
 )
 
 PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
@@ -67,6 +67,8 @@ def lib():
                 fn = getattr(L, name)
                 fn.restype = i
                 fn.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, vp]
+            L.gemm_debug_wait_probe.restype = i
+            L.gemm_debug_wait_probe.argtypes = [ctypes.c_longlong, vp]
             L.gemm_f16_f32out.restype = i
             L.gemm_f16_f32out.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, f, vp]
             L.gemm_f32_to_f16.restype = i
@@ -257,6 +259,12 @@ def plan_stream_k(tiles: int, slots: int, kb: int, all_tiles: bool = False) -> d
     out = (ctypes.c_longlong * 4)()
     _check(lib().gemm_plan_stream_k(tiles, slots, kb, int(bool(all_tiles)), out), "gemm_plan_stream_k")
     return {"dp_tiles": out[0], "sk_tiles": out[1], "workers": out[2], "max_pieces": out[3]}
+
+
+def debug_wait_probe(limit_ns: int, stream=None):
+    """Launches a wait on a barrier that nothing releases; it gives up after
+    limit_ns and the next debug_status() returns GEMM_ERR_TIMEOUT (-6)."""
+    _check(lib().gemm_debug_wait_probe(int(limit_ns), _stream(stream)), "gemm_debug_wait_probe")
 
 
 def launch_count() -> int:

@@ -820,6 +820,17 @@ int gemm_debug_status(void) {
 
 const char* gemm_last_path(void) { return t_last_path; }
 
+int gemm_debug_wait_probe(long long limit_ns, cudaStream_t stream) {
+  if (limit_ns <= 0) return GEMM_ERR_ARG;
+  DevState* d = nullptr;
+  if (int rc = device_state(&d, nullptr)) return rc;
+  t_last_path = "wait_probe";
+  return launch_wait_probe(static_cast<unsigned long long>(limit_ns), d->status, stream) ==
+                 cudaSuccess
+             ? GEMM_OK
+             : GEMM_ERR_CUDA;
+}
+
 int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, long long* out) {
   if (out == nullptr) return GEMM_ERR_NULL;
   const SkPlan p = plan_stream_k(tiles, slots, kb, all_tiles != 0);

@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gb300 {
 namespace {
@@ -276,7 +277,24 @@ __global__ void f32_to_f16_kernel(const float* __restrict__ src, uint16_t* __res
   }
 }
 
+// One thread waits (bounded) on an mbarrier that nothing arrives on: the wait
+// runs out after limit_ns, records GEMM_ERR_TIMEOUT in the status word and the
+// kernel returns normally.  Used by the failure-detection test.
+__global__ void wait_probe_kernel(unsigned long long limit_ns, DeviceStatus* st) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1u);
+  fence_barrier_init();
+  wait_parity(b, 0u, limit_ns, st, 99);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, DeviceStatus* status,
+                              cudaStream_t stream) {
+  wait_probe_kernel<<<1, 1, 0, stream>>>(limit_ns, status);
+  return counted_launch(cudaGetLastError());
+}
 
 cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int grid,
                               cudaStream_t stream) {

@@ -93,6 +93,11 @@ cudaError_t launch_gemm_f16_tc_skinny(int am, int epi_mode, const CUtensorMap& t
                                       const CUtensorMap& tmB, const CUtensorMap& tmC,
                                       const TcArgs& args, int grid, cudaStream_t stream);
 
+// One thread waits on an mbarrier that nothing arrives on, so the bounded wait
+// runs out after limit_ns and records GEMM_ERR_TIMEOUT in *status.
+cudaError_t launch_wait_probe(unsigned long long limit_ns, DeviceStatus* status,
+                              cudaStream_t stream);
+
 // fp32 -> fp16 conversion of n elements, round to nearest even.
 cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int grid,
                               cudaStream_t stream);

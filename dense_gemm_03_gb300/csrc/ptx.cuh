@@ -77,12 +77,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                             DeviceStatus* st, int where) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  // the clock is first read after 64 more tries, keeping it off the path of
+  // short waits (the limit then counts from that read)
+  uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*reinterpret_cast<volatile int*>(&st->code) != 0) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
         if (atomicCAS(&st->code, 0, kStatusTimeout) == 0) st->where = where;
         return false;
       }

@@ -204,6 +204,16 @@ long long gemm_set_wait_limit_ns(long long ns);
  */
 int gemm_debug_status(void);
 
+/*
+ * Failure-detection probe: launches one thread that waits, through the same
+ * bounded wait every kernel of the library uses, on an mbarrier that nothing
+ * ever arrives on.  After `limit_ns` nanoseconds the wait gives up, records
+ * GEMM_ERR_TIMEOUT in the device status word and the kernel returns normally
+ * (no trap; the context stays usable), so the next gemm_debug_status() call
+ * returns GEMM_ERR_TIMEOUT.  limit_ns <= 0 is GEMM_ERR_ARG.  Asynchronous.
+ */
+int gemm_debug_wait_probe(long long limit_ns, cudaStream_t stream);
+
 /* Describes the path the last call on this thread took (static string). */
 const char* gemm_last_path(void);
 
