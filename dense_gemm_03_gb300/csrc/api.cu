@@ -22,6 +22,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <unordered_map>
 
@@ -38,6 +39,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
+constexpr int kHostBlocks = 4;   // row blocks of the pipelined host-buffer forms
 
 // Scratch of one stream: fp32 partial sums (split-K or tail tiles) and the
 // tail-tile arrival counters.  Kernels on one stream run in order, so giving
@@ -65,9 +67,15 @@ struct DevState {
   size_t flush_bytes = 0;
   void* host_buf[3] = {nullptr, nullptr, nullptr};  // staging for the host-buffer forms
   size_t host_bytes[3] = {0, 0, 0};
+  // host forms: copy-in and copy-back streams, and per row block an "in"
+  // event (operands on the device) and a "done" event (block computed), plus
+  // the call's entry and exit events
+  cudaStream_t copy_in = nullptr, copy_back = nullptr;
+  cudaEvent_t host_ev[2 * kHostBlocks + 2] = {};
 };
 
 std::mutex g_mu;
+std::mutex g_host_mu;   // host-buffer forms share their staging buffers: one call at a time
 DevState g_dev[kMaxDevices];
 std::atomic<int> g_force_path{0};
 std::atomic<int> g_force_splits{0};
@@ -662,7 +670,9 @@ int host_form(const T* A, const T* B, T* C, int M, int N, int K, int lda, int ld
   if (M == 0 || N == 0) return GEMM_OK;
   DevState* d = nullptr;
   if (int rc = device_state(&d, nullptr)) return rc;
+  std::lock_guard<std::mutex> host_lk(g_host_mu);
   const bool read_ab = alpha != 0.0f && K > 0;
+  const bool read_c = beta != 0.0f || ldc > N;   // ldc > N: the padding must come back unchanged
   const size_t ba = read_ab ? extent_bytes(M, K, lda, sizeof(T)) : 0;
   const size_t bb = read_ab ? extent_bytes(K, N, ldb, sizeof(T)) : 0;
   const size_t bc = extent_bytes(M, N, ldc, sizeof(T));
@@ -677,20 +687,58 @@ int host_form(const T* A, const T* B, T* C, int M, int N, int K, int lda, int ld
     }
     if (int rc = ensure_buffer(&d->host_buf[2], &d->host_bytes[2], bc)) return rc;
     dC = static_cast<T*>(d->host_buf[2]);
+    for (cudaStream_t* st : {&d->copy_in, &d->copy_back})
+      if (!*st && cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    for (cudaEvent_t& e : d->host_ev)
+      if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return GEMM_ERR_CUDA;
   }
-  if (read_ab) {
-    if (cudaMemcpyAsync(dA, A, ba, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(dB, B, bb, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+  cudaEvent_t* const ev_in = d->host_ev;                    // [kHostBlocks]
+  cudaEvent_t* const ev_done = d->host_ev + kHostBlocks;    // [kHostBlocks]
+  cudaEvent_t const ev_entry = d->host_ev[2 * kHostBlocks];
+  cudaEvent_t const ev_exit = d->host_ev[2 * kHostBlocks + 1];
+  // Blocks of rows of A and C, on three streams: the copy-in stream brings B
+  // and then block after block of A and C; `stream` computes block j once it
+  // is in; the copy-back stream returns block j's C once it is computed.  So
+  // copies in, GEMMs and copies back of different blocks overlap (the two
+  // directions of the host link run concurrently).  Blocks are multiples of
+  // 256 rows: whole output tiles of the big kernels.
+  const int nblk = (read_ab && M >= 2048) ? kHostBlocks : 1;
+  const int rb = (M + nblk - 1) / nblk;
+  const int rows_per = nblk == 1 ? M : (rb + 255) / 256 * 256;
+  // the copies follow whatever the caller queued on `stream` before this call
+  if (cudaEventRecord(ev_entry, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(d->copy_in, ev_entry, 0) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (read_ab && cudaMemcpyAsync(dB, B, bb, cudaMemcpyHostToDevice, d->copy_in) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  int j = 0;
+  for (int r0 = 0; r0 < M; r0 += rows_per, ++j) {
+    const int mr = std::min(rows_per, M - r0);
+    const size_t a_off = static_cast<size_t>(r0) * lda, c_off = static_cast<size_t>(r0) * ldc;
+    if (read_ab && cudaMemcpyAsync(dA + a_off, A + a_off, extent_bytes(mr, K, lda, sizeof(T)),
+                                   cudaMemcpyHostToDevice, d->copy_in) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    const size_t cbytes = extent_bytes(mr, N, ldc, sizeof(T));
+    if (read_c && cudaMemcpyAsync(dC + c_off, C + c_off, cbytes, cudaMemcpyHostToDevice,
+                                  d->copy_in) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    if (cudaEventRecord(ev_in[j], d->copy_in) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, ev_in[j], 0) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    if (int rc = device_fn(read_ab ? dA + a_off : nullptr, dB, dC + c_off, mr, N, K, lda, ldb, ldc,
+                           alpha, beta, stream))
+      return rc;
+    if (cudaEventRecord(ev_done[j], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(d->copy_back, ev_done[j], 0) != cudaSuccess ||
+        cudaMemcpyAsync(C + c_off, dC + c_off, cbytes, cudaMemcpyDeviceToHost, d->copy_back) !=
+            cudaSuccess)
       return GEMM_ERR_CUDA;
   }
-  // C is copied in whole when beta != 0, and also when ldc > N so that the
-  // padding between rows comes back unchanged.
-  if (beta != 0.0f || ldc > N) {
-    if (cudaMemcpyAsync(dC, C, bc, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-      return GEMM_ERR_CUDA;
-  }
-  if (int rc = device_fn(dA, dB, dC, M, N, K, lda, ldb, ldc, alpha, beta, stream)) return rc;
-  if (cudaMemcpyAsync(C, dC, bc, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  // the caller's stream (and so the next call) waits for the last copy back
+  if (cudaEventRecord(ev_exit, d->copy_back) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, ev_exit, 0) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return cudaStreamSynchronize(stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -858,6 +906,7 @@ const char* gemm_strerror(int code) {
 }
 
 int gemm_release(void) {
+  std::lock_guard<std::mutex> host_lk(g_host_mu);
   std::lock_guard<std::mutex> lk(g_mu);
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -885,6 +934,14 @@ int gemm_release(void) {
       if (kv.second.split) cudaFree(kv.second.split);
     }
     d.ws.clear();
+    for (cudaStream_t* st : {&d.copy_in, &d.copy_back}) {
+      if (*st) cudaStreamDestroy(*st);
+      *st = nullptr;
+    }
+    for (cudaEvent_t& e : d.host_ev) {
+      if (e) cudaEventDestroy(e);
+      e = nullptr;
+    }
   }
   cudaSetDevice(prev);
   return rc;

@@ -126,9 +126,18 @@ int sgemm_f32_ld(const float* A, const float* B, float* C,
 
 /*
  * Host-buffer forms: A, B, C are HOST pointers (pinned memory gives the
- * fastest copies; pageable memory works).  The call copies A, B (and C when
- * beta != 0) to library-owned device buffers, runs the GEMM on `stream`,
- * copies C back and synchronises the stream before returning.  The device
+ * fastest copies and lets them overlap; pageable memory works).  On a
+ * library-owned copy-in stream the call copies B, then A and C (C when
+ * beta != 0 or ldc > N) in blocks of rows to library-owned device buffers;
+ * each block is computed on `stream` as soon as it is in, and copied back on
+ * a library-owned copy-back stream as soon as it is computed (M >= 2048: four
+ * blocks of a multiple of 256 rows; else one), so copies in, GEMMs and copies
+ * back of different blocks overlap.  The copies in wait for the work already
+ * queued on `stream`; the call returns after `stream` has synchronised with
+ * the last copy back.  A blocked call
+ * may round differently in the last bit from the device form on the same
+ * operands (each block is its own GEMM, with its own tile schedule).  Calls
+ * are serialised process-wide (they share the staging buffers).  The device
  * buffers are kept for reuse and freed by gemm_release().
  */
 int gemm_f16_host(const uint16_t* A, const uint16_t* B, uint16_t* C,

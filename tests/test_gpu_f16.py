@@ -162,6 +162,24 @@ def test_host_form_matches_device_form():
     assert np.array_equal(hC.numpy().view(np.uint16), dev.view(np.uint16))
 
 
+@pytest.mark.parametrize("M,N,K,ldc", [(4096, 1024, 512, 1024), (2100, 777, 300, 800)])
+def test_host_form_in_row_blocks(M, N, K, ldc):
+    """M >= 2048: four row blocks copied in, computed and copied back in turn;
+    the result matches the oracle, and C's padding comes back unchanged."""
+    import dense_gemm_03_gb300 as g
+    t = torch()
+    A, B, C0 = operands(808 + M, M, N, K, K, N, ldc, np.float16)
+    hA = t.from_numpy(A).pin_memory()
+    hB = t.from_numpy(B).pin_memory()
+    hC = t.from_numpy(C0.copy()).pin_memory()
+    g.gemm_f16_host(hA, hB, hC, 0.75, -0.25, M=M, N=N, K=K, ldc=ldc)
+    got = hC.numpy()
+    check("f16", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc,
+          rows=oracle.sample_rows(M, block=64), cols=oracle.sample_cols(N))
+    assert padding_untouched(got, C0, N)
+    assert g.debug_status() == 0
+
+
 def test_streams_are_respected():
     """Work goes on the caller's stream: a GEMM enqueued on a side stream after
     an event sees the inputs the main stream wrote before it."""
