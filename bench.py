@@ -444,9 +444,23 @@ def cpu_baseline(seconds: float):
     target_rows = int(min(M, max(rows, rows * seconds / max(t, 1e-6))))
     t = _time_rows(oracle, A, B, C0, target_rows)
     flops = 2.0 * target_rows * N * K
+    # the oracle on one thread, on the two smallest fp32 workloads (256^3, 1024^3)
+    single = {}
+    oracle.set_threads(1)
+    try:
+        for n in (256, 1024):
+            sa = synthetic.uniform(synthetic.config_seed(1), synthetic.STREAM_A, (n, n))
+            sb = synthetic.uniform(synthetic.config_seed(1), synthetic.STREAM_B, (n, n))
+            t0 = time.perf_counter()
+            oracle.gemm(sa, sb, None, 1.0, 0.0)
+            dt = time.perf_counter() - t0
+            single["fp32 %d^3" % n] = {"s": round(dt, 4), "tflops": round(2.0 * n ** 3 / dt / 1e12, 6)}
+    finally:
+        oracle.set_threads(cores)
     return {"value": round(flops / t / 1e12, 6), "unit": "TFLOPS", "cores": cores,
             "kind": "oracle",
-            "sample": "%d of %d rows of C for the fp16 4096^3 workload (%.1f s)" % (target_rows, M, t)}
+            "sample": "%d of %d rows of C for the fp16 4096^3 workload (%.1f s)" % (target_rows, M, t),
+            "single_thread": single}
 
 
 def _time_rows(oracle, A, B, C0, nrows):
