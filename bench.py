@@ -16,6 +16,8 @@ while the replays run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --sweep [--sweep-out FILE]    # fp32 size sweep 1024..12800
+  python bench.py --sweep-f16 [--sweep-out FILE] [--sweep-sizes a,b,...]
+                                                # fp16: automatic path vs the alternatives
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas, no collective on the data path); rank 0 prints the
@@ -553,6 +555,62 @@ def run_sweep(args):
                       "tflops_mean": round(sum(r["tflops"] for r in results) / max(1, len(results)), 3)}))
 
 
+# ---------------------------------------------------------------- fp16 tile-heuristic sweep
+
+F16_VARIANTS = [(0, "auto"), (6, "no_pairs"), (5, "whole_tiles"), (9, "k_slices_tail"),
+                (10, "stream_k")]
+
+
+def run_sweep_f16(args):
+    """Square fp16 GEMMs (C = 1.5*A*B + 0.5*C) over the sweep sizes: the
+    automatic path and the forced alternatives it chooses between, each timed
+    the same way (L2 cleared before every replay, second-half mean of a
+    quarter of the page's replay count)."""
+    import torch
+    import dense_gemm_03_gb300 as g
+    import synthetic
+    from dense_gemm_03_gb300 import build as _b
+    _b.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(0)
+    flush = 2 * int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    out = open(args.sweep_out, "a") if args.sweep_out else None
+    sizes = sweep_sizes()
+    if args.sweep_sizes:
+        sizes = [int(x) for x in args.sweep_sizes.split(",")]
+    sampler = ClockSampler(0).start()
+    best_is_auto = 0
+    within = 0
+    for n in sizes:
+        seed = synthetic.config_seed(5) + n
+        A = torch.from_numpy(synthetic.uniform(seed, synthetic.STREAM_A, (n, n), dtype=np.float16)).cuda()
+        B = torch.from_numpy(synthetic.uniform(seed, synthetic.STREAM_B, (n, n), dtype=np.float16)).cuda()
+        C = torch.from_numpy(synthetic.uniform(seed, synthetic.STREAM_C, (n, n), dtype=np.float16)).cuda()
+        R = max(8, replay_count(n) // 4)
+        rec = {"size": n, "replays": R}
+        for path, name in F16_VARIANTS:
+            prev = g.force_path(path)
+            try:
+                ms = timed_replays(lambda: g.gemm_f16(A, B, C, 1.5, 0.5, stream=stream), R, 3,
+                                   stream, flush)
+                rec[name] = {"us": round(second_half_mean(ms) * 1e3, 2), "path": g.last_path()}
+            finally:
+                g.force_path(prev)
+        rec["tflops_auto"] = round(2.0 * n ** 3 / (rec["auto"]["us"] * 1e-6) / 1e12, 1)
+        best = min(v["us"] for k, v in rec.items() if isinstance(v, dict))
+        rec["auto_vs_best"] = round(rec["auto"]["us"] / best, 4)
+        best_is_auto += rec["auto"]["us"] <= best
+        within += rec["auto_vs_best"] <= 1.02
+        if out:
+            out.write(json.dumps(rec) + "\n")
+            out.flush()
+        del A, B, C
+    clocks = sampler.stop()
+    print(json.dumps({"sweep": "fp16 heuristic 1024..12800 step 128", "sizes": len(sizes),
+                      "auto_best": best_is_auto, "auto_within_2pct": within, "clocks": clocks}))
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -565,6 +623,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-shapes", action="store_true", help="skip the edge-shape timings")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-f16", action="store_true",
+                    help="fp16 sweep: the automatic path beside the forced alternatives")
     ap.add_argument("--sweep-out", default=None)
     ap.add_argument("--sweep-sizes", default=None)
     args = ap.parse_args()
@@ -579,6 +639,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.sweep_f16:
+        run_sweep_f16(args)
         return
     if world > 1:
         import torch

@@ -241,6 +241,25 @@ SkPlan plan_stream_k(long long tiles, long long slots, int kb, bool all_tiles) {
   return p;
 }
 
+// Whether stream-K over all of a few tiles (plan_stream_k's all_tiles form)
+// is expected to beat half-width whole-K units, in k-block times of one
+// tile: stream-K takes the longest range plus a fix-up growing with the
+// pieces a tile is cut into (publishing and re-reading partial sums); a wave
+// of half-width units takes about 3/4 of a tile's k-blocks (measured: they
+// stage 3/4 of the operand bytes for half the FLOPs).  Measured at 1024^3
+// (32 tiles of 16 k-blocks): half-width units 16 us, stream-K 24 us; at
+// 16x8192x8192 (64 tiles of 128 k-blocks): stream-K 42 us, equal K slices 51.
+bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool halves_ok) {
+  const SkPlan sk = plan_stream_k(tiles, slots, kb, true);
+  if (sk.sk_tiles == 0) return false;
+  if (!halves_ok) return true;
+  const long long range = (sk.sk_tiles * kb + sk.workers - 1) / sk.workers;
+  const long long sk_cost = range + kSkFixKb + 4 * (sk.max_pieces - 1);
+  const long long waves = (2 * tiles + slots - 1) / slots;
+  const long long halves_cost = (3 * kb * waves + 3) / 4;
+  return sk_cost < halves_cost;
+}
+
 int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
                  int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = nullptr;
@@ -405,7 +424,13 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   // Few tiles for many SMs: the k-blocks of all tiles are shared out evenly
   // over the SMs (stream-K); the forced split-K path cuts every tile into
   // equal K slices instead.
+  // Few tiles for many SMs: stream-K over all tiles when it beats half-width
+  // whole-K units (few_sk; then one CTA per worker, no pairs).
   const bool few = tiles * 2 <= d->sm_count && a.kb_total >= 8;
+  const bool few_sk =
+      (few && force == 0 &&
+       few_tiles_prefer_stream_k(tiles, d->sm_count, a.kb_total, load == kLoadTma && bn >= 128)) ||
+      force == 11;
   if (force == 3) {
     // as many K slices as fit in ONE wave of CTAs (a second, partial wave would
     // double the time of these bandwidth-bound shapes)
@@ -427,7 +452,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   // CTA pairs (256 x 256 tiles on clusters of 2 sharing each MMA) for the
   // large aligned shapes: each SM then stages half as much of B per MMA.
   int pair_slots = 0;
-  const bool pair = splits == 1 && !(force == 0 && few) && force != 6 && bn == 256 &&
+  const bool pair = splits == 1 && !few_sk && force != 6 && bn == 256 &&
                     load == kLoadTma && a.tiles_m >= 2 &&
                     (pair_slots = tc_pair_max_clusters(epi)) > 0;
   long long units_tiles = tiles;   // tiles in units of the worker (CTA or pair)
@@ -493,7 +518,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
       if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
       cut = ".sk";
     }
-  } else if (force != 5 && !(few && force == 0)) {
+  } else if (force != 5 && !few_sk) {
     // The tiles of the last, partial wave become two half-width units each
     // (whole K, no partial sums) when the halves fit in one wave.
     const long long rem = units_tiles % slots;
@@ -840,7 +865,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 10) return GEMM_ERR_ARG;
+  if (path < 0 || path > 11) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 

@@ -191,7 +191,9 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * 8 = (fp32) 3xTF32 tensor-core kernel whatever the shape; 9 = the last,
  * partial wave of tiles cut into two equal K slices (instead of two
  * half-width units); 10 = stream-K over the last waves of tiles (k-block
- * ranges shared out evenly; automatic only when there are few tiles).
+ * ranges shared out evenly); 11 = stream-K over all tiles, one CTA per worker
+ * (chosen automatically for few tiles when it is expected to beat half-width
+ * units).
  * A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.

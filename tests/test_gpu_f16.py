@@ -11,7 +11,7 @@ from helpers import check, operands, padding_untouched, run, to_dev, torch
 pytestmark = pytest.mark.gpu
 
 AUTO, MANUAL, SPLITK = 0, 2, 3
-NO_TAIL, NO_PAIR, TAIL2, SK = 5, 6, 9, 10
+NO_TAIL, NO_PAIR, TAIL2, SK, SK_ALL = 5, 6, 9, 10, 11
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -253,10 +253,12 @@ def test_tail_deterministic(path, mark):
     (2560, 2560, 1024, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 100 pair tiles: 24 halved
     (2560, 2560, 1024, NO_PAIR, ".bn256.tma.epi_tma.halves"),     # 200 CTA tiles, halved tail
     (3300, 2001, 700, AUTO, ".epi_manual.halves"),                # predicated epilogue, halved
-    (16, 8192, 4096, AUTO, ".bn128.tma.epi_tma.a32.sk"),   # skinny: every tile shared
+    (16, 8192, 8192, AUTO, ".bn128.tma.epi_tma.a32.sk"),   # skinny: every tile shared
     (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma.sk"),      # tall: every tile shared
-    (64, 128, 4096, AUTO, ".sk"),                        # one tile cut into many pieces
-    (100, 300, 1000, AUTO, ".sk"),                       # ragged, small
+    (64, 128, 4096, SK_ALL, ".sk"),                      # one tile cut into 16 pieces
+    (100, 300, 1000, SK_ALL, ".sk"),                     # ragged, small
+    (64, 128, 4096, AUTO, ".halves"),                    # the same, as two half-width units
+    (1024, 1024, 1024, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # few tiles, short K
 ])
 def test_balanced_schedules_integers_exact(M, N, K, path, mark):
     """Entries in {-1, 0, 1}: partial sums are integers below 2^24, exact in
@@ -362,7 +364,7 @@ def test_odd_pointers_are_rejected():
 # ---------------------------------------------------------------- skinny shapes (A rows staged: 32 or 64)
 @pytest.mark.parametrize("M,N,K,mark", [
     (1, 300, 2000, ".a32"),
-    (16, 8192, 2048, ".a32.sk"),
+    (16, 8192, 2048, ".a32"),
     (31, 1000, 700, ".a32"),
     (32, 1000, 700, ".a32"),
     (33, 1000, 700, ".a64"),

@@ -49,7 +49,7 @@ def _c32(seed, M, ldc, fill="uniform"):
     (256, 512, 128, AUTO, ".epi_f32"),
     (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_f32.halves"),
     (2000, 2600, 2048, SK, ".pair.bn256.tma.epi_f32.sk"),
-    (16, 8192, 2048, AUTO, ".bn128.tma.epi_f32.a32.sk"),
+    (16, 8192, 8192, AUTO, ".bn128.tma.epi_f32.a32.sk"),
     (48, 3000, 1500, AUTO, ".epi_f32.a64"),
     (700, 300, 500, NO_PAIR, ".bn256.tma.epi_f32"),
     (129, 65, 17, AUTO, ".epi_f32"),
