@@ -370,21 +370,26 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
       if (int rc = ensure_buffer(&w.realigned, &w.realigned_bytes, a_bytes + b_bytes + 256))
         return rc;
       uint16_t* buf = static_cast<uint16_t*>(w.realigned);
+      // one launch copies whichever of A and B breaks the rule
+      RealignJob jobs[2];
+      int grids[2];
+      int njobs = 0;
       if (!a_tma) {
-        if (launch_realign_f16(A, lda, buf, lda2, M, K, scale_grid(*d, 1ll * M * lda2 / 8),
-                               stream) != cudaSuccess)
-          return GEMM_ERR_CUDA;
+        jobs[njobs] = RealignJob{A, lda, buf, lda2, M, K};
+        grids[njobs++] = scale_grid(*d, 1ll * M * lda2 / 8);
         A = buf;
         lda = lda2;
         buf += (a_bytes / 2 + 127) / 128 * 128;   // keep the next copy 256-byte aligned
       }
       if (!b_tma) {
-        if (launch_realign_f16(B, ldb, buf, ldb2, K, N, scale_grid(*d, 1ll * K * ldb2 / 8),
-                               stream) != cudaSuccess)
-          return GEMM_ERR_CUDA;
+        jobs[njobs] = RealignJob{B, ldb, buf, ldb2, K, N};
+        grids[njobs++] = scale_grid(*d, 1ll * K * ldb2 / 8);
         B = buf;
         ldb = ldb2;
       }
+      if (launch_realign_f16(jobs[0], njobs > 1 ? &jobs[1] : nullptr, grids[0],
+                             njobs > 1 ? grids[1] : 0, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
       how = ".realigned";
     }
   }

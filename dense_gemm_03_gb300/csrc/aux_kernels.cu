@@ -104,12 +104,12 @@ __device__ __forceinline__ uint4 shift_bytes(uint4 lo, uint4 hi, uint32_t m) {
 // blocks that contain it -- blocks that hold at least one element of the
 // piece, so the reads never leave memory the caller owns -- and shifted into
 // place; the ragged end of a row uses element loads.
-__global__ void realign_f16_kernel(const uint16_t* __restrict__ src, long long lds,
-                                   uint16_t* __restrict__ dst, long long ldd, int rows, int cols) {
+__device__ __forceinline__ void realign_rows(const uint16_t* __restrict__ src, long long lds,
+                                             uint16_t* __restrict__ dst, long long ldd, int rows,
+                                             int cols, long long block, long long nblocks) {
   const long long groups = ldd / 8;
   const long long total = static_cast<long long>(rows) * groups;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+  for (long long g = block * blockDim.x + threadIdx.x; g < total; g += nblocks * blockDim.x) {
     const int r = static_cast<int>(g / groups);
     const int c0 = static_cast<int>(g % groups) * 8;
     const uint16_t* p = src + static_cast<long long>(r) * lds + c0;
@@ -118,7 +118,10 @@ __global__ void realign_f16_kernel(const uint16_t* __restrict__ src, long long l
       const uintptr_t a = reinterpret_cast<uintptr_t>(p);
       const uint32_t m = static_cast<uint32_t>(a & 15u);
       const uint4* blk = reinterpret_cast<const uint4*>(a - m);
-      // m is even: half pointers are 2-byte aligned (checked by the host)
+      // m is even: half pointers are 2-byte aligned (checked by the host).
+      // blk + 1 starts 16 - m bytes into the 16 bytes read, so both aligned
+      // blocks hold bytes of the row: no read leaves a 16-byte block (and so
+      // a page) that holds operand data.
       v = (m == 0) ? __ldg(blk) : shift_bytes(__ldg(blk), __ldg(blk + 1), m);
     } else {
       uint32_t h[8];
@@ -129,6 +132,19 @@ __global__ void realign_f16_kernel(const uint16_t* __restrict__ src, long long l
     }
     *reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * ldd + c0) = v;
   }
+}
+
+// Both operands in one launch: blocks [0, grid_a) copy the first, the others
+// the second (rows2 == 0: none).
+__global__ void realign_f16_kernel(const uint16_t* __restrict__ src1, long long lds1,
+                                   uint16_t* __restrict__ dst1, long long ldd1, int rows1, int cols1,
+                                   const uint16_t* __restrict__ src2, long long lds2,
+                                   uint16_t* __restrict__ dst2, long long ldd2, int rows2, int cols2,
+                                   int grid_1) {
+  if (static_cast<int>(blockIdx.x) < grid_1)
+    realign_rows(src1, lds1, dst1, ldd1, rows1, cols1, blockIdx.x, grid_1);
+  else
+    realign_rows(src2, lds2, dst2, ldd2, rows2, cols2, blockIdx.x - grid_1, gridDim.x - grid_1);
 }
 
 // tf32 value nearest to x (ties away from zero), as fp32 bits with the low 13
@@ -315,9 +331,13 @@ cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float
 }
 
 
-cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
-                               int rows, int cols, int grid, cudaStream_t stream) {
-  realign_f16_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, rows, cols);
+cudaError_t launch_realign_f16(const RealignJob& first, const RealignJob* second, int grid_1,
+                               int grid_2, cudaStream_t stream) {
+  const RealignJob none{};
+  const RealignJob& b = second ? *second : none;
+  realign_f16_kernel<<<grid_1 + (second ? grid_2 : 0), 256, 0, stream>>>(
+      first.src, first.lds, first.dst, first.ldd, first.rows, first.cols, b.src, b.lds, b.dst, b.ldd,
+      b.rows, b.cols, grid_1);
   return counted_launch(cudaGetLastError());
 }
 

@@ -118,8 +118,17 @@ cudaError_t launch_splitk_reduce_f16(const float* ws, long long ws_ld, int split
 
 // Copies a rows x cols half matrix with any leading dimension and alignment
 // into a 16-byte-aligned one with ldd = cols rounded up to 8 (zero padding).
-cudaError_t launch_realign_f16(const uint16_t* src, long long lds, uint16_t* dst, long long ldd,
-                               int rows, int cols, int grid, cudaStream_t stream);
+struct RealignJob {
+  const uint16_t* src;
+  long long lds;
+  uint16_t* dst;
+  long long ldd;
+  int rows, cols;
+};
+// One launch for one or two copies (second may be null): grid_1 blocks on the
+// first, grid_2 on the second.
+cudaError_t launch_realign_f16(const RealignJob& first, const RealignJob* second, int grid_1,
+                               int grid_2, cudaStream_t stream);
 
 // Both splits of a 3xTF32 product in one launch: A (M x K) into Ab, As and
 // B^T (B is K x N) into Bb, Bs, all with leading dimension ld2 (>= K, % 4 == 0);
