@@ -243,18 +243,22 @@ SkPlan plan_stream_k(long long tiles, long long slots, int kb, bool all_tiles) {
 
 // Whether stream-K over all of a few tiles (plan_stream_k's all_tiles form)
 // is expected to beat half-width whole-K units, in k-block times of one
-// tile: stream-K takes the longest range plus a fix-up growing with the
-// pieces a tile is cut into (publishing and re-reading partial sums); a wave
-// of half-width units takes about 3/4 of a tile's k-blocks (measured: they
-// stage 3/4 of the operand bytes for half the FLOPs).  Measured at 1024^3
-// (32 tiles of 16 k-blocks): half-width units 16 us, stream-K 24 us; at
-// 16x8192x8192 (64 tiles of 128 k-blocks): stream-K 42 us, equal K slices 51.
-bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool halves_ok) {
+// tile: stream-K takes the longest range plus a fix-up for every extra piece
+// of a tile, in proportion to the partial sums each publishes and the
+// finisher re-reads (about 8 k-blocks for 128 full rows of a 128-wide tile);
+// a wave of half-width units takes about 3/4 of a tile's k-blocks (measured:
+// they stage 3/4 of the operand bytes for half the FLOPs).  Measured: 1024^3
+// (32 tiles of 16 k-blocks) half-width units 16 us, stream-K 24 us;
+// 1000x1001x4096 (32 tiles of 64) 38 us and 61 us; 16x8192x8192 (64 tiles of
+// 128, 16 rows) stream-K 42 us, equal K slices 51 us.
+bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool halves_ok,
+                               int rows, int bn) {
   const SkPlan sk = plan_stream_k(tiles, slots, kb, true);
   if (sk.sk_tiles == 0) return false;
   if (!halves_ok) return true;
   const long long range = (sk.sk_tiles * kb + sk.workers - 1) / sk.workers;
-  const long long sk_cost = range + kSkFixKb + 4 * (sk.max_pieces - 1);
+  const long long per_piece = std::max(1ll, 8ll * std::min(rows, kBM) * bn / (kBM * 128));
+  const long long sk_cost = range + kSkFixKb + per_piece * (sk.max_pieces - 1);
   const long long waves = (2 * tiles + slots - 1) / slots;
   const long long halves_cost = (3 * kb * waves + 3) / 4;
   return sk_cost < halves_cost;
@@ -434,7 +438,8 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   const bool few = tiles * 2 <= d->sm_count && a.kb_total >= 8;
   const bool few_sk =
       (few && force == 0 &&
-       few_tiles_prefer_stream_k(tiles, d->sm_count, a.kb_total, load == kLoadTma && bn >= 128)) ||
+       few_tiles_prefer_stream_k(tiles, d->sm_count, a.kb_total, load == kLoadTma && bn >= 128, M,
+                                 bn)) ||
       force == 11;
   if (force == 3) {
     // as many K slices as fit in ONE wave of CTAs (a second, partial wave would
