@@ -158,6 +158,20 @@ def _fill_device(shape, dtype_np, seed, stream_id, dist="uniform"):
     return torch.from_numpy(host).cuda(), host
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of `values` (a list of floats) over all ranks of
+    the default process group: the slowest rank's times decide the job's
+    throughput.  `device` is where the reduction runs ("cuda" under NCCL,
+    "cpu" under gloo)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 # ---------------------------------------------------------------- device-timed replays
 
 class LaunchTally:
@@ -242,9 +256,7 @@ def run_ours(args, rank, world):
     mean16 = sum(ms16) / len(ms16)
     mean32 = sum(ms32) / len(ms32)
     if world > 1:
-        t = torch.tensor([mean16, mean32], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean16, mean32 = float(t[0]), float(t[1])
+        mean16, mean32 = max_over_ranks([mean16, mean32], device="cuda")
     flops = 2.0 * M * N * K
     tflops16 = flops / (mean16 * 1e-3) / 1e12
     tflops32 = flops / (mean32 * 1e-3) / 1e12
@@ -317,9 +329,7 @@ def run_ours(args, rank, world):
     LaunchTally.total += g.launch_count() - n0
     e2e_mean = sum(e2e_ms) / len(e2e_ms)
     if world > 1:
-        t = torch.tensor([e2e_mean], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_mean = float(t[0])
+        (e2e_mean,) = max_over_ranks([e2e_mean], device="cuda")
 
     peak16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
