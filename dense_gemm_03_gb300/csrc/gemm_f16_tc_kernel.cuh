@@ -783,6 +783,10 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             if (!kCs && EPI == kEpiTma && has_c) load_c_sub(p, row, colw, c_next);
           }
         }
+        // Every other piece of the tile has counted in: the finisher clears the
+        // counter, so the next launch starts from zero whatever its epoch (a
+        // replayed CUDA graph repeats the captured epoch).
+        if (finish && lane == 0) *reinterpret_cast<volatile unsigned long long*>(cnt) = 0ull;
       }
 
       if (kCs && !finish) {   // unused C retired

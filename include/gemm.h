@@ -40,12 +40,16 @@
  *              stream) and the call returns without synchronising.  Calls on
  *              different streams that write the same C race.
  *   Scratch    some shapes split K over several thread blocks and need an
- *              fp32 workspace: small M*N with a long K, and the tiles of the
- *              last, partial wave when the tiles outnumber the SMs; unaligned
- *              half operands need an aligned copy.  The library owns this
- *              scratch, per device and stream, grows it on first need (that
- *              call may allocate device memory) and frees it in
+ *              fp32 workspace (few tiles with a long K: stream-K; the forced
+ *              split paths); unaligned half operands need an aligned copy;
+ *              the fp32 path keeps its tf32 operand parts.  The library owns
+ *              this scratch, per device and stream, grows it on first need
+ *              (that call may allocate device memory) and frees it in
  *              gemm_release().
+ *   Graphs     a call may be captured in a CUDA graph on `stream` once the
+ *              same shape has run on that stream outside the capture (so
+ *              that no scratch has to be allocated inside it); replays give
+ *              the same results as direct calls.
  *   Errors     a negative return code (below) and nothing enqueued, except
  *              GEMM_ERR_CUDA, which reports a failed launch.  Kernels never
  *              trap: a wait that runs past its time limit sets a device

@@ -1,0 +1,57 @@
+"""The GEMM captured in a CUDA graph and replayed: schedules whose shared
+tiles count their pieces in device counters (stream-K, K slices) must give
+the right result on every replay, with new operands each time."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import check, operands, torch
+
+pytestmark = pytest.mark.gpu
+
+AUTO, SPLITK, TAIL2, SK_ALL = 0, 3, 9, 11
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dense_gemm_03_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("M,N,K,path,mark", [
+    (16, 8192, 8192, AUTO, ".sk"),
+    (300, 500, 3000, SPLITK, ".splitk"),
+    (2000, 2600, 4096, TAIL2, ".tail"),
+    (64, 128, 4096, SK_ALL, ".sk"),
+])
+def test_graph_replays(M, N, K, path, mark):
+    import dense_gemm_03_gb300 as g
+    t = torch()
+    s = t.cuda.Stream()
+    dA = t.empty((M, K), dtype=t.float16, device="cuda")
+    dB = t.empty((K, N), dtype=t.float16, device="cuda")
+    dC = t.empty((M, N), dtype=t.float16, device="cuda")
+    prev = g.force_path(path)
+    try:
+        # a first call outside the capture sets up scratch buffers and counters
+        A, B, C0 = operands(5000, M, N, K, K, N, N, np.float16)
+        dA.copy_(t.from_numpy(A)); dB.copy_(t.from_numpy(B)); dC.copy_(t.from_numpy(C0))
+        g.gemm_f16(dA, dB, dC, 0.75, -0.25, stream=s)
+        s.synchronize()
+        assert mark in g.last_path()
+        graph = t.cuda.CUDAGraph()
+        with t.cuda.graph(graph, stream=s):
+            g.gemm_f16(dA, dB, dC, 0.75, -0.25, stream=s)
+    finally:
+        g.force_path(prev)
+    for i in range(3):
+        A, B, C0 = operands(5001 + i, M, N, K, K, N, N, np.float16)
+        dA.copy_(t.from_numpy(A)); dB.copy_(t.from_numpy(B)); dC.copy_(t.from_numpy(C0))
+        t.cuda.synchronize()
+        graph.replay()
+        t.cuda.synchronize()
+        got = dC.cpu().numpy()
+        big = M * N * K > 2e9
+        check("f16", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N,
+              rows=oracle.sample_rows(M) if big else None, cols=oracle.sample_cols(N) if big else None)
+    assert g.debug_status() == 0
