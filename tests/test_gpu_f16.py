@@ -379,3 +379,17 @@ def test_skinny_parity(M, N, K, mark, alpha, beta, c_fill):
     got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, N)
     assert mark in taken, taken
     check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
+
+
+# ---------------------------------------------------------------- extreme dimensions
+@pytest.mark.parametrize("M,N,K", [
+    (4096, 1024, 1),       # K = 1: one ragged k-block, realigned operands
+    (1, 1, 65536),         # one output, a very long K
+    (1, 16384, 256),       # one row
+    (3, 5, 100003),        # ragged everything, long K
+    (16384, 1, 64),        # one column
+])
+def test_extreme_dimensions(M, N, K):
+    A, B, C0 = operands(31337 + M + N, M, N, K, K, N, N, np.float16)
+    got, taken = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+    check("f16", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N)

@@ -159,3 +159,10 @@ def test_3xtf32_half_width_tail(M, N, K):
     check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N, rows=rows)
     bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
     assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 65536), (300, 260, 1), (257, 1000, 64), (3000, 1, 4)])
+def test_fp32_extreme_dimensions(M, N, K):
+    A, B, C0 = operands(4242 + M + K, M, N, K, K, N, N, np.float32)
+    got, _ = run("f32", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+    check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
