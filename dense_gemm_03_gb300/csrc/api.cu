@@ -2,18 +2,26 @@
 // checks, path choice, tensor-map construction, workspace management and
 // kernel launches on the caller's stream.
 //
-// Path choice for the half-precision GEMM (gemm_f16_ld):
+// Path choice for the half-precision GEMM (gemm_f16_ld, gemm_f16_f32out):
 //   1. M == 0 or N == 0                 -> nothing to do
 //   2. alpha == 0 or K == 0             -> scale-only kernel, C := beta*C
-//   3. tile width BN from N (64 / 128 / 256)
+//   3. tile width BN from N (64 / 128 / 256; 128 when one row of 256-wide
+//      tiles could not fill the SMs)
 //   4. operand loads: TMA when A and B start on 16-byte boundaries and
-//      lda*2, ldb*2 are multiples of 16 bytes, else predicated element loads
-//      (the run-time alignment check of the "advanced SGEMM" page, kernel
-//      selection section, extended to the 16-byte rule of TMA)
-//   5. epilogue: TMA for C under the same rule when N is a multiple of 8,
-//      else predicated accesses
-//   6. split-K over an fp32 workspace when the output tiles alone cannot
-//      fill the SMs and K is long enough to share out
+//      lda*2, ldb*2 are multiples of 16 bytes (the run-time alignment check
+//      of the "advanced SGEMM" page, kernel selection section, extended to
+//      the 16-byte rule of TMA); an operand that breaks it is first copied to
+//      16-byte rows (one launch for both), else predicated element loads
+//   5. epilogue: TMA for a half C under the same rule when N is a multiple of
+//      8, else predicated accesses; a float C is written from registers
+//   6. few tiles for many SMs with a long K: stream-K over all tiles when it
+//      is expected to beat half-width units (few_tiles_prefer_stream_k)
+//   7. CTA pairs (256 x 256 tiles) for 256-wide TMA shapes with at least two
+//      tile rows; 32 or 64 rows of A staged per k-block when M <= 64
+//   8. the tiles of the last, partial wave run as two half-width units each
+//      when the halves fit in one wave
+// The fp32 GEMM (sgemm_f32_ld) takes the 3xTF32 tensor-core path for
+// M, N >= 256 and K >= 64, else the FFMA kernel.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -299,7 +307,8 @@ int scale_grid(const DevState& d, long long elems) {
   return static_cast<int>(std::max(1ll, std::min<long long>(blocks, 8ll * d.sm_count)));
 }
 
-const char* kPathNames[3][3][3] = {
+// [bn index][load][epilogue: TMA, predicated, fp32 partial sums (split-K)]
+const char* kPathNames[3][2][3] = {
     // [bn index][load][epi]
     {{"f16.tc.bn64.tma.epi_tma", "f16.tc.bn64.tma.epi_manual", "f16.tc.bn64.tma.splitk"},
      {"f16.tc.bn64.manual.epi_tma", "f16.tc.bn64.manual.epi_manual", "f16.tc.bn64.manual.splitk"}},
