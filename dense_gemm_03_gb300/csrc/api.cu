@@ -288,7 +288,7 @@ int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long lon
 }
 
 int make_map_f32(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
-                 int box_cols, int box_rows) {
+                 int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = nullptr;
   if (int rc = encode_fn(&enc)) return rc;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -296,9 +296,8 @@ int make_map_f32(CUtensorMap* map, const void* ptr, int rows, int cols, long lon
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -474,6 +473,10 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   const bool pair = splits == 1 && !few_sk && force != 6 && bn == 256 &&
                     load == kLoadTma && a.tiles_m >= 2 &&
                     (pair_slots = tc_pair_max_clusters(epi)) > 0;
+  // fp32 C on CTA pairs goes through shared memory and TMA when its rows are
+  // 16-byte aligned and N is a multiple of 4 (a TMA store writes whole 16-byte
+  // pieces of a row)
+  if (epi == kEpiF32 && pair && a.vec_c && N % 4 == 0) epi = kEpiF32Tma;
   long long units_tiles = tiles;   // tiles in units of the worker (CTA or pair)
   long long slots = d->sm_count;   // workers that can run at once
   if (pair) {
@@ -579,13 +582,19 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   if (epi == kEpiTma) {
     // epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle
     if (int rc = make_map_f16(&tmC, a.C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
+  } else if (epi == kEpiF32Tma) {
+    // the same 64-byte rows: 32 rows x 16 floats
+    if (int rc = make_map_f32(&tmC, a.Cf, M, N, ldc, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
   }
   // one CTA (pair) per worker; with stream-K exactly sk_workers of them
   const long long nw = a.sk_tiles > 0 ? a.sk_workers : std::min<long long>(a.num_units, workers);
   if (pair) {
     const int grid = 2 * static_cast<int>(nw);
     snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s",
-             c_f32 ? "f16.tc.pair.bn256.tma.epi_f32" : kPairPathNames[epi], cut, how);
+             c_f32 ? (epi == kEpiF32Tma ? "f16.tc.pair.bn256.tma.epi_f32_tma"
+                                        : "f16.tc.pair.bn256.tma.epi_f32")
+                   : kPairPathNames[epi],
+             cut, how);
     t_last_path = t_path_buf;
     if (launch_gemm_f16_tc_pair(epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;

@@ -28,15 +28,18 @@ cudaError_t launch_gemm_f16_tc_f32(int bn, int load_mode, const CUtensorMap& tmA
   }
 }
 
-cudaError_t launch_gemm_f16_tc_pair_f32(const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_gemm_f16_tc_pair_f32(int epi_mode, const CUtensorMap& tmA,
+                                        const CUtensorMap& tmB, const CUtensorMap& tmC,
                                         const TcArgs& args, int grid, cudaStream_t stream) {
+  if (epi_mode == kEpiF32Tma)
+    return launch_one<256, kLoadTma, kEpiF32Tma, true>(tmA, tmB, tmC, args, grid, stream);
   return launch_one<256, kLoadTma, kEpiF32, true>(tmA, tmB, tmA, args, grid, stream);
 }
 
-int tc_pair_max_clusters_f32() {
+int tc_pair_max_clusters_f32(int epi_mode) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  return pair_max_clusters<kEpiF32>(dev);
+  return epi_mode == kEpiF32Tma ? pair_max_clusters<kEpiF32Tma>(dev) : pair_max_clusters<kEpiF32>(dev);
 }
 
 }  // namespace gb300

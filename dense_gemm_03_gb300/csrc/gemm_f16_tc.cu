@@ -39,7 +39,8 @@ cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtens
 cudaError_t launch_gemm_f16_tc_pair(int epi_mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                     const CUtensorMap& tmC, const TcArgs& args, int grid,
                                     cudaStream_t stream) {
-  if (epi_mode == kEpiF32) return launch_gemm_f16_tc_pair_f32(tmA, tmB, args, grid, stream);
+  if (epi_mode == kEpiF32 || epi_mode == kEpiF32Tma)
+    return launch_gemm_f16_tc_pair_f32(epi_mode, tmA, tmB, tmC, args, grid, stream);
   if (epi_mode == kEpiTma)
     return launch_one<256, kLoadTma, kEpiTma, true>(tmA, tmB, tmC, args, grid, stream);
   if (epi_mode == kEpiManual)
@@ -50,7 +51,7 @@ cudaError_t launch_gemm_f16_tc_pair(int epi_mode, const CUtensorMap& tmA, const 
 int tc_pair_max_clusters(int epi_mode) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (epi_mode == kEpiF32) return tc_pair_max_clusters_f32();
+  if (epi_mode == kEpiF32 || epi_mode == kEpiF32Tma) return tc_pair_max_clusters_f32(epi_mode);
   return epi_mode == kEpiTma ? pair_max_clusters<kEpiTma>(dev) : pair_max_clusters<kEpiManual>(dev);
 }
 

@@ -105,7 +105,7 @@ template <int BN, int EPI, bool PAIR, int AM = 128>
 struct Smem {
   // C read by TMA into the epilogue's staging tiles: the CTA-pair kernel with
   // TMA stores
-  static constexpr bool kCs = PAIR && EPI == kEpiTma;
+  static constexpr bool kCs = PAIR && (EPI == kEpiTma || EPI == kEpiF32Tma);
   using Cfg = TcCfg<BN, PAIR, kCs, AM>;
   // 32 x 32 staging tiles per epilogue warp
   static constexpr int kBufs = kCs ? kCsBufs : 2;
@@ -328,6 +328,21 @@ __device__ __forceinline__ uint4 epilogue8(const uint32_t* acc, uint4 cbits, boo
                     float2_to_half2_bits(o[4], o[5]), float2_to_half2_bits(o[6], o[7]));
 }
 
+// alpha*acc (+ beta*c) for 4 accumulator columns -> 4 floats (16 bytes).
+__device__ __forceinline__ uint4 epilogue4f(const uint32_t* acc, uint4 cbits, bool has_c,
+                                            float alpha, float beta) {
+  const float c[4] = {__uint_as_float(cbits.x), __uint_as_float(cbits.y), __uint_as_float(cbits.z),
+                      __uint_as_float(cbits.w)};
+  float o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = __uint_as_float(acc[i]);
+    o[i] = has_c ? __fmaf_rn(alpha, a, beta * c[i]) : alpha * a;
+  }
+  return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                    __float_as_uint(o[3]));
+}
+
 // C values of one row for a 32-column sub-chunk (4 groups of 8 halves), read
 // straight into registers with streaming loads; zero outside the matrix.  Used
 // by the TMA epilogue, where rows of C are 16-byte aligned and N % 8 == 0.
@@ -451,7 +466,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  if (EPI == kEpiTma && warp == R::kEpiWarp0 && lane == 0) prefetch_tensormap(&tmC);
+  if ((EPI == kEpiTma || EPI == kEpiF32Tma) && warp == R::kEpiWarp0 && lane == 0)
+    prefetch_tensormap(&tmC);
   tc_fence_before();
   __syncwarp();
   if (PAIR)
@@ -654,13 +670,15 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     const uint32_t sbuf0 = base + L::kEpiOff + ew * L::kWarpEpiBytes;
     uint8_t* const sptr0 = base_ptr + L::kEpiOff + ew * L::kWarpEpiBytes;
     uint32_t local = 0, nstore = 0;
-    // kCs: C sub-tiles (32 rows x 32 columns) are read by TMA into the
-    // staging tiles, where the result replaces them and is stored by TMA.
-    // The first kBufs sub-tiles of a unit are requested while its main loop
-    // runs; sub-tile k + kBufs as soon as the store of sub-tile k has read its
-    // tile.  c_loads[b] counts the loads into tile b (the parity of its
-    // barrier).
+    // kCs: C sub-tiles (32 rows x 64 bytes: 32 halves or 16 floats) are read
+    // by TMA into the staging tiles, where the result replaces them and is
+    // stored by TMA.  The first kBufs sub-tiles of a unit are requested while
+    // its main loop runs; sub-tile j + kBufs as soon as the store of sub-tile
+    // j has read its tile.  c_loads[b] counts the loads into tile b (the
+    // parity of its barrier).
     constexpr int NB = L::kBufs;
+    constexpr int kTc = (EPI == kEpiF32Tma) ? 16 : 32;   // columns per staging sub-tile
+    constexpr int kTpc = kSubCols / kTc;                  // staging sub-tiles per TMEM chunk
     uint32_t c_loads[NB];
     bool c_pending[NB];
 #pragma unroll
@@ -689,8 +707,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       const int r0 = u2.m0 + 32 * q, cw = u2.n0 + h * wc;
       if (!has_c || r0 >= p.M || cw >= p.N) return;
 #pragma unroll
-      for (int k = 0; k < NB && k < kSubs; ++k)
-        if (kSubCols * k < wc && cw + kSubCols * k < p.N) load_c_sub_tma(k, cw + kSubCols * k, r0);
+      for (int j = 0; j < NB; ++j)
+        if (kTc * j < wc && cw + kTc * j < p.N) load_c_sub_tma(j, cw + kTc * j, r0);
     };
     UnitCursor cur = first_unit(p, worker);
     Unit t, tn;
@@ -713,10 +731,11 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         // L2, so that the epilogue's reads of C wait on L2 and not on DRAM.
         const int ncols = min(wcols, p.N - colw);
         const long long e0 = static_cast<long long>(row) * p.ldc + colw;
-        const uintptr_t c0 = EPI == kEpiF32 ? reinterpret_cast<uintptr_t>(p.Cf + e0)
+        constexpr bool kF32C = EPI == kEpiF32 || EPI == kEpiF32Tma;
+        const uintptr_t c0 = kF32C ? reinterpret_cast<uintptr_t>(p.Cf + e0)
                                             : reinterpret_cast<uintptr_t>(p.C + e0);
         const uintptr_t first = c0 & ~static_cast<uintptr_t>(127);
-        const uintptr_t last = c0 + static_cast<uintptr_t>(ncols) * (EPI == kEpiF32 ? 4 : 2) - 1;
+        const uintptr_t last = c0 + static_cast<uintptr_t>(ncols) * (kF32C ? 4 : 2) - 1;
         for (uintptr_t a = first; a <= last; a += 128) prefetch_l2(reinterpret_cast<const void*>(a));
       }
       // C of the first sub-chunk is requested before the accumulator is ready.
@@ -893,31 +912,45 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
               }
             }
           } else if (kCs) {
-            // C sub-tile k in staging tile k % NB -> result in place -> TMA store
-            const int b = k % NB;
-            uint8_t* const sptr = sptr0 + b * kEpiBufBytes;
-            if (has_c) {
-              if (!wait_c_sub(b)) break;
-            } else {
-              // the store issued from this tile NB sub-chunks ago must have read it
-              if (lane == 0) bulk_wait_group_read<NB - 1>();
-              __syncwarp();
-            }
+            // staging sub-tile j in tile j % NB -> result in place -> TMA store
+            bool c_ok = true;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              uint8_t* const e = sptr + sw64_chunk(lane, g);
-              const uint4 cv =
-                  has_c ? *reinterpret_cast<const uint4*>(e) : make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(e) = epilogue8(cur + 8 * g, cv, has_c, p.alpha, p.beta);
+            for (int e = 0; e < kTpc; ++e) {
+              const int j = k * kTpc + e;
+              const int colt = col0 + e * kTc;
+              if (colt >= p.N) break;
+              const int b = j % NB;
+              uint8_t* const sptr = sptr0 + b * kEpiBufBytes;
+              if (has_c) {
+                if (!wait_c_sub(b)) {
+                  c_ok = false;
+                  break;
+                }
+              } else {
+                // the store issued from this tile NB sub-tiles ago must have read it
+                if (lane == 0) bulk_wait_group_read<NB - 1>();
+                __syncwarp();
+              }
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                uint8_t* const ep = sptr + sw64_chunk(lane, g);
+                const uint4 cv =
+                    has_c ? *reinterpret_cast<const uint4*>(ep) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(ep) =
+                    (EPI == kEpiF32Tma)
+                        ? epilogue4f(cur + e * kTc + 4 * g, cv, has_c, p.alpha, p.beta)
+                        : epilogue8(cur + 8 * g, cv, has_c, p.alpha, p.beta);
+              }
+              fence_proxy_async_smem();   // generic writes -> TMA store reads
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, sbuf0 + b * kEpiBufBytes, colt, row0);
+                bulk_commit_group();
+              }
+              if (has_c && j + NB < nsub * kTpc && colt + NB * kTc < p.N)
+                load_c_sub_tma(b, colt + NB * kTc, row0);
             }
-            fence_proxy_async_smem();   // generic writes -> TMA store reads
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmC, sbuf0 + b * kEpiBufBytes, col0, row0);
-              bulk_commit_group();
-            }
-            if (has_c && k + NB < nsub && col0 + NB * kSubCols < p.N)
-              load_c_sub_tma(b, col0 + NB * kSubCols, row0);
+            if (!c_ok) break;
           } else if (EPI == kEpiTma) {
             const uint32_t b = nstore & 1u;
             const uint32_t sbuf = sbuf0 + b * kEpiBufBytes;
@@ -997,7 +1030,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     for (int b = 0; b < NB; ++b)
       if (kCs && c_pending[b] && lane == 0)
         drain_wait(cfull_bar(ew, b), (c_loads[b] - 1u) & 1u, st, 17);
-    if (EPI == kEpiTma && lane == 0) bulk_wait_group<0>();   // stores done reading smem
+    if ((EPI == kEpiTma || kCs) && lane == 0) bulk_wait_group<0>();   // stores done reading smem
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(tmem_free_bar);

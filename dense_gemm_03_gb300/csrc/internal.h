@@ -22,7 +22,9 @@ struct DeviceStatus;
 enum LoadMode : int { kLoadTma = 0, kLoadManual = 1 };
 // Epilogue modes: TMA load/store of C, predicated element access of C, or
 // raw fp32 partial sums to the split-K workspace.
-enum EpiMode : int { kEpiTma = 0, kEpiManual = 1, kEpiPartial = 2, kEpiF32 = 3 };
+// kEpiF32: fp32 C from registers; kEpiF32Tma: fp32 C through shared memory
+// and TMA (CTA pairs, C 16-byte aligned, N % 4 == 0).
+enum EpiMode : int { kEpiTma = 0, kEpiManual = 1, kEpiPartial = 2, kEpiF32 = 3, kEpiF32Tma = 4 };
 
 struct TcArgs {
   const uint16_t* A;
@@ -83,9 +85,10 @@ int tc_threads(int load_mode);
 cudaError_t launch_gemm_f16_tc_f32(int bn, int load_mode, const CUtensorMap& tmA,
                                    const CUtensorMap& tmB, const TcArgs& args, int grid,
                                    cudaStream_t stream);
-cudaError_t launch_gemm_f16_tc_pair_f32(const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_gemm_f16_tc_pair_f32(int epi_mode, const CUtensorMap& tmA,
+                                        const CUtensorMap& tmB, const CUtensorMap& tmC,
                                         const TcArgs& args, int grid, cudaStream_t stream);
-int tc_pair_max_clusters_f32();
+int tc_pair_max_clusters_f32(int epi_mode);
 
 // The same GEMM (128-wide tiles, TMA loads, one CTA per tile) for M <= am,
 // staging am = 32 or 64 rows of A per k-block (gemm_f16_skinny.cu).

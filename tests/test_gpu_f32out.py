@@ -47,8 +47,9 @@ def _c32(seed, M, ldc, fill="uniform"):
 
 @pytest.mark.parametrize("M,N,K,path,mark", [
     (256, 512, 128, AUTO, ".epi_f32"),
-    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_f32.halves"),
-    (2000, 2600, 2048, SK, ".pair.bn256.tma.epi_f32.sk"),
+    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_f32_tma.halves"),
+    (2000, 2601, 1024, AUTO, ".pair.bn256.tma.epi_f32.halves"),    # N % 4 != 0: direct stores
+    (2000, 2600, 2048, SK, ".pair.bn256.tma.epi_f32_tma.sk"),
     (16, 8192, 8192, AUTO, ".bn128.tma.epi_f32.a32.sk"),
     (48, 3000, 1500, AUTO, ".epi_f32.a64"),
     (700, 300, 500, NO_PAIR, ".bn256.tma.epi_f32"),
@@ -125,7 +126,7 @@ def test_rounded_to_half_equals_gemm_f16():
     A, B, C16 = operands(404, M, N, K, K, N, N, np.float16)
     want, p16 = run("f16", A, B, C16, 1.5, 0.5, M, N, K, K, N, N)
     got32, p32 = run32(A, B, C16.astype(np.float32), 1.5, 0.5, M, N, K, K, N, N)
-    assert p16.replace("epi_tma", "epi_f32") == p32, (p16, p32)
+    assert p16.replace("epi_tma", "epi_f32_tma") == p32, (p16, p32)
     src = t.from_numpy(got32.reshape(-1)).cuda()
     dst = t.empty(src.numel(), dtype=t.float16, device="cuda")
     g.f32_to_f16(src, dst)
