@@ -52,6 +52,8 @@ def library_path() -> str:
 def lib():
     """The loaded library (ctypes.CDLL).  Raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
@@ -112,15 +114,32 @@ def _addr(x):
     raise TypeError("expected a tensor, an array or an address, got %r" % type(x))
 
 
-def _stream(stream):
-    if stream is None:
+_current_stream = None
+
+
+def _current_stream_fn():
+    """A cheap getter of the current CUDA stream's handle (None without CUDA)."""
+    global _current_stream
+    if _current_stream is None:
+        fn = lambda: None
         try:
             import torch
             if torch.cuda.is_available():
-                return torch.cuda.current_stream().cuda_stream
+                raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+                dev = getattr(torch._C, "_cuda_getDevice", None)
+                if raw is not None and dev is not None:
+                    fn = lambda: raw(dev())
+                else:
+                    fn = lambda: torch.cuda.current_stream().cuda_stream
         except ImportError:
             pass
-        return None
+        _current_stream = fn
+    return _current_stream
+
+
+def _stream(stream):
+    if stream is None:
+        return _current_stream_fn()()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
