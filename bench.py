@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 METRIC = ("GEMM TFLOPS (2MNK/t) at 4096³ fp16-in/fp32-acc and fp32; "
           "% of tensor/FMA peak")
 F16_CFG = dict(M=4096, N=4096, K=4096, alpha=1.5, beta=0.5)
+PATH_FFMA_ONLY = 7          # gemm_force_path: the CUDA-core FFMA SGEMM only
 F32_CFG = dict(M=4096, N=4096, K=4096, alpha=1.0, beta=0.0)
 # (M, N, K, lda, alpha, beta, name): the fp16 edge shapes, ldb = ldc = N
 EDGE_SHAPES = [
@@ -245,8 +246,11 @@ def run_ours(args, rank, world):
     path16 = g.last_path()
     launches16 = LaunchTally.last / args.steps
     f32_steps = max(3, args.steps // 20)
+    prev_path = g.force_path(PATH_FFMA_ONLY) if args.f32_ffma else None
     ms32 = timed_replays(f32, f32_steps, max(3, args.warmup // 10), stream, flush_bytes)
     path32 = g.last_path()
+    if prev_path is not None:
+        g.force_path(prev_path)
     launches32 = LaunchTally.last / f32_steps
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
@@ -390,7 +394,8 @@ def run_ours(args, rank, world):
             "launches_per_step": launches16,
         },
         "fp32_sgemm": {
-            "workload": "fp32 SGEMM C=A*B, M=N=K=4096, alpha=1 beta=0",
+            "workload": "fp32 SGEMM C=A*B, M=N=K=4096, alpha=1 beta=0" +
+                        (" (CUDA-core FFMA kernel forced)" if args.f32_ffma else ""),
             "value": round(tflops32 * world, 3),
             "unit": "TFLOPS",
             "ms_per_step": round(mean32, 5),
@@ -632,6 +637,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-shapes", action="store_true", help="skip the edge-shape timings")
+    ap.add_argument("--f32-ffma", action="store_true",
+                    help="time the fp32 leg on the CUDA-core FFMA kernel instead of 3xTF32")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-f16", action="store_true",
                     help="fp16 sweep: the automatic path beside the forced alternatives")

@@ -14,6 +14,12 @@
 //     of its warp's sub-tile), with tm = lane % 4 and tn = lane / 4, so a
 //     16-byte B fragment is shared by at most 4 consecutive lanes and an A
 //     fragment by lanes 4 apart;
+//   * the products use the packed two-lane FMA of sm_100-class GPUs
+//     (fma.rn.f32x2, one instruction for two adjacent columns of a row; each
+//     lane is an ordinary fp32 fused multiply-add, so the result is the same
+//     as with scalar FMAs in the same k order), which halves the FMA
+//     instructions per k step; the kernel then needs ~146 registers and runs
+//     one 256-thread block per SM;
 //   * with that thread layout every 16-byte store of C from a warp covers
 //     four full 128-byte row segments, so C is written (and, when beta != 0,
 //     read) coalesced straight from registers;
@@ -31,7 +37,7 @@ constexpr int kBM = 128, kBN = 128, kBK = 8;
 constexpr int kLdA = kBM + 4;   // padded, transposed A slice
 
 template <bool VEC>
-__global__ void __launch_bounds__(256, 2) sgemm_ffma_kernel(const SgemmArgs p) {
+__global__ void __launch_bounds__(256, 1) sgemm_ffma_kernel(const SgemmArgs p) {
   __shared__ __align__(16) float As[2][kBK][kLdA];
   __shared__ __align__(16) float Bs[2][kBK][kBN];
 
@@ -89,11 +95,13 @@ __global__ void __launch_bounds__(256, 2) sgemm_ffma_kernel(const SgemmArgs p) {
     fb[slot][1] = *reinterpret_cast<const float4*>(&Bs[buf][k][b_off1]);
   };
 
-  float acc[8][8];
+  // acc[i][q] holds columns 2q and 2q+1 of row i: one packed two-lane FMA
+  // (fma.rn.f32x2) updates both, so a k step is 32 instructions, not 64.
+  float2 acc[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
 
   const int nkt = (K + kBK - 1) / kBK;
   load_tile(0);
@@ -111,12 +119,14 @@ __global__ void __launch_bounds__(256, 2) sgemm_ffma_kernel(const SgemmArgs p) {
       const int s = k & 1;
       const float a[8] = {fa[s][0].x, fa[s][0].y, fa[s][0].z, fa[s][0].w,
                           fa[s][1].x, fa[s][1].y, fa[s][1].z, fa[s][1].w};
-      const float b[8] = {fb[s][0].x, fb[s][0].y, fb[s][0].z, fb[s][0].w,
-                          fb[s][1].x, fb[s][1].y, fb[s][1].z, fb[s][1].w};
+      const float2 b[4] = {make_float2(fb[s][0].x, fb[s][0].y), make_float2(fb[s][0].z, fb[s][0].w),
+                           make_float2(fb[s][1].x, fb[s][1].y), make_float2(fb[s][1].z, fb[s][1].w)};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const float2 ai = make_float2(a[i], a[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int q = 0; q < 4; ++q) acc[i][q] = __ffma2_rn(ai, b[q], acc[i][q]);
+      }
     }
     if (has_next) {
       store_tile(buf ^ 1);
@@ -127,6 +137,7 @@ __global__ void __launch_bounds__(256, 2) sgemm_ffma_kernel(const SgemmArgs p) {
   }
 
   // epilogue: alpha*acc (+ beta*C), straight from registers
+  auto elem = [&](int i, int j) { return (j & 1) ? acc[i][j >> 1].y : acc[i][j >> 1].x; };
   const bool has_c = p.beta != 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -143,13 +154,13 @@ __global__ void __launch_bounds__(256, 2) sgemm_ffma_kernel(const SgemmArgs p) {
         const float cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          o[j] = has_c ? fmaf(p.alpha, acc[i][h * 4 + j], p.beta * cv[j]) : p.alpha * acc[i][h * 4 + j];
+          o[j] = has_c ? fmaf(p.alpha, elem(i, h * 4 + j), p.beta * cv[j]) : p.alpha * elem(i, h * 4 + j);
         *reinterpret_cast<float4*>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (col + j < N) {
-            const float a = acc[i][h * 4 + j];
+            const float a = elem(i, h * 4 + j);
             crow[col + j] = has_c ? fmaf(p.alpha, a, p.beta * crow[col + j]) : p.alpha * a;
           }
         }
