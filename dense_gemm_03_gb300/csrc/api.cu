@@ -21,7 +21,8 @@
 //   8. the tiles of the last, partial wave run as two half-width units each
 //      when the halves fit in one wave
 // The fp32 GEMM (sgemm_f32_ld) takes the 3xTF32 tensor-core path for
-// M, N >= 256 and K >= 64, else the FFMA kernel.
+// M, N >= 256 and K >= 64 (with K slices when few tiles meet a long K,
+// plan_tf32_slices), else the FFMA kernel.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -182,6 +183,34 @@ int stream_scratch(DevState* d, cudaStream_t stream, size_t bytes, size_t counte
   }
   *out = &w;
   return GEMM_OK;
+}
+
+// K slices for the fp32 tensor-core kernel when few pair tiles leave most
+// pairs idle: the slice count in [2, cap] (slices of whole 4-k-block chunks)
+// with the least estimated time, or 1 when whole-K half-width units are
+// expected to be faster.  Estimates measured on GB300: a whole-K half-width
+// unit runs ~0.6 us per k-block, a full-width slice ~0.75 us, and publishing
+// plus adding up S slices' partial sums costs ~8 + 1.5 S us.  `forced` takes
+// the largest count up to `cap` whatever the estimate.
+struct TailSplit {
+  int splits = 1;
+  int kb_per_split = 0;
+};
+TailSplit plan_tf32_slices(int kb_total, int cap, bool forced) {
+  TailSplit best;
+  double best_us = 0.6 * kb_total;
+  for (int want = 2; want <= cap; ++want) {
+    const int per = ((kb_total + want - 1) / want + 3) / 4 * 4;
+    const int s = (kb_total + per - 1) / per;   // no empty slice
+    if (s < 2) continue;
+    const double us = 0.75 * per + 8.0 + 1.5 * s;
+    if (forced || us < best_us) {
+      best_us = us;
+      best.splits = s;
+      best.kb_per_split = per;
+    }
+  }
+  return best;
 }
 
 // Tail plan for `tiles` whole tiles on `ctas` persistent CTAs: the number of K
@@ -685,19 +714,53 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       t.tiles_m = (M + 255) / 256;
       t.tiles_n = (N + 255) / 256;
       t.kb_total = (K + 31) / 32;
-      // the tiles of the last, partial wave run as two half-width units each
-      // when the halves fit in one wave
       const int tiles = t.tiles_m * t.tiles_n;
-      const int rem = tiles % pairs;
-      const bool halves = force != 5 && rem > 0 && 2 * rem <= pairs;
-      t.dp_tiles = halves ? tiles - rem : tiles;
-      t.num_units = t.dp_tiles + 2 * (tiles - t.dp_tiles);
+      // Few tiles for the pairs and a long K: every tile is cut into equal K
+      // slices (whole 4-k-block accumulation chunks) that fill about one
+      // wave; each slice publishes fp32 partial sums and the last to finish
+      // adds them up.  Otherwise the tiles of the last, partial wave run as
+      // two half-width units each when the halves fit in one wave.
+      // gemm_force_splits: 1 keeps whole-K units, > 1 sets the slice count.
+      const int fs = g_force_splits.load();
+      int splits = 1;
+      if (force != 5 && fs != 1 && 2 * tiles <= pairs && t.kb_total >= 8) {
+        const int cap = std::min({fs > 1 ? fs : pairs / tiles, t.kb_total / 4, 16});
+        const TailSplit ts = plan_tf32_slices(t.kb_total, cap, fs > 1);
+        if (ts.splits > 1) {
+          splits = ts.splits;
+          t.kb_per_split = ts.kb_per_split;
+        }
+      }
+      bool halves = false;
+      t.splits = 1;
+      if (splits > 1) {
+        t.splits = splits;
+        t.dp_tiles = tiles;
+        t.num_units = tiles * splits;
+        // per tile: 2 CTAs x 8 epilogue warps x splits x (32 rows x 128 fp32)
+        const size_t need = static_cast<size_t>(tiles) * splits * 2 * 8 * 32 * 128 * sizeof(float);
+        std::lock_guard<std::mutex> lk(g_mu);
+        StreamWs* w = nullptr;
+        if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tiles) * 16, &w))
+          return rc;
+        t.part_ws = static_cast<float4*>(w->ptr);
+        t.counters = static_cast<unsigned long long*>(w->counters);
+        t.epoch = ++w->epoch;
+        if (t.epoch == 0) t.epoch = ++w->epoch;   // 0 marks never-used counters
+      } else {
+        const int rem = tiles % pairs;
+        halves = force != 5 && rem > 0 && 2 * rem <= pairs;
+        t.dp_tiles = halves ? tiles - rem : tiles;
+        t.num_units = t.dp_tiles + 2 * (tiles - t.dp_tiles);
+        t.kb_per_split = t.kb_total;
+      }
       t.group_m = 8;
       t.vec_c = aligned16(C) && ldc % 4 == 0;
       t.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
       t.status = d->status;
       const int grid = 2 * std::min(t.num_units, pairs);
-      t_last_path = halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair";
+      t_last_path = splits > 1 ? "f32.3xtf32.pair.ksplit"
+                               : (halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair");
       return launch_sgemm_3xtf32(mAb, mAs, mBb, mBs, mBbh, mBsh, t, grid, stream) == cudaSuccess
                  ? GEMM_OK
                  : GEMM_ERR_CUDA;

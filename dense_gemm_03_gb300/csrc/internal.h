@@ -162,6 +162,16 @@ struct Tf32Args {
   bool vec_c;             // C 16-byte aligned with ldc % 4 == 0
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
+  // splits > 1: every unit is one K slice of a whole tile (unit = tile *
+  // splits + slice, slice s covering k-blocks [s * kb_per_split, ...), a
+  // multiple of the 4-k-block accumulation chunk); each slice publishes fp32
+  // partial sums and the last one of a tile to finish adds them up in slice
+  // order and writes C
+  int splits;
+  int kb_per_split;
+  float4* part_ws;                  // [tile][rank][warp][slice][32 column quads][32 rows]
+  unsigned long long* counters;     // [tile][rank][warp]: (epoch << 32) | arrivals
+  unsigned int epoch;
 };
 // tmBbh / tmBsh: the B parts with 64-row boxes, for the half-width units.
 cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,

@@ -23,6 +23,11 @@
 // epilogue (8 warps, fp32 written straight from registers) follow the fp16
 // tensor-core kernel.  Both operands are K-major (the pre-pass stores the B
 // parts transposed): 128-byte swizzle, 32 floats per row, SBO 1024 B.
+//
+// Units: whole 256 x 256 tiles; the tiles of a last, partial wave as two
+// half-width units each; or, when few tiles meet a long K, equal K slices of
+// every tile (whole accumulation chunks), whose fp32 partial sums the last
+// slice of a tile to arrive adds up in slice order before writing C.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -72,6 +77,54 @@ __device__ __forceinline__ void tmem_wait_regs32(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
+}
+
+// Partial sums of one K slice for one epilogue warp: [32 column quads][32
+// rows] of float4, so a warp's stores and loads are contiguous.
+constexpr long long kSliceF4 = (kCols / 4) * 32;
+constexpr int kSumQuads = 16;   // column quads the finisher sums at a time
+
+// One K slice of a tile, for one epilogue warp (32 rows x 128 columns of its
+// CTA's half of the tile, the row sums in `acc`): publishes the slice's
+// partial sums and counts it in.  Returns true (warp-uniform) in the slice
+// that arrives last, which then owns the tile's sum: `part` points at slice
+// 0 of this warp's partial sums, the slices following at kSliceF4 apart; the
+// finisher adds them in slice order, so the result does not depend on which
+// slice finishes.  The finisher also clears the counter, so the next launch
+// starts from zero whatever its epoch.
+__device__ __forceinline__ bool publish_slice(const Tf32Args& p, int u, int rank, int ew, int lane,
+                                              const float (&acc)[kCols], const float4*& part) {
+  const int tile = u / p.splits, slice = u - tile * p.splits;
+  const long long slot = (static_cast<long long>(tile) * 2 + rank) * kEpiWarps + ew;
+  unsigned long long* const cnt = p.counters + slot;
+  float4* const mine = p.part_ws + (slot * p.splits + slice) * kSliceF4 + lane;
+#pragma unroll
+  for (int g = 0; g < kCols / 4; ++g)
+    __stcg(mine + g * 32, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
+  __threadfence();
+  __syncwarp();
+  uint32_t arrived = 0;
+  if (lane == 0) {
+    unsigned long long cv = *reinterpret_cast<volatile unsigned long long*>(cnt);
+    for (;;) {
+      const unsigned long long next =
+          (static_cast<unsigned int>(cv >> 32) == p.epoch)
+              ? cv + 1ull
+              : ((static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
+      const unsigned long long prev = atomicCAS(cnt, cv, next);
+      if (prev == cv) {
+        arrived = static_cast<uint32_t>(next & 0xFFFFFFFFull);
+        break;
+      }
+      cv = prev;
+    }
+  }
+  arrived = __shfl_sync(0xffffffffu, arrived, 0);
+  if (arrived != static_cast<uint32_t>(p.splits)) return false;
+  __threadfence();
+  if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(cnt) = 0ull;
+  part = p.part_ws + slot * p.splits * kSliceF4 + lane;
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -135,11 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const unsigned long long limit = p.wait_limit_ns;
   DeviceStatus* const st = p.status;
 
-  // unit -> (m0 of this CTA, n0, columns); groups of group_m tile-rows share B
-  // in L2; units past dp_tiles are the two column halves of a tile
-  auto tile_of = [&](int u, int& m0, int& n0, int& ncols) {
+  // unit -> (m0 of this CTA, n0, columns, k-block range); groups of group_m
+  // tile-rows share B in L2; units past dp_tiles are the two column halves of
+  // a tile; with K slices a unit is one slice of a whole tile
+  auto tile_of = [&](int u, int& m0, int& n0, int& ncols, int& kb0, int& kb1) {
     int tile = u, half = -1;
-    if (u >= p.dp_tiles) {
+    kb0 = 0;
+    kb1 = p.kb_total;
+    if (p.splits > 1) {
+      tile = u / p.splits;
+      kb0 = (u - tile * p.splits) * p.kb_per_split;
+      kb1 = min(kb0 + p.kb_per_split, p.kb_total);
+    } else if (u >= p.dp_tiles) {
       tile = p.dp_tiles + ((u - p.dp_tiles) >> 1);
       half = (u - p.dp_tiles) & 1;
     }
@@ -160,14 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int u = worker; ok && u < p.num_units; u += nworkers) {
-        int m0, n0, ncols;
-        tile_of(u, m0, n0, ncols);
+        int m0, n0, ncols, kb0, kb1;
+        tile_of(u, m0, n0, ncols, kb0, kb1);
         // B rows (columns of B) this CTA stages: half of the unit's
         const int bcols = ncols / 2;
         const uint32_t bytes = static_cast<uint32_t>(2 * kATile + 2 * bcols * BK * 4);
         const CUtensorMap* mb = bcols == kBCols ? &tmBb : &tmBbh;
         const CUtensorMap* ms = bcols == kBCols ? &tmBs : &tmBsh;
-        for (int kb = 0; kb < p.kb_total; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_parity(empty_bar(s), phase ^ 1u, limit, st, 21)) {
             ok = false;
             break;
@@ -204,8 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, chunk = 0;
       bool ok = true;
       for (int u = worker; ok && u < p.num_units; u += nworkers) {
-        const uint32_t idesc = u < p.dp_tiles ? idesc_full : idesc_half;
-        for (int kc = 0; ok && kc < p.kb_total; kc += kChunkKb, ++chunk) {
+        int m0, n0, ncols, kb0, kb1;
+        tile_of(u, m0, n0, ncols, kb0, kb1);
+        const uint32_t idesc = ncols == BN ? idesc_full : idesc_half;
+        for (int kc = kb0; ok && kc < kb1; kc += kChunkKb, ++chunk) {
           const uint32_t buf = chunk & 1u, use = chunk >> 1;
           if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 23)) {
             ok = false;
@@ -213,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + buf * BN;
-          const int kend = min(kc + kChunkKb, p.kb_total);
+          const int kend = min(kc + kChunkKb, kb1);
           for (int kb = kc; kb < kend; ++kb) {
             if (!wait_parity(full_bar(s), phase, limit, st, 24)) {
               ok = false;
@@ -265,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t chunk = 0;
     bool ok = true;
     for (int u = worker; ok && u < p.num_units; u += nworkers) {
-      int m0, n0, ncols;
-      tile_of(u, m0, n0, ncols);
+      int m0, n0, ncols, kb0, kb1;
+      tile_of(u, m0, n0, ncols, kb0, kb1);
       const int wcols = ncols / 2;   // this warp's columns of the unit
       const int row0 = m0 + 32 * q;
       const int row = row0 + lane;
@@ -275,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
-      for (int kc = 0; kc < p.kb_total; kc += kChunkKb, ++chunk) {
+      for (int kc = kb0; kc < kb1; kc += kChunkKb, ++chunk) {
         const uint32_t buf = chunk & 1u, use = chunk >> 1;
         if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 28)) {
           ok = false;
@@ -299,13 +361,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(buf), 0));
       }
-      if (!ok || !active || row >= p.M) continue;
-      float* crow = p.C + static_cast<long long>(row) * p.ldc;
-#pragma unroll
-      for (int g = 0; g < kCols / 4; ++g) {
+      if (!ok || !active) continue;
+      float* const crow = p.C + static_cast<long long>(row) * p.ldc;
+      // C[row][colw + 4g ..] := alpha * v + beta * C (columns past N and rows
+      // past M are not written)
+      auto store_quad = [&](int g, float4 v) {
         const int col = colw + 4 * g;
-        if (4 * g >= wcols || col >= p.N) break;
-        float o[4] = {acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]};
+        if (row >= p.M || 4 * g >= wcols || col >= p.N) return;
+        float o[4] = {v.x, v.y, v.z, v.w};
         if (p.vec_c && col + 4 <= p.N) {
           float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
           if (has_c) c = __ldcs(reinterpret_cast<const float4*>(crow + col));
@@ -318,10 +381,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             if (col + j < p.N)
-              crow[col + j] =
-                  has_c ? fmaf(p.alpha, o[j], p.beta * crow[col + j]) : p.alpha * o[j];
+              crow[col + j] = has_c ? fmaf(p.alpha, o[j], p.beta * crow[col + j]) : p.alpha * o[j];
         }
+      };
+      if (p.splits > 1) {
+        // K slices: publish; the last slice of the tile to arrive adds all
+        // slices up in slice order, kSumQuads column quads at a time (as many
+        // loads in flight per slice), and writes C from the sums
+        const float4* part = nullptr;
+        if (!publish_slice(p, u, static_cast<int>(rank), ew, lane, acc, part)) continue;
+#pragma unroll
+        for (int gb = 0; gb < kCols / 4 / kSumQuads; ++gb) {
+          float4 sum[kSumQuads];
+#pragma unroll
+          for (int i = 0; i < kSumQuads; ++i) sum[i] = __ldcg(part + (kSumQuads * gb + i) * 32);
+          for (int s2 = 1; s2 < p.splits; ++s2) {
+            float4 v[kSumQuads];
+#pragma unroll
+            for (int i = 0; i < kSumQuads; ++i)
+              v[i] = __ldcg(part + s2 * kSliceF4 + (kSumQuads * gb + i) * 32);
+#pragma unroll
+            for (int i = 0; i < kSumQuads; ++i) {
+              sum[i].x += v[i].x;
+              sum[i].y += v[i].y;
+              sum[i].z += v[i].z;
+              sum[i].w += v[i].w;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kSumQuads; ++i) store_quad(kSumQuads * gb + i, sum[i]);
+        }
+        continue;
       }
+#pragma unroll
+      for (int g = 0; g < kCols / 4; ++g)
+        store_quad(g, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
     }
     tc_fence_before();
     __syncwarp();

@@ -166,3 +166,64 @@ def test_fp32_extreme_dimensions(M, N, K):
     A, B, C0 = operands(4242 + M + K, M, N, K, K, N, N, np.float32)
     got, _ = run("f32", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+
+
+# ---------------------------------------------------------------- 3xTF32 K slices (few tiles)
+KSPLIT = "f32.3xtf32.pair.ksplit"
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 1100, 4000), (256, 256, 2048), (513, 1025, 4100),
+                                   (300, 300, 8200)])
+def test_3xtf32_k_slices(M, N, K):
+    """Few pair tiles and a long K: every tile is cut into K slices whose fp32
+    partial sums the last slice to finish adds up.  Exact on integers; within
+    the fp32 bound of the oracle and of whole-K units; bit-identical run to
+    run."""
+    rng = np.random.default_rng(M + 3 * K)
+    A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N)
+    assert taken == KSPLIT, taken
+    assert np.array_equal(got.astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0))
+    A, B, C0 = operands(606 + M + K, M, N, K, K, N, N, np.float32)
+    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    again, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    assert np.array_equal(got, again)
+    check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, splits=1)
+    assert not t2.endswith(".ksplit"), t2
+    bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
+    assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7, 16])
+def test_3xtf32_forced_slice_counts(splits):
+    """Any slice count (slices are whole 4-k-block chunks; a count that would
+    leave a slice empty is reduced): parity with the oracle, NaN-filled C with
+    beta = 0 never read."""
+    M, N, K = 700, 900, 1500
+    A, B, C0 = operands(707 + splits, M, N, K, K, N, N, np.float32, c_fill="nan")
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, splits=splits)
+    assert taken == KSPLIT, taken
+    check("f32", got, A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+
+
+def test_3xtf32_k_slices_padded_ldc():
+    """Sliced tiles with ldc > N: the padding of C stays untouched."""
+    M, N, K, ldc = 600, 700, 2000, 712
+    A, B, C0 = operands(808, M, N, K, K, N, ldc, np.float32)
+    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc)
+    assert taken == KSPLIT, taken
+    check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc)
+    assert padding_untouched(got, C0, N)
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (256, 256, 256), (1000, 1100, 900)])
+def test_3xtf32_short_k_keeps_whole_units(M, N, K):
+    """Few tiles with a short K: slicing would cost more in its fix-up than it
+    saves, so the tiles run as whole-K half-width units."""
+    A, B, C0 = operands(909 + K, M, N, K, K, N, N, np.float32)
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    assert taken == "f32.3xtf32.pair.halves", taken
+    check("f32", got, A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
