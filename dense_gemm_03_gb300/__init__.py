@@ -32,7 +32,7 @@ EXPORTS = (
     "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
     "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
     "gemm_f16_splitk_noalloc", "gemm_launch_count", "gemm_plan_stream_k", "gemm_f16_f32out",
-    "gemm_f32_to_f16", "gemm_debug_wait_probe",
+    "gemm_f32_to_f16", "gemm_debug_wait_probe", "gemm_plan_tf32_slices",
 )
 
 PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
@@ -90,6 +90,9 @@ def lib():
             L.gemm_plan_stream_k.restype = i
             L.gemm_plan_stream_k.argtypes = [ctypes.c_longlong, ctypes.c_longlong, i, i,
                                              ctypes.POINTER(ctypes.c_longlong)]
+            L.gemm_plan_tf32_slices.restype = i
+            L.gemm_plan_tf32_slices.argtypes = [ctypes.c_longlong, ctypes.c_longlong, i, i,
+                                                ctypes.POINTER(ctypes.c_longlong)]
             L.gemm_launch_count.restype = ctypes.c_longlong
             L.gemm_launch_count.argtypes = []
             L.gemm_last_path.restype = ctypes.c_char_p
@@ -278,6 +281,14 @@ def plan_stream_k(tiles: int, slots: int, kb: int, all_tiles: bool = False) -> d
     out = (ctypes.c_longlong * 4)()
     _check(lib().gemm_plan_stream_k(tiles, slots, kb, int(bool(all_tiles)), out), "gemm_plan_stream_k")
     return {"dp_tiles": out[0], "sk_tiles": out[1], "workers": out[2], "max_pieces": out[3]}
+
+
+def plan_tf32_slices(tiles: int, pairs: int, kb: int, forced_slices: int = 0) -> dict:
+    """The K-slice plan of the fp32 tensor-core path (host-side query)."""
+    out = (ctypes.c_longlong * 2)()
+    _check(lib().gemm_plan_tf32_slices(tiles, pairs, kb, forced_slices, out),
+           "gemm_plan_tf32_slices")
+    return {"splits": out[0], "kb_per_split": out[1]}
 
 
 def debug_wait_probe(limit_ns: int, stream=None):

@@ -213,6 +213,16 @@ TailSplit plan_tf32_slices(int kb_total, int cap, bool forced) {
   return best;
 }
 
+// The K-slice plan of the fp32 tensor-core path: slices only when the tiles
+// fill at most half the pairs and K has at least two chunks; `fs` > 1 forces
+// that many slices (fs == 1: none).
+TailSplit tf32_slice_plan(long long tiles, long long pairs, int kb_total, int fs) {
+  if (fs == 1 || tiles <= 0 || 2 * tiles > pairs || kb_total < 8) return TailSplit{};
+  const long long fit = pairs / tiles;
+  const int cap = static_cast<int>(std::min<long long>({fs > 1 ? fs : fit, kb_total / 4, 16}));
+  return plan_tf32_slices(kb_total, cap, fs > 1);
+}
+
 // Tail plan for `tiles` whole tiles on `ctas` persistent CTAs: the number of K
 // slices (1 = none) that minimises the number of tile-times, counting a tile
 // cut into s slices as 1/s of a tile-time per slice plus a small fix-up cost.
@@ -723,9 +733,8 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       // gemm_force_splits: 1 keeps whole-K units, > 1 sets the slice count.
       const int fs = g_force_splits.load();
       int splits = 1;
-      if (force != 5 && fs != 1 && 2 * tiles <= pairs && t.kb_total >= 8) {
-        const int cap = std::min({fs > 1 ? fs : pairs / tiles, t.kb_total / 4, 16});
-        const TailSplit ts = plan_tf32_slices(t.kb_total, cap, fs > 1);
+      if (force != 5) {
+        const TailSplit ts = tf32_slice_plan(tiles, pairs, t.kb_total, fs);
         if (ts.splits > 1) {
           splits = ts.splits;
           t.kb_per_split = ts.kb_per_split;
@@ -1002,6 +1011,16 @@ int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, 
   out[1] = p.sk_tiles;
   out[2] = p.workers;
   out[3] = p.max_pieces;
+  return GEMM_OK;
+}
+
+int gemm_plan_tf32_slices(long long tiles, long long pairs, int kb, int forced_slices,
+                          long long* out) {
+  if (out == nullptr) return GEMM_ERR_NULL;
+  if (tiles < 0 || pairs < 0 || kb < 0 || forced_slices < 0) return GEMM_ERR_ARG;
+  const TailSplit ts = tf32_slice_plan(tiles, pairs, kb, forced_slices);
+  out[0] = ts.splits;
+  out[1] = ts.splits > 1 ? ts.kb_per_split : kb;
   return GEMM_OK;
 }
 

@@ -204,8 +204,10 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  */
 int gemm_force_path(int path);
 
-/* Fixes the split count of the split-K path (0 = automatic).  Returns the
- * previous value. */
+/* Fixes the split count of the split-K path (0 = automatic).  On the fp32
+ * tensor-core path it also sets the K slices of few-tile shapes: 1 keeps
+ * whole-K units, > 1 asks for that many slices (fewer when a slice would be
+ * empty).  Process wide; returns the previous value. */
 int gemm_force_splits(int splits);
 
 /* Limit, in nanoseconds, of every wait inside the kernels (0 = default of
@@ -243,6 +245,18 @@ const char* gemm_last_path(void);
  * (no device call); returns GEMM_OK, or GEMM_ERR_NULL for a null `out`.
  */
 int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, long long* out);
+
+/*
+ * The K-slice plan of the fp32 tensor-core path for `tiles` 256x256 output
+ * tiles of `kb` 32-deep k-blocks on `pairs` concurrent CTA pairs, as the
+ * automatic choice makes it (`forced_slices` > 1 plays gemm_force_splits).
+ * Writes out[0] = slices per tile (1 = whole-K units, no slicing) and
+ * out[1] = k-blocks per slice (a multiple of 4; the last slice may be
+ * shorter).  Host-only; returns GEMM_OK, GEMM_ERR_NULL for a null `out`, or
+ * GEMM_ERR_ARG for a negative argument.
+ */
+int gemm_plan_tf32_slices(long long tiles, long long pairs, int kb, int forced_slices,
+                          long long* out);
 
 /* Number of kernels the library has launched in this process (all threads,
  * all devices; launches that failed are not counted).  Nothing else --
