@@ -40,8 +40,9 @@
  *              stream) and the call returns without synchronising.  Calls on
  *              different streams that write the same C race.
  *   Scratch    some shapes split K over several thread blocks and need an
- *              fp32 workspace (few tiles with a long K: stream-K; the forced
- *              split paths); unaligned half operands need an aligned copy;
+ *              fp32 workspace (few tiles with a long K: stream-K for half
+ *              operands, K slices for fp32 ones; the forced split paths);
+ *              unaligned half operands need an aligned copy;
  *              the fp32 path keeps its tf32 operand parts.  The library owns
  *              this scratch, per device and stream, grows it on first need
  *              (that call may allocate device memory) and frees it in
@@ -119,8 +120,10 @@ int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t s
  * result.  Shapes of at least 256 x 256 x 64 run on the tensor cores as three
  * tf32 products of split operands (A = Ab + As, B = Bb + Bs; the As*Bs term,
  * about 2^-22 of |A||B|, is dropped) with fp32 accumulation, after a pre-pass
- * that writes the split operands to library-owned scratch; smaller shapes use
- * an FFMA kernel (exact fp32 products). */
+ * that writes the split operands to library-owned scratch (few output tiles
+ * with a long K: every tile cut into K slices whose fp32 partial sums are
+ * added in slice order, so results are reproducible run to run); smaller
+ * shapes use an FFMA kernel (exact fp32 products). */
 int sgemm_f32(const float* A, const float* B, float* C,
               int M, int N, int K, float alpha, float beta, cudaStream_t stream);
 
