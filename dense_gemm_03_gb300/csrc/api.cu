@@ -190,15 +190,16 @@ int stream_scratch(DevState* d, cudaStream_t stream, size_t bytes, size_t counte
 // with the least estimated time, or 1 when whole-K half-width units are
 // expected to be faster.  Estimates measured on GB300: a whole-K half-width
 // unit runs ~0.6 us per k-block, a full-width slice ~0.75 us, and publishing
-// plus adding up S slices' partial sums costs ~8 + 1.5 S us.  `forced` takes
-// the largest count up to `cap` whatever the estimate.
+// plus adding up S slices' partial sums costs ~8 + 1.5 S us; slices must be
+// estimated at least 10% faster.  `forced` takes the largest count up to
+// `cap` whatever the estimate.
 struct TailSplit {
   int splits = 1;
   int kb_per_split = 0;
 };
 TailSplit plan_tf32_slices(int kb_total, int cap, bool forced) {
   TailSplit best;
-  double best_us = 0.6 * kb_total;
+  double best_us = 0.9 * 0.6 * kb_total;
   for (int want = 2; want <= cap; ++want) {
     const int per = ((kb_total + want - 1) / want + 3) / 4 * 4;
     const int s = (kb_total + per - 1) / per;   // no empty slice
