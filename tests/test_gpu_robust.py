@@ -20,14 +20,14 @@ def _built():
 
 
 def test_concurrent_threads_own_streams():
-    """Four threads, each on its own stream, repeatedly run shapes whose tiles
-    are shared out (stream-K, half-width units, 3xTF32); every result checks
-    against the oracle."""
+    """Five threads, each on its own stream, repeatedly run shapes whose tiles
+    are shared out (stream-K, half-width units, 3xTF32 whole-K and K slices);
+    every result checks against the oracle."""
     import dense_gemm_03_gb300 as g
     t = torch()
     cases = [
         ("f16", 16, 8192, 8192), ("f16", 2000, 2600, 1024), ("f32", 700, 900, 500),
-        ("f16", 1000, 1001, 4096),
+        ("f16", 1000, 1001, 4096), ("f32", 600, 700, 2000),
     ]
     prepared = []
     for i, (kind, M, N, K) in enumerate(cases):
