@@ -341,9 +341,12 @@ int make_map_f32(CUtensorMap* map, const void* ptr, int rows, int cols, long lon
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-int scale_grid(const DevState& d, long long elems) {
+// Blocks of 256 threads for `elems` work items, at most `per_sm` blocks per SM
+// (grid-stride kernels loop over the rest).
+int scale_grid(const DevState& d, long long elems, int per_sm = 8) {
   const long long blocks = (elems + 255) / 256;
-  return static_cast<int>(std::max(1ll, std::min<long long>(blocks, 8ll * d.sm_count)));
+  return static_cast<int>(
+      std::max(1ll, std::min<long long>(blocks, static_cast<long long>(per_sm) * d.sm_count)));
 }
 
 // [bn index][load][epilogue: TMA, predicated, fp32 partial sums (split-K)]
@@ -919,7 +922,9 @@ int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t s
   DevState* d = nullptr;
   if (int rc = device_state(&d, nullptr)) return rc;
   t_last_path = "f32_to_f16";
-  return launch_f32_to_f16(src, dst, n, scale_grid(*d, (n + 7) / 8), stream) == cudaSuccess
+  // up to 64 blocks per SM: about one step per thread, so the block scheduler
+  // balances the SMs (22.5 -> 20.5 us for 4096 x 4096 against 8 per SM)
+  return launch_f32_to_f16(src, dst, n, scale_grid(*d, (n + 7) / 8, 64), stream) == cudaSuccess
              ? GEMM_OK
              : GEMM_ERR_CUDA;
 }
