@@ -458,6 +458,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   int epi = c_f32 ? kEpiF32 : ((c_tma && force != 2) ? kEpiTma : kEpiManual);
 
   TcArgs a{};
+  a.pdl = *how != '\0';   // the realignment copy was launched just before
   a.A = A;
   a.B = B;
   a.C = c_f32 ? nullptr : static_cast<uint16_t*>(C);
@@ -714,6 +715,7 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       if (int rc = make_map_f32(&mBbh, Bb, N, K, K2, 32, 64)) return rc;
       if (int rc = make_map_f32(&mBsh, Bs, N, K, K2, 32, 64)) return rc;
       Tf32Args t{};
+      t.pdl = true;   // the split pre-pass was launched just before
       t.Ab = Ab;
       t.As = As;
       t.Bb = Bb;

@@ -145,6 +145,9 @@ __global__ void realign_f16_kernel(const uint16_t* __restrict__ src1, long long 
     realign_rows(src1, lds1, dst1, ldd1, rows1, cols1, blockIdx.x, grid_1);
   else
     realign_rows(src2, lds2, dst2, ldd2, rows2, cols2, blockIdx.x - grid_1, gridDim.x - grid_1);
+  // this block's copies are issued: the GEMM launched next may be scheduled
+  // (it waits for this kernel's completion before reading the copies)
+  griddep_launch_dependents();
 }
 
 // tf32 value nearest to x (ties away from zero), as fp32 bits with the low 13
@@ -264,6 +267,8 @@ __global__ void split_tf32_ab_kernel(const float* __restrict__ A, long long lda,
     split_rows(A, lda, Ab, As, ld2, M, K, blockIdx.x, grid_a);
   else
     split_transpose(B, ldb, Bb, Bs, ld2, K, N, blockIdx.x - grid_a, gridDim.x - grid_a, tile);
+  // as for the realignment: the GEMM launched next may be scheduled
+  griddep_launch_dependents();
 }
 
 // dst[i] = src[i] rounded to the nearest half (ties to even), eight elements

@@ -475,6 +475,10 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   else
     __syncthreads();
   tc_fence_after();
+  // everything above touched only this CTA's shared and tensor memory; from
+  // here on global memory is read and written, once a pre-pass launched just
+  // before this kernel has completed
+  griddep_wait();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::kTmemPtrOff);
 
   const unsigned long long limit = p.wait_limit_ns;
@@ -1074,15 +1078,22 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   cfg.blockDim = dim3(Roles<LOAD>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned int nattr = 0;
   if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
   }
+  if (args.pdl) {
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
+  cfg.attrs = nattr ? attr : nullptr;
+  cfg.numAttrs = nattr;
   e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM>, tmA, tmB, tmC, args);
   if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());

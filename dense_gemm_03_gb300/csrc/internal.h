@@ -72,6 +72,10 @@ struct TcArgs {
   int tail_halves;
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
+  // host only: the launch directly follows this call's pre-pass kernel on the
+  // same stream, so it may start early (programmatic dependent launch; the
+  // kernel waits for the pre-pass before touching global memory)
+  bool pdl;
 };
 
 // Tensor-core fp16 GEMM (tcgen05).  Maps are ignored by the modes that do not
@@ -172,6 +176,7 @@ struct Tf32Args {
   float4* part_ws;                  // [tile][rank][warp][slice][32 column quads][32 rows]
   unsigned long long* counters;     // [tile][rank][warp]: (epoch << 32) | arrivals
   unsigned int epoch;
+  bool pdl;                         // host only: as TcArgs::pdl (after the split pre-pass)
 };
 // tmBbh / tmBsh: the B parts with 64-row boxes, for the half-width units.
 cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,

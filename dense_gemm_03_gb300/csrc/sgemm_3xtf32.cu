@@ -184,6 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   cluster_sync();
   tc_fence_after();
+  // global memory (the split operand parts, C) only after the split pre-pass,
+  // which may still run when this kernel starts, has completed
+  griddep_wait();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + kTmemPtrOff);
   const unsigned long long limit = p.wait_limit_ns;
   DeviceStatus* const st = p.status;
@@ -475,8 +478,13 @@ cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = configure(dev)) != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
+  if (args.pdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, tmAb, tmAs, tmBb, tmBs, tmBbh, tmBsh, args);
   if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());
