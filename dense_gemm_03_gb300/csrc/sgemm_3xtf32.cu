@@ -19,9 +19,10 @@
 // with M = 256 (128 rows of A in each CTA) and N = 256 (each CTA stages 128 of
 // the columns of B); per 32-deep k-block each CTA stages Ab, As (128 x 32) and
 // Bb, Bs (128 columns x 32) by TMA into a 3-stage ring (64 KB per stage), and
-// the leader issues 3 MMAs per 8-deep K step.  Warp roles, barriers and the
-// epilogue (8 warps, fp32 written straight from registers) follow the fp16
-// tensor-core kernel.  Both operands are K-major (the pre-pass stores the B
+// the leader issues 3 MMAs per 8-deep K step.  Warp roles and barriers follow
+// the fp16 tensor-core kernel; the 8 epilogue warps keep fp32 row sums in
+// registers and write C through a small shared-memory tile each, so that
+// stores cover whole 64-byte row pieces.  Both operands are K-major (the pre-pass stores the B
 // parts transposed): 128-byte swizzle, 32 floats per row, SBO 1024 B.
 //
 // Units: whole 256 x 256 tiles; the tiles of a last, partial wave as two
@@ -51,7 +52,11 @@ constexpr int kTmemCols = 2 * BN;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1;   // full, empty, accf, acce, done, tmem_free
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
-constexpr int kSmemAlloc = kTmemPtrOff + 16 + 1024;
+// per epilogue warp a 32-row x 16-float staging tile that turns the row-owned
+// sums into row-contiguous stores of C
+constexpr int kEpiOff = (kTmemPtrOff + 16 + 127) / 128 * 128;
+constexpr int kEpiTileF4 = 32 * 4;
+constexpr int kSmemAlloc = kEpiOff + kEpiWarps * kEpiTileF4 * 16 + 1024;
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
@@ -368,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* const crow = p.C + static_cast<long long>(row) * p.ldc;
       // C[row][colw + 4g ..] := alpha * v + beta * C (columns past N and rows
       // past M are not written)
+      float4* const tile = reinterpret_cast<float4*>(base_ptr + kEpiOff) + ew * kEpiTileF4;
       auto store_quad = [&](int g, float4 v) {
         const int col = colw + 4 * g;
         if (row >= p.M || 4 * g >= wcols || col >= p.N) return;
@@ -386,6 +392,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col + j < p.N)
               crow[col + j] = has_c ? fmaf(p.alpha, o[j], p.beta * crow[col + j]) : p.alpha * o[j];
         }
+      };
+      // Columns colw + 16j .. +15 (quads 4j .. 4j+3) through the staging tile:
+      // lane r writes its row's four quads (slot q ^ ((r >> 1) & 3): eight
+      // lanes fill 128 distinct bytes), then every store instruction covers 8
+      // rows x 64 contiguous bytes of C.  Groups that cross N, or a C that
+      // breaks the 16-byte rule, are written row by row.  Warp-uniform.
+      auto store_group = [&](int j, const float4 (&v)[4]) {
+        const int col0 = colw + 16 * j;
+        if (16 * j >= wcols || col0 >= p.N) return;
+        if (!p.vec_c || col0 + 16 > p.N) {
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) store_quad(4 * j + q2, v[q2]);
+          return;
+        }
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) tile[lane * 4 + (q2 ^ sw)] = v[q2];
+        __syncwarp();
+        const int rq = lane & 3;
+        float* const cq = p.C + static_cast<long long>(row0 + (lane >> 2)) * p.ldc + col0 + 4 * rq;
+        const long long row8 = 8 * p.ldc;   // eight rows further
+        float4 val[4], cv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 8 * i + (lane >> 2);
+          val[i] = tile[r * 4 + (rq ^ ((r >> 1) & 3))];
+          cv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (has_c && row0 + r < p.M) cv[i] = __ldcs(reinterpret_cast<const float4*>(cq + i * row8));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (row0 + 8 * i + (lane >> 2) >= p.M) continue;
+          const float4 o =
+              has_c ? make_float4(fmaf(p.alpha, val[i].x, p.beta * cv[i].x),
+                                  fmaf(p.alpha, val[i].y, p.beta * cv[i].y),
+                                  fmaf(p.alpha, val[i].z, p.beta * cv[i].z),
+                                  fmaf(p.alpha, val[i].w, p.beta * cv[i].w))
+                    : make_float4(p.alpha * val[i].x, p.alpha * val[i].y, p.alpha * val[i].z,
+                                  p.alpha * val[i].w);
+          __stcs(reinterpret_cast<float4*>(cq + i * row8), o);
+        }
+        __syncwarp();
       };
       if (p.splits > 1) {
         // K slices: publish; the last slice of the tile to arrive adds all
@@ -412,13 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #pragma unroll
-          for (int i = 0; i < kSumQuads; ++i) store_quad(kSumQuads * gb + i, sum[i]);
+          for (int jj = 0; jj < kSumQuads / 4; ++jj) {
+            const float4 v4[4] = {sum[4 * jj], sum[4 * jj + 1], sum[4 * jj + 2], sum[4 * jj + 3]};
+            store_group(kSumQuads / 4 * gb + jj, v4);
+          }
         }
         continue;
       }
 #pragma unroll
-      for (int g = 0; g < kCols / 4; ++g)
-        store_quad(g, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
+      for (int j = 0; j < kCols / 16; ++j) {
+        float4 v4[4];
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const int g = 4 * j + q2;
+          v4[q2] = make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+        }
+        store_group(j, v4);
+      }
     }
     tc_fence_before();
     __syncwarp();
