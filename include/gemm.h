@@ -117,13 +117,13 @@ int gemm_f16_f32out(const uint16_t* A, const uint16_t* B, float* C,
 int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t stream);
 
 /* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 operands and
- * result.  Shapes of at least 256 x 256 x 64 run on the tensor cores as three
+ * result.  Shapes with K >= 64 run on the tensor cores as three
  * tf32 products of split operands (A = Ab + As, B = Bb + Bs; the As*Bs term,
  * about 2^-22 of |A||B|, is dropped) with fp32 accumulation, after a pre-pass
  * that writes the split operands to library-owned scratch (few output tiles
  * with a long K: every tile cut into K slices whose fp32 partial sums are
- * added in slice order, so results are reproducible run to run); smaller
- * shapes use an FFMA kernel (exact fp32 products). */
+ * added in slice order, so results are reproducible run to run); a shorter K
+ * uses an FFMA kernel (exact fp32 products). */
 int sgemm_f32(const float* A, const float* B, float* C,
               int M, int N, int K, float alpha, float beta, cudaStream_t stream);
 

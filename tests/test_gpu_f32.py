@@ -50,10 +50,16 @@ def test_random_parity(path, M, N, K, alpha, beta, c_fill):
     (130, 190, 100, 101, 193, 191),
 ])
 def test_leading_dimensions(M, N, K, lda, ldb, ldc):
+    """Leading dimensions on the FFMA kernel (vector or scalar accesses) and on
+    the automatic 3xTF32 path, whose split pre-pass reads any stride."""
     A, B, C0 = operands(17 + lda, M, N, K, lda, ldb, ldc, np.float32)
-    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
+    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc, path=FFMA_ONLY)
     vec = lda % 4 == 0 and ldb % 4 == 0 and ldc % 4 == 0
     assert taken == ("f32.ffma.vec" if vec else "f32.ffma.scalar")
+    check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
+    assert padding_untouched(got, C0, N)
+    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
+    assert taken.startswith("f32.3xtf32.pair"), taken
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
     assert padding_untouched(got, C0, N)
 
@@ -227,3 +233,16 @@ def test_3xtf32_short_k_keeps_whole_units(M, N, K):
     got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
     assert taken == "f32.3xtf32.pair.halves", taken
     check("f32", got, A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+
+
+@pytest.mark.parametrize("M,N,K,expect", [
+    (16, 8192, 1024, "f32.3xtf32"), (1, 4096, 512, "f32.3xtf32"), (200, 200, 200, "f32.3xtf32"),
+    (16, 16, 4096, "f32.3xtf32"), (1024, 1024, 16, "f32.ffma"), (300, 260, 1, "f32.ffma"),
+])
+def test_fp32_path_choice_small_and_skinny(M, N, K, expect):
+    """K >= 64 takes the tensor cores whatever M and N (skinny and tiny shapes
+    included); a shorter K takes the FFMA kernel.  Parity either way."""
+    A, B, C0 = operands(3030 + M + K, M, N, K, K, N, N, np.float32)
+    got, taken = run("f32", A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
+    assert taken.startswith(expect), taken
+    check("f32", got, A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
