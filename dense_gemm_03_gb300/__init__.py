@@ -225,6 +225,7 @@ def gemm_f16_host(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None
 
 def sgemm_f32_host(A, B, C, alpha=1.0, beta=0.0, M=None, N=None, K=None, lda=None, ldb=None,
                    ldc=None, stream=None):
+    """Host-buffer fp32 form: copies in, computes, copies C back, synchronises."""
     M, N, K = _dims(A, B, M, N, K)
     rc = lib().sgemm_f32_host(_addr(A), _addr(B), _addr(C), M, N, K,
                               int(K if lda is None else lda), int(N if ldb is None else ldb),

@@ -246,3 +246,23 @@ def test_fp32_path_choice_small_and_skinny(M, N, K, expect):
     got, taken = run("f32", A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
     assert taken.startswith(expect), taken
     check("f32", got, A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
+
+
+@pytest.mark.parametrize("M,N,K,ldc", [(700, 900, 500, 900), (2600, 1000, 700, 1004)])
+def test_fp32_host_form(M, N, K, ldc):
+    """sgemm_f32_host: pinned host operands copied in, computed (in four row
+    blocks when M >= 2048, each block with its own split pre-pass) and copied
+    back; parity with the oracle and C's padding unchanged."""
+    import dense_gemm_03_gb300 as g
+    from helpers import torch
+    t = torch()
+    A, B, C0 = operands(4400 + M, M, N, K, K, N, ldc, np.float32)
+    hA = t.from_numpy(A).pin_memory()
+    hB = t.from_numpy(B).pin_memory()
+    hC = t.from_numpy(C0.copy()).pin_memory()
+    g.sgemm_f32_host(hA, hB, hC, 0.75, -0.25, M=M, N=N, K=K, ldc=ldc)
+    got = hC.numpy()
+    check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc,
+          rows=oracle.sample_rows(M, block=64) if M >= 2048 else None)
+    assert padding_untouched(got, C0, N)
+    assert g.debug_status() == 0
