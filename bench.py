@@ -297,6 +297,7 @@ def run_ours(args, rank, world):
 
     # the other workloads of the metric, timed the same way (context for the headline)
     shapes = []
+    squares = []
     if not args.no_shapes:
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         for (sM, sN, sK, slda, alpha, beta, name) in EDGE_SHAPES:
@@ -316,6 +317,22 @@ def run_ours(args, rank, world):
                            "gb_s": round(gbs, 1), "frac_tensor": round(tf / peak16_local, 3),
                            "frac_hbm": round(gbs / hbm, 3), "kernel_path": g.last_path()})
             del eA, eB, eC
+        # the fp32 square configurations below 4096 (4096 is the fp32 leg above)
+        ceiling32 = peak16_local * (1.1 / 2.25) / 3.0
+        for n in (256, 512, 1024, 2048):
+            seed_s = synthetic.config_seed(1)
+            sA, _ = _fill_device((n, n), np.float32, seed_s, synthetic.STREAM_A)
+            sB, _ = _fill_device((n, n), np.float32, seed_s, synthetic.STREAM_B)
+            sC = torch.zeros((n, n), dtype=torch.float32, device="cuda")
+            fn = lambda: g.sgemm_f32(sA, sB, sC, 1.0, 0.0, stream=stream)
+            ms = timed_replays(fn, max(20, args.steps // 20), 5, stream, flush_bytes)
+            t = sum(ms) / len(ms)
+            tf = 2.0 * n ** 3 / (t * 1e-3) / 1e12
+            squares.append({"workload": "fp32 SGEMM %d^3, alpha=1 beta=0" % n,
+                            "us": round(t * 1e3, 2), "tflops": round(tf, 2),
+                            "frac_3xtf32_ceiling": round(tf / ceiling32, 4),
+                            "kernel_path": g.last_path()})
+            del sA, sB, sC
 
     # end to end through the host-buffer C-ABI call (copies inside the timed region)
     pA = torch.from_numpy(hA).pin_memory()
@@ -413,6 +430,7 @@ def run_ours(args, rank, world):
             "api": "gemm_f16_host (pinned host buffers)",
         },
         "edge_shapes": shapes,
+        "fp32_squares": squares,
         **extra,
         "gpu_launches": LaunchTally.total,
         "clocks": clocks,
