@@ -89,65 +89,156 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling in the background (200 ms period)."""
+    """SM clock, clock-event (throttle) reasons and power, sampled through NVML
+    (libnvidia-ml, read-only queries) every `period` seconds by a background
+    thread.  `mark(name)` / `end(name)` bracket host-time windows (a timed
+    region: from the first enqueue to the synchronise after the last replay);
+    `summary(names)` summarises the samples that fall inside those windows.
+    Without NVML it falls back to nvidia-smi at its 100 ms minimum period."""
 
-    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    IDLE_BIT = 0x1
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.out = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv", delete=False)
-
-    def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        return self
-
-    def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-        self.out.close()
-        rows = []
-        try:
-            with open(self.out.name) as f:
-                for line in f:
-                    parts = [x.strip() for x in line.split(",")]
-                    if len(parts) >= 10:
-                        rows.append(parts)
-        finally:
-            os.unlink(self.out.name)
-        return self._summary(rows)
+    def __init__(self, cuda_index: int, period: float = 0.002):
+        self.period = period
+        self.samples = []          # (t, sm_mhz, max_mhz, reasons, power_w)
+        self.windows = {}
+        self._stop = None
+        self._thread = None
+        self._smi = None
+        self.source = "none"
+        self._nvml = self._open_nvml(cuda_index)
 
     @staticmethod
-    def _summary(rows):
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
+    def _open_nvml(cuda_index):
+        import ctypes
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
                 return None
-        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
-        smax = [num(r[3]) for r in rows if num(r[3]) is not None]
-        power = [num(r[4]) for r in rows if num(r[4]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
-        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        except OSError:
+            return None
+        h = ctypes.c_void_p()
+        found = False
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(cuda_index)
+            uuid = str(getattr(props, "uuid", "") or "")
+            if uuid:
+                key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                found = L.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(h)) == 0
+            if not found and hasattr(props, "pci_bus_id"):
+                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id,
+                                            props.pci_device_id)
+                found = L.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            found = False
+        if not found and L.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+            return None
+        reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        return (L, h, reasons)
+
+    def _sample_nvml(self):
+        import ctypes
+        L, h, reasons_fn = self._nvml
+        clk, mx, pw = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_uint(0)
+        rs = ctypes.c_ulonglong(0)
+        t = time.perf_counter()
+        ok = L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0      # NVML_CLOCK_SM
+        L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        if reasons_fn is not None:
+            reasons_fn(h, ctypes.byref(rs))
+        L.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+        if ok:
+            self.samples.append((t, float(clk.value), float(mx.value), int(rs.value),
+                                 pw.value / 1000.0))
+
+    def start(self):
+        import threading
+        if self._nvml is not None:
+            self.source = "nvml, %.0f ms period" % (self.period * 1e3)
+            self._stop = threading.Event()
+
+            def loop():
+                while not self._stop.is_set():
+                    try:
+                        self._sample_nvml()
+                    except Exception:
+                        return
+                    time.sleep(self.period)
+            self._thread = threading.Thread(target=loop, daemon=True)
+            self._thread.start()
+        else:
+            self.source = "nvidia-smi, 100 ms period"
+            self._t0 = time.perf_counter()
+            self._smi_out = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv",
+                                                        delete=False)
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=timestamp,clocks.sm,clocks.max.sm,power.draw,"
+                     "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=self._smi_out, stderr=subprocess.DEVNULL)
+            except OSError:
+                self._smi = None
+        return self
+
+    def mark(self, name):
+        self.windows[name] = [time.perf_counter(), None]
+
+    def end(self, name):
+        self.windows[name][1] = time.perf_counter()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self._smi is not None:
+            self._smi.terminate()
+            try:
+                self._smi.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._smi.kill()
+            self._smi_out.close()
+            # nvidia-smi rows carry no perf_counter time: spread them evenly
+            rows = []
+            with open(self._smi_out.name) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 5:
+                        rows.append(parts)
+            os.unlink(self._smi_out.name)
+            t1 = time.perf_counter()
+            for i, r in enumerate(rows):
+                try:
+                    t = self._t0 + (t1 - self._t0) * (i + 0.5) / len(rows)
+                    self.samples.append((t, float(r[1]), float(r[2]), int(r[4], 16),
+                                         float(r[3])))
+                except ValueError:
+                    pass
+        return self
+
+    def summary(self, names=None):
+        """Samples inside the named windows (all samples when names is None)."""
+        if names is None:
+            sel = list(self.samples)
+        else:
+            wins = [self.windows[n] for n in names if n in self.windows and self.windows[n][1]]
+            sel = [x for x in self.samples if any(a <= x[0] <= b for a, b in wins)]
+        smax = max((x[2] for x in sel), default=None)
+        loaded = [x for x in sel if not (x[3] & self.IDLE_BIT) and
+                  (smax is None or x[1] > 0.5 * smax)]
+        reasons = sorted({name for x in loaded for bit, name in self.REASON_BITS.items()
+                          if x[3] & bit})
         return {
-            "sm_mhz": statistics.median(loaded) if loaded else None,
-            "sm_max_mhz": max(smax) if smax else None,
+            "sm_mhz": statistics.median([x[1] for x in loaded]) if loaded else None,
+            "sm_max_mhz": smax,
             "reasons": reasons,
-            "samples": len(rows),
-            "power_w_max": max(power) if power else None,
+            "samples": len(sel),
+            "samples_under_load": len(loaded),
+            "power_w_max": max((x[4] for x in sel), default=None),
+            "source": self.source,
         }
 
 
@@ -181,10 +272,11 @@ class LaunchTally:
     total = 0
 
 
-def timed_replays(fn, steps, warmup, stream, flush_bytes):
+def timed_replays(fn, steps, warmup, stream, flush_bytes, sampler=None, window=None):
     """W warm-up + K timed replays; L2 flush before each, one event pair per
     replay on `stream`.  Returns per-replay milliseconds; the library's
-    launches during the K timed replays are added to LaunchTally."""
+    launches during the K timed replays are added to LaunchTally.  With a
+    sampler, the timed replays form the clock window `window`."""
     import torch
     import dense_gemm_03_gb300 as g
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -195,15 +287,108 @@ def timed_replays(fn, steps, warmup, stream, flush_bytes):
             fn()
         torch.cuda.synchronize()
         n0 = g.launch_count()
+        if sampler is not None:
+            sampler.mark(window)
         for i in range(steps):
             g.l2_flush(flush_bytes, stream)
             starts[i].record(stream)
             fn()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.end(window)
         LaunchTally.last = g.launch_count() - n0
         LaunchTally.total += LaunchTally.last
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def sustained_replays(fn, seconds, stream, flush_bytes, sampler, window, batch=200):
+    """The same replays (flush, event pair, call) back to back for about
+    `seconds` of wall time, in batches; returns per-replay milliseconds."""
+    import torch
+    import dense_gemm_03_gb300 as g
+    out = []
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(batch)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(batch)]
+    n0 = g.launch_count()
+    sampler.mark(window)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t0 < seconds:
+            for i in range(batch):
+                g.l2_flush(flush_bytes, stream)
+                starts[i].record(stream)
+                fn()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            out.extend(s.elapsed_time(e) for s, e in zip(starts, ends))
+    sampler.end(window)
+    LaunchTally.total += g.launch_count() - n0
+    return out
+
+
+def measured_tf32_tflops(n=8192, reps=10):
+    """Dense tf32 rate of this GPU, measured off the library's path like the
+    bf16 figure of the peaks file: torch.matmul on fp32 operands with tf32
+    allowed (cuBLAS), n^3, best of `reps` after 3 warm-ups, CUDA events."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        gen = torch.Generator(device="cuda").manual_seed(1)
+        a = torch.randn((n, n), device="cuda", generator=gen)
+        b = torch.randn((n, n), device="cuda", generator=gen)
+        c = torch.empty((n, n), device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+# fp32 size-sweep sizes timed in the default line: every eighth size of the
+# 1024..12800 step-128 sweep, and its last one
+SWEEP_SUBSET = list(range(1024, 12800, 1024)) + [12800]
+
+
+def sweep_subset(stream, flush_bytes, sampler, sizes=SWEEP_SUBSET):
+    """The fp32 sweep's schedule (R(n) replays, L2 flushed before each,
+    second-half mean) on a subset of its sizes.  Operands: N(0,1) filled on
+    the device by a seeded torch generator (timing only; the parity tests use
+    the host generator)."""
+    import torch
+    import dense_gemm_03_gb300 as g
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    nmax = max(sizes)
+    A = torch.randn((nmax * nmax,), device="cuda", generator=gen)
+    B = torch.randn((nmax * nmax,), device="cuda", generator=gen)
+    C = torch.zeros((nmax * nmax,), device="cuda")
+    res = []
+    sampler.mark("fp32_sweep")
+    for n in sizes:
+        a, b, c = A[:n * n], B[:n * n], C[:n * n]
+        R = replay_count(n)
+        ms = timed_replays(lambda: g.sgemm_f32(a, b, c, 1.0, 0.0, M=n, N=n, K=n, stream=stream),
+                           R, 3, stream, flush_bytes)
+        t = second_half_mean(ms)
+        res.append({"n": n, "replays": R, "tflops": round(2.0 * n ** 3 / (t * 1e-3) / 1e12, 1)})
+    sampler.end("fp32_sweep")
+    del A, B, C
+    tf = [r["tflops"] for r in res]
+    return {"workload": "fp32 SGEMM m=n=k sweep subset (every 8th size of 1024..12800 step 128, "
+                        "and 12800), R(n) = 1000*exp((1024-n)/3100) replays, second-half mean",
+            "kernel_path": g.last_path(), "tflops_mean": round(sum(tf) / len(tf), 1),
+            "tflops_min": min(tf), "tflops_max": max(tf), "sizes": res}
 
 
 def run_ours(args, rank, world):
@@ -220,6 +405,8 @@ def run_ours(args, rank, world):
     l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
     flush_bytes = 2 * l2
     peaks, peaks_src = _peaks()
+    sm_count = props.multi_processor_count or SM_COUNT_NOMINAL
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
 
     # fp16 headline workload
     M, N, K = F16_CFG["M"], F16_CFG["N"], F16_CFG["K"]
@@ -242,28 +429,40 @@ def run_ours(args, rank, world):
     sampler = ClockSampler(dev).start()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    ms16 = timed_replays(f16, args.steps, args.warmup, stream, flush_bytes)
+    ms16 = timed_replays(f16, args.steps, args.warmup, stream, flush_bytes, sampler, "fp16")
     path16 = g.last_path()
     launches16 = LaunchTally.last / args.steps
-    f32_steps = max(3, args.steps // 20)
+    t_wall1 = time.perf_counter()
+    # the headline replays again, back to back for a few seconds: enough clock
+    # samples under load, and the rate once power limits have settled
+    ms16s = sustained_replays(f16, args.sustain_seconds, stream, flush_bytes, sampler,
+                              "fp16_sustained") if args.sustain_seconds > 0 else []
+    f32_steps = max(50, args.steps // 20)
     prev_path = g.force_path(PATH_FFMA_ONLY) if args.f32_ffma else None
-    ms32 = timed_replays(f32, f32_steps, max(3, args.warmup // 10), stream, flush_bytes)
+    ms32 = timed_replays(f32, f32_steps, 5, stream, flush_bytes, sampler, "fp32")
     path32 = g.last_path()
     if prev_path is not None:
         g.force_path(prev_path)
     launches32 = LaunchTally.last / f32_steps
+    # the CUDA-core FFMA SGEMM on the same workload (forced)
+    prev_path = g.force_path(PATH_FFMA_ONLY)
+    try:
+        ms_ffma = timed_replays(f32, 20, 3, stream, flush_bytes, sampler, "fp32_ffma")
+        path_ffma = g.last_path()
+    finally:
+        g.force_path(prev_path)
     torch.cuda.synchronize()
-    t_wall1 = time.perf_counter()
-    clocks = sampler.stop()
     assert g.debug_status() == 0, "a kernel reported a timeout"
 
     mean16 = sum(ms16) / len(ms16)
     mean32 = sum(ms32) / len(ms32)
+    mean_ffma = sum(ms_ffma) / len(ms_ffma)
     if world > 1:
         mean16, mean32 = max_over_ranks([mean16, mean32], device="cuda")
     flops = 2.0 * M * N * K
     tflops16 = flops / (mean16 * 1e-3) / 1e12
     tflops32 = flops / (mean32 * 1e-3) / 1e12
+    tflops_ffma = flops / (mean_ffma * 1e-3) / 1e12
 
     # fp16 operands with an fp32 C, and the fp32 -> fp16 conversion of C
     f32c = torch.from_numpy(synthetic.uniform(seed, synthetic.STREAM_C, (M, N),
@@ -298,6 +497,7 @@ def run_ours(args, rank, world):
     # the other workloads of the metric, timed the same way (context for the headline)
     shapes = []
     squares = []
+    sweep = None
     if not args.no_shapes:
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         for (sM, sN, sK, slda, alpha, beta, name) in EDGE_SHAPES:
@@ -333,6 +533,8 @@ def run_ours(args, rank, world):
                             "frac_3xtf32_ceiling": round(tf / ceiling32, 4),
                             "kernel_path": g.last_path()})
             del sA, sB, sC
+        del fA, fB, fC
+        sweep = sweep_subset(stream, flush_bytes, sampler)
 
     # end to end through the host-buffer C-ABI call (copies inside the timed region)
     pA = torch.from_numpy(hA).pin_memory()
@@ -352,21 +554,37 @@ def run_ours(args, rank, world):
     if world > 1:
         (e2e_mean,) = max_over_ranks([e2e_mean], device="cuda")
 
+    tf32_meas = None
+    if not args.no_tf32_peak:
+        try:
+            tf32_meas = measured_tf32_tflops()
+        except Exception:        # noqa: BLE001 -- the denominator falls back to the nominal ratio
+            tf32_meas = None
+    sampler.stop()
+    clk16 = sampler.summary(["fp16", "fp16_sustained"])
+    clk32 = sampler.summary(["fp32"])
+    clk_ffma = sampler.summary(["fp32_ffma"])
+
     peak16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    sm_count = props.multi_processor_count or SM_COUNT_NOMINAL
     peak_ffma = sm_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     traffic = _profiled_traffic("tc_f16_4096")
     if path32.startswith("f32.3xtf32"):
         # three tf32 tensor products per fp32 multiply-add: the fp32 ceiling is
-        # a third of the tf32 dense rate (the bf16 peak x the nominal
-        # tf32/bf16 ratio of 1.1/2.25 PFLOP/s)
-        peak32 = peak16 * (1.1 / 2.25) / 3.0
+        # a third of the dense tf32 rate (measured in this run when possible,
+        # else the bf16 peak x the nominal tf32/bf16 ratio of 1.1/2.25)
+        nominal32 = peak16 * (1.1 / 2.25) / 3.0
+        if tf32_meas:
+            peak32 = tf32_meas / 3.0
+            src32 = ("dense tf32 rate measured in this run (torch.matmul fp32 with tf32 allowed, "
+                     "8192^3, best of 10: %.1f TFLOP/s) / 3 tf32 products per fp32 FLOP" % tf32_meas)
+        else:
+            peak32 = nominal32
+            src32 = ("%s bf16 dense burst x 1.1/2.25 (tf32 nominal ratio) / 3 tf32 products per "
+                     "fp32 FLOP" % peaks_src)
         roof32 = {"bound": "tensor", "achieved": round(tflops32, 2), "peak": round(peak32, 2),
                   "unit": "TFLOP/s", "frac": round(tflops32 / peak32, 4),
                   "traffic": _profiled_traffic("sgemm_3xtf32_4096"),
-                  "peak_source": "%s bf16 dense burst x 1.1/2.25 (tf32 nominal ratio) / 3 tf32 "
-                                 "products per fp32 FLOP" % peaks_src,
+                  "peak_source": src32, "frac_of_nominal_ratio_ceiling": round(tflops32 / nominal32, 4),
                   "launches_per_step": launches32,
                   "note": "time includes the operand-split pre-passes",
                   "vs_ffma_peak": round(tflops32 / peak_ffma, 3)}
@@ -377,6 +595,9 @@ def run_ours(args, rank, world):
                   "traffic": _profiled_traffic("sgemm_ffma_4096"),
                   "peak_source": "%d SMs x 128 FP32 lanes x 2 FLOP x %.0f MHz" % (sm_count, sm_max),
                   "launches_per_step": launches32}
+    ffma_clock_peak = (sm_count * FP32_LANES_PER_SM * 2 * clk_ffma["sm_mhz"] * 1e6 / 1e12
+                       if clk_ffma["sm_mhz"] else None)
+    mean16s = sum(ms16s) / len(ms16s) if ms16s else None
 
     line = {
         "metric": METRIC,
@@ -410,6 +631,15 @@ def run_ours(args, rank, world):
             "algorithmic_bytes_per_launch": 2 * (M * K + K * N) + 2 * 2 * M * N,
             "launches_per_step": launches16,
         },
+        "fp16_sustained": {
+            "workload": "the headline replays (flush, event pair, GEMM) back to back for %.1f s"
+                        % args.sustain_seconds,
+            "replays": len(ms16s),
+            "us": round(mean16s * 1e3, 2) if mean16s else None,
+            "tflops": round(flops / (mean16s * 1e-3) / 1e12, 1) if mean16s else None,
+            "frac": round(flops / (mean16s * 1e-3) / 1e12 / peak16, 4) if mean16s else None,
+            "clocks": sampler.summary(["fp16_sustained"]),
+        },
         "fp32_sgemm": {
             "workload": "fp32 SGEMM C=A*B, M=N=K=4096, alpha=1 beta=0" +
                         (" (CUDA-core FFMA kernel forced)" if args.f32_ffma else ""),
@@ -419,8 +649,27 @@ def run_ours(args, rank, world):
             "steps": f32_steps,
             "kernel_path": path32,
             "roofline": roof32,
+            "clocks": clk32,
             "context_vs_page_colab_86ms": round(tflops32 / (2 * 4096 ** 3 / 86.1e-3 / 1e12), 1),
         },
+        "fp32_ffma": {
+            "workload": "fp32 SGEMM C=A*B, M=N=K=4096, alpha=1 beta=0, CUDA-core FFMA kernel forced",
+            "tflops": round(tflops_ffma, 2),
+            "ms_per_step": round(mean_ffma, 4),
+            "steps": len(ms_ffma),
+            "kernel_path": path_ffma,
+            "roofline": {"bound": "alu", "achieved": round(tflops_ffma, 2),
+                         "peak": round(peak_ffma, 2), "unit": "TFLOP/s",
+                         "frac": round(tflops_ffma / peak_ffma, 4),
+                         "peak_source": "%d SMs x 128 FP32 lanes x 2 FLOP x %.0f MHz (max clock)"
+                                        % (sm_count, sm_max),
+                         "frac_at_sampled_clock": (round(tflops_ffma / ffma_clock_peak, 4)
+                                                   if ffma_clock_peak else None),
+                         "traffic": _profiled_traffic("sgemm_ffma_4096")},
+            "clocks": clk_ffma,
+        },
+        "fp32_sweep": sweep,
+        "tf32_dense_tflops_measured": round(tf32_meas, 1) if tf32_meas else None,
         "e2e": {
             "value": round(flops * world / (e2e_mean * 1e-3) / 1e12, 3),
             "unit": "TFLOPS",
@@ -433,7 +682,8 @@ def run_ours(args, rank, world):
         "fp32_squares": squares,
         **extra,
         "gpu_launches": LaunchTally.total,
-        "clocks": clocks,
+        "clocks": clk16,
+        "clock_scaled_ms": (round(mean16 * clk16["sm_mhz"], 3) if clk16["sm_mhz"] else None),
         "wall_s_timed": round(t_wall1 - t_wall0, 3),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -582,7 +832,7 @@ def run_sweep(args):
             out.write(json.dumps(rec) + "\n")
             out.flush()
         del A, B, C
-    clocks = sampler.stop()
+    clocks = sampler.stop().summary()
     print(json.dumps({"sweep": "fp32 SGEMM 1024..12800 step 128", "sizes": len(results),
                       "clocks": clocks,
                       "tflops_mean": round(sum(r["tflops"] for r in results) / max(1, len(results)), 3)}))
@@ -639,7 +889,7 @@ def run_sweep_f16(args):
             out.write(json.dumps(rec) + "\n")
             out.flush()
         del A, B, C
-    clocks = sampler.stop()
+    clocks = sampler.stop().summary()
     print(json.dumps({"sweep": "fp16 heuristic 1024..12800 step 128", "sizes": len(sizes),
                       "auto_best": best_is_auto, "auto_within_2pct": within, "clocks": clocks}))
 
@@ -655,6 +905,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-shapes", action="store_true", help="skip the edge-shape timings")
+    ap.add_argument("--sustain-seconds", type=float, default=2.0,
+                    help="headline replays back to back afterwards (clock samples under load)")
+    ap.add_argument("--no-tf32-peak", action="store_true",
+                    help="skip measuring the dense tf32 rate (3xTF32 denominator)")
     ap.add_argument("--f32-ffma", action="store_true",
                     help="time the fp32 leg on the CUDA-core FFMA kernel instead of 3xTF32")
     ap.add_argument("--sweep", action="store_true")

@@ -312,33 +312,69 @@ bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool ha
   return sk_cost < halves_cost;
 }
 
-int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
-                 int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+// Tensor maps encode only host-side facts (address, shape, stride, box,
+// swizzle), so a map built once for a key stays valid for every later call
+// with the same key, whatever happened to the memory in between.  Each host
+// thread keeps the last kMapCache maps it encoded and reuses them: repeated
+// calls on the same operands skip cuTensorMapEncodeTiled (the run-time
+// dispatch stays cheap, as the kernel-selection section of the "advanced
+// SGEMM" page asks of it).
+struct MapKey {
+  const void* ptr;
+  long long ld;
+  int rows, cols, box_cols, box_rows;
+  int dtype, swizzle;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && ld == o.ld && rows == o.rows && cols == o.cols &&
+           box_cols == o.box_cols && box_rows == o.box_rows && dtype == o.dtype &&
+           swizzle == o.swizzle;
+  }
+};
+constexpr int kMapCache = 16;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int used = 0, next = 0;
+};
+thread_local MapCache t_maps;
+
+int make_map(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const void* ptr, int rows,
+             int cols, long long ld, int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
+  const MapKey k{ptr, ld, rows, cols, box_cols, box_rows, static_cast<int>(dtype),
+                 static_cast<int>(swizzle)};
+  MapCache& c = t_maps;
+  for (int i = 0; i < c.used; ++i)
+    if (c.key[i] == k) {
+      *map = c.map[i];
+      return GEMM_OK;
+    }
   EncodeTiledFn enc = nullptr;
   if (int rc = encode_fn(&enc)) return rc;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+  const CUresult r = enc(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+  const int slot = c.used < kMapCache ? c.used++ : c.next;
+  c.next = (slot + 1) % kMapCache;
+  c.key[slot] = k;
+  c.map[slot] = *map;
+  return GEMM_OK;
+}
+
+int make_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
+                 int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, rows, cols, ld, box_cols, box_rows,
+                  swizzle);
 }
 
 int make_map_f32(CUtensorMap* map, const void* ptr, int rows, int cols, long long ld,
                  int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  EncodeTiledFn enc = nullptr;
-  if (int rc = encode_fn(&enc)) return rc;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, rows, cols, ld, box_cols, box_rows,
+                  swizzle);
 }
 
 // Blocks of 256 threads for `elems` work items, at most `per_sm` blocks per SM
@@ -896,6 +932,8 @@ int encode_map_f16(CUtensorMap* map, const void* ptr, int rows, int cols, long l
 }
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void set_last_path(const char* path) { t_last_path = path; }
 
 }  // namespace gb300
 

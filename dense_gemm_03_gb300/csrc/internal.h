@@ -11,6 +11,9 @@ namespace gb300 {
 // Every kernel launch of the library goes through counted_launch: a
 // successful launch adds one to a process-wide counter (gemm_launch_count).
 void note_launch();
+// Records the path the current call on this thread takes (a static string);
+// gemm_last_path() returns it.
+void set_last_path(const char* path);
 inline cudaError_t counted_launch(cudaError_t e) {
   if (e == cudaSuccess) note_launch();
   return e;

@@ -80,7 +80,10 @@ extern "C" int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uin
                                        int N, int K, int lda, int ldb, int ldc, float alpha,
                                        float beta, int splits, cudaStream_t stream) {
   if (M < 0 || N < 0 || K < 0 || splits < 0) return M < 0 || N < 0 || K < 0 ? GEMM_ERR_DIM : GEMM_ERR_ARG;
-  if (M == 0 || N == 0) return GEMM_OK;
+  if (M == 0 || N == 0) {
+    set_last_path("noop");
+    return GEMM_OK;
+  }
   if (ldc < N || (K > 0 && (lda < K || ldb < N))) return GEMM_ERR_LD;
   if (C == nullptr) return GEMM_ERR_NULL;
   if (K > 0 && alpha != 0.0f && (A == nullptr || B == nullptr)) return GEMM_ERR_NULL;
@@ -96,6 +99,7 @@ extern "C" int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uin
   if (int rc = scratch_on_current_device(&scratch)) return rc;
 
   if (alpha == 0.0f || K == 0) {   // no products: C := beta*C, scratch unused
+    set_last_path("f16.scale.noalloc");
     const long long blocks = (1ll * M * N + 255) / 256;
     const int grid = static_cast<int>(std::max(1ll, std::min<long long>(blocks, 8ll * sm_count)));
     return launch_scale_f16(C, ldc, M, N, beta, grid, stream) == cudaSuccess ? GEMM_OK
@@ -147,6 +151,7 @@ extern "C" int gemm_f16_splitk_noalloc(const uint16_t* A, const uint16_t* B, uin
     if (int rc = encode_map_f16(&tmB, B, K, N, ldb, 64, 64)) return rc;
   }
   const int grid = static_cast<int>(std::min<long long>(a.num_units, sm_count));
+  set_last_path(ab_tma ? "f16.splitk.noalloc.tma" : "f16.splitk.noalloc.manual");
   if (launch_gemm_f16_tc(bn, ab_tma ? kLoadTma : kLoadManual, kEpiPartial, tmA, tmB, tmC, a, grid,
                          stream) != cudaSuccess)
     return GEMM_ERR_CUDA;

@@ -32,9 +32,22 @@ def test_sweep_range():
     assert all(a >= b for a, b in zip(counts, counts[1:])) and counts[-1] >= 1
 
 
-def test_clock_summary_parses_nvidia_smi_rows():
-    rows = [["0", "t", "1900", "2070", "900.1", "0x0", "Not Active", "Not Active", "Not Active", "Active"],
-            ["0", "t", "1800", "2070", "950.0", "0x4", "Not Active", "Not Active", "Not Active", "Not Active"],
-            ["0", "t", "300", "2070", "90.0", "0x1", "Not Active", "Not Active", "Not Active", "Not Active"]]
-    s = bench.ClockSampler._summary(rows)
-    assert s["sm_mhz"] == 1850 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+def test_clock_summary_keeps_samples_inside_timed_windows():
+    """Only samples taken inside the named timed windows count; idle samples
+    (NVML reason bit 0x1, or a clock below half the maximum) are not 'under
+    load'; reason bits map to their names."""
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples = [(0.5, 1000.0, 2070.0, 0x0, 90.0),      # outside every window
+                 (1.1, 1900.0, 2070.0, 0x0, 900.0),
+                 (1.2, 1800.0, 2070.0, 0x4, 950.0),     # sw_power_cap
+                 (1.9, 300.0, 2070.0, 0x1, 80.0),       # idle
+                 (3.0, 2000.0, 2070.0, 0x8, 1000.0)]    # hw_slowdown, second window
+    s.windows = {"a": [1.0, 2.0], "b": [2.5, 3.5]}
+    s.source = "test"
+    r = s.summary(["a"])
+    assert r["samples"] == 3 and r["samples_under_load"] == 2
+    assert r["sm_mhz"] == 1850 and r["sm_max_mhz"] == 2070 and r["reasons"] == ["sw_power_cap"]
+    assert r["power_w_max"] == 950.0
+    r = s.summary(["a", "b"])
+    assert r["sm_mhz"] == 1900 and r["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert s.summary(["missing"])["sm_mhz"] is None
