@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 
 # M, N, K, lda, ldb, ldc, alpha, beta, K slices (0 = automatic), load mode in the path
 CASES = [(16, 8192, 8192, 8192, 8192, 8192, 0.75, -0.25, 0, "tma"),
-         (300, 500, 3000, 3000, 500, 500, 1.5, 0.5, 4, "tma"),
+         (300, 512, 3000, 3000, 512, 512, 1.5, 0.5, 4, "tma"),
          # rows of A and B off the 16-byte grid (K + 3, N): predicated element loads
          (300, 1023, 777, 780, 1023, 1023, 0.75, -0.25, 4, "manual")]
 
