@@ -277,10 +277,14 @@ def last_path() -> str:
     return lib().gemm_last_path().decode()
 
 
-def plan_stream_k(tiles: int, slots: int, kb: int, all_tiles: bool = False) -> dict:
-    """The stream-K plan of the half-precision path (host-side query)."""
+def plan_stream_k(tiles: int, slots: int, kb: int, all_tiles: bool = False,
+                  tail: bool = False) -> dict:
+    """The stream-K plan of the half-precision path (host-side query):
+    the last two waves, all tiles (``all_tiles``) or the last partial wave
+    (``tail``)."""
     out = (ctypes.c_longlong * 4)()
-    _check(lib().gemm_plan_stream_k(tiles, slots, kb, int(bool(all_tiles)), out), "gemm_plan_stream_k")
+    mode = 2 if tail else int(bool(all_tiles))
+    _check(lib().gemm_plan_stream_k(tiles, slots, kb, mode, out), "gemm_plan_stream_k")
     return {"dp_tiles": out[0], "sk_tiles": out[1], "workers": out[2], "max_pieces": out[3]}
 
 

@@ -18,8 +18,11 @@
 //      is expected to beat half-width units (few_tiles_prefer_stream_k)
 //   7. CTA pairs (256 x 256 tiles) for 256-wide TMA shapes with at least two
 //      tile rows; 32 or 64 rows of A staged per k-block when M <= 64
-//   8. the tiles of the last, partial wave run as two half-width units each
-//      when the halves fit in one wave
+//   8. the tiles of the last, partial wave are shared out as stream-K pieces
+//      (each worker runs the piece that starts a tile first and the piece that
+//      ends a tile last, plan_tail_stream_k) when that is expected to beat two
+//      half-width units per tile, which are used otherwise when the halves fit
+//      in one wave
 // The fp32 GEMM (sgemm_f32_ld) takes the 3xTF32 tensor-core path for
 // K >= 64 (with K slices when few tiles meet a long K, plan_tf32_slices),
 // else the FFMA kernel.
@@ -289,6 +292,52 @@ SkPlan plan_stream_k(long long tiles, long long slots, int kb, bool all_tiles) {
   return p;
 }
 
+// Stream-K over the last, partial wave only, in the order of sk_order 1:
+// the `tiles` % `slots` tiles after the whole waves are shared out as k-block
+// ranges over up to kTailPieces workers per tile (no range longer than a
+// tile, none shorter than kSkMinKb k-blocks).  Each worker runs the part of its range
+// that starts a tile before its whole tiles and the part that ends a tile
+// after them, so the piece that finishes a tile finds the others published.
+constexpr long long kTailPieces = 4;
+
+SkPlan plan_tail_stream_k(long long tiles, long long slots, int kb) {
+  SkPlan p;
+  if (tiles <= slots || slots <= 0 || kb < 2 * kSkMinKb) return p;
+  const long long rem = tiles % slots;
+  if (rem == 0) return p;
+  const long long iters = rem * kb;
+  if (iters >= (1ll << 31)) return p;
+  const long long workers = std::min({slots, rem * kTailPieces, iters / kSkMinKb});
+  if (workers <= rem) return p;   // no range may be longer than a tile
+  const long long range = iters / workers;   // shortest range
+  p.dp_tiles = tiles - rem;
+  p.sk_tiles = rem;
+  p.workers = workers;
+  p.max_pieces = (kb + range - 1) / range + 1;
+  return p;
+}
+
+// The last, partial wave as two K slices per tile, publisher first: the
+// first slice of each of its tiles is the first unit of one worker (it
+// publishes fp32 partial sums), the second is the last unit of another worker
+// (it finishes the tile, reading the first slice's partial sums back, which
+// are long published by then and prefetched into L2 while its main loop
+// runs).  Returns the k-blocks of the first slice, or 0 when the shape does
+// not suit: at least one whole wave before the tail, the two slices of every
+// tail tile on different workers (2 x tail tiles <= slots), and at least 48
+// k-blocks (measured: with 32 or 16, half-width units are faster -- 4096^2 x
+// 2048 55.6 against 57.3 us, 2560^2 x 1024 24.6 against 27.1 us).  The finishing slice is kTailReadKb k-blocks shorter, for the
+// read-back of the other slice (measured on GB300: ~2.5 us against 0.32 us
+// per k-block of a pair tile).
+constexpr int kTailReadKb = 8;
+
+int tail_first_slice(long long tiles, long long slots, int kb) {
+  if (tiles <= slots || slots <= 0 || kb < 48) return 0;
+  const long long rem = tiles % slots;
+  if (rem == 0 || 2 * rem > slots) return 0;
+  return std::min(kb - 4, (kb + kTailReadKb + 1) / 2);
+}
+
 // Whether stream-K over all of a few tiles (plan_stream_k's all_tiles form)
 // is expected to beat half-width whole-K units, in k-block times of one
 // tile: stream-K takes the longest range plus a fix-up for every extra piece
@@ -337,6 +386,19 @@ struct MapCache {
   int used = 0, next = 0;
 };
 thread_local MapCache t_maps;
+
+// Width of the CTA-pair tiles: 256 unless forced (paths 12 / 13: 224 / 192).
+// Measured on GB300 (same-box A/B, alpha 1.5 beta 0.5): a k-block of a
+// 256 x 224 or 256 x 192 pair tile takes as long as one of a 256 x 256 tile,
+// and so does a half-width unit (N = 128; 4096^3 as 512 half-width units in
+// 7 rounds: 139 us, against 20.5 us per full round), so narrower tiles only
+// move the partial last wave: 4096^3 (304 tiles of 224 = 4 waves) 91.7 us
+// against 92.2 us for 256-wide tiles with a half-width tail; 8192x8192x4096
+// 351 against 315 us, 6144^2 x 4096 197 against 184 us, 192-wide slower
+// still.  A narrower tile never wins once its per-tile time equals the
+// 256-wide one, so the automatic choice keeps 256 and balances the last wave
+// along K instead (plan_tail_stream_k).
+int pair_width(int force) { return force == 12 ? 224 : (force == 13 ? 192 : 256); }
 
 int make_map(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const void* ptr, int rows,
              int cols, long long ld, int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
@@ -397,9 +459,6 @@ const char* kPathNames[3][2][3] = {
      {"f16.tc.bn256.manual.epi_tma", "f16.tc.bn256.manual.epi_manual",
       "f16.tc.bn256.manual.splitk"}},
 };
-
-const char* kPairPathNames[2] = {"f16.tc.pair.bn256.tma.epi_tma",
-                                 "f16.tc.pair.bn256.tma.epi_manual"};
 
 int check_common(const void* A, const void* B, const void* C, int M, int N, int K, long long lda,
                  long long ldb, long long ldc, float alpha, size_t elem = 1) {
@@ -553,6 +612,11 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   const bool pair = splits == 1 && !few_sk && force != 6 && bn == 256 &&
                     load == kLoadTma && a.tiles_m >= 2 &&
                     (pair_slots = tc_pair_max_clusters(epi)) > 0;
+  // forced narrower pair tiles (the tile-family comparison)
+  if (pair && !c_f32 && (force == 12 || force == 13)) {
+    bn = pair_width(force);
+    a.tiles_n = (N + bn - 1) / bn;
+  }
   // fp32 C on CTA pairs goes through shared memory and TMA when its rows are
   // 16-byte aligned and N is a multiple of 4 (a TMA store writes whole 16-byte
   // pieces of a row)
@@ -620,18 +684,44 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
       if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
       cut = ".sk";
     }
-  } else if (force != 5 && !few_sk) {
-    // The tiles of the last, partial wave become two half-width units each
-    // (whole K, no partial sums) when the halves fit in one wave.
+  } else if (force != 5 && force != 12 && force != 13 && !few_sk) {
+    // The tiles of the last, partial wave: two K slices each, the first slice
+    // a worker's first unit and the second another worker's last
+    // (tail_first_slice); else two half-width units each (whole K, no partial
+    // sums) when the halves fit in one wave.  Forced path 14 shares them out
+    // as stream-K pieces instead (plan_tail_stream_k), 15 takes half-width
+    // units.
     const long long rem = units_tiles % slots;
-    if (load == kLoadTma && bn >= 128 && rem > 0 && 2 * rem <= slots) {
+    const SkPlan sk = force == 14 ? plan_tail_stream_k(units_tiles, slots, a.kb_total) : SkPlan{};
+    const int first_kb =
+        (force == 14 || force == 15) ? 0 : tail_first_slice(units_tiles, slots, a.kb_total);
+    if (first_kb > 0) {
+      a.dp_tiles = static_cast<int>(units_tiles - rem);
+      a.tail_splits = 2;
+      a.tail_kb_per_split = first_kb;
+      a.tail_first = 1;
+      workers = slots;
+      if (int rc = take_scratch(rem * (pair ? 2 : 1), 2)) return rc;
+      cut = ".ktail";
+    } else if (sk.sk_tiles > 0) {
+      a.dp_tiles = static_cast<int>(sk.dp_tiles);
+      a.sk_tile0 = static_cast<int>(sk.dp_tiles);
+      a.sk_tiles = static_cast<int>(sk.sk_tiles);
+      a.sk_workers = static_cast<int>(sk.workers);
+      a.sk_iters = sk.sk_tiles * a.kb_total;
+      a.sk_order = 1;
+      a.tail_splits = static_cast<int>(sk.max_pieces);
+      workers = slots;
+      if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
+      cut = ".sktail";
+    } else if (load == kLoadTma && (bn == 128 || bn == 256) && rem > 0 && 2 * rem <= slots) {
       a.dp_tiles = static_cast<int>(units_tiles - rem);
       a.tail_splits = 2;
       a.tail_halves = 1;
       workers = std::min<long long>(slots, a.dp_tiles > 0 ? slots : 2 * rem);
       cut = ".halves";
     }
-  } else if (force != 5) {
+  } else if (force != 5 && few_sk) {
     const SkPlan sk = plan_stream_k(units_tiles, slots, a.kb_total, true);
     if (sk.sk_tiles > 0) {
       a.dp_tiles = static_cast<int>(sk.dp_tiles);
@@ -666,17 +756,18 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
     // the same 64-byte rows: 32 rows x 16 floats
     if (int rc = make_map_f32(&tmC, a.Cf, M, N, ldc, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
   }
-  // one CTA (pair) per worker; with stream-K exactly sk_workers of them
-  const long long nw = a.sk_tiles > 0 ? a.sk_workers : std::min<long long>(a.num_units, workers);
+  // one CTA (pair) per worker; with stream-K over all tiles or the last waves
+  // exactly sk_workers of them, with the stream-K tail every worker
+  const long long nw = a.sk_tiles > 0 ? (a.sk_order ? workers : a.sk_workers)
+                                      : std::min<long long>(a.num_units, workers);
   if (pair) {
     const int grid = 2 * static_cast<int>(nw);
-    snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s",
-             c_f32 ? (epi == kEpiF32Tma ? "f16.tc.pair.bn256.tma.epi_f32_tma"
-                                        : "f16.tc.pair.bn256.tma.epi_f32")
-                   : kPairPathNames[epi],
+    snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.pair.bn%d.tma.%s%s%s", bn,
+             epi == kEpiF32Tma ? "epi_f32_tma"
+                               : (epi == kEpiF32 ? "epi_f32" : (epi == kEpiTma ? "epi_tma" : "epi_manual")),
              cut, how);
     t_last_path = t_path_buf;
-    if (launch_gemm_f16_tc_pair(epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
+    if (launch_gemm_f16_tc_pair(bn, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     return GEMM_OK;
   }
@@ -1014,7 +1105,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 11) return GEMM_ERR_ARG;
+  if (path < 0 || path > 15) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 
@@ -1055,7 +1146,8 @@ int gemm_debug_wait_probe(long long limit_ns, cudaStream_t stream) {
 
 int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, long long* out) {
   if (out == nullptr) return GEMM_ERR_NULL;
-  const SkPlan p = plan_stream_k(tiles, slots, kb, all_tiles != 0);
+  const SkPlan p = all_tiles == 2 ? plan_tail_stream_k(tiles, slots, kb)
+                                  : plan_stream_k(tiles, slots, kb, all_tiles != 0);
   out[0] = p.dp_tiles;
   out[1] = p.sk_tiles;
   out[2] = p.workers;

@@ -36,11 +36,14 @@ cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtens
   }
 }
 
-cudaError_t launch_gemm_f16_tc_pair(int epi_mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                    const CUtensorMap& tmC, const TcArgs& args, int grid,
-                                    cudaStream_t stream) {
+cudaError_t launch_gemm_f16_tc_pair(int bn, int epi_mode, const CUtensorMap& tmA,
+                                    const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                    const TcArgs& args, int grid, cudaStream_t stream) {
   if (epi_mode == kEpiF32 || epi_mode == kEpiF32Tma)
-    return launch_gemm_f16_tc_pair_f32(epi_mode, tmA, tmB, tmC, args, grid, stream);
+    return bn == 256 ? launch_gemm_f16_tc_pair_f32(epi_mode, tmA, tmB, tmC, args, grid, stream)
+                     : cudaErrorInvalidValue;
+  if (bn != 256)
+    return launch_gemm_f16_tc_pair_narrow(bn, epi_mode, tmA, tmB, tmC, args, grid, stream);
   if (epi_mode == kEpiTma)
     return launch_one<256, kLoadTma, kEpiTma, true>(tmA, tmB, tmC, args, grid, stream);
   if (epi_mode == kEpiManual)

@@ -62,15 +62,19 @@ constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 constexpr int kCsBufs = 2;
 
 // PAIR: two CTAs of a cluster share each tcgen05.mma.cta_group::2 (M = 256);
-// each CTA stages its own 128 rows of A and half of the BN columns of B.
+// each CTA stages its own 128 rows of A and half of the BN columns of B.  A
+// pair tile is 256 wide, or 224 / 192 wide (the tile-family comparison: the
+// MMA takes N = BN; B is still staged in whole 64-column boxes, of which the
+// MMA reads the first BN/2 columns).
 // AM: rows of A staged per k-block.  128 normally; 32 or 64 for shapes with
 // M <= AM, whose stages then hold more of B (the MMA still reads 128 rows of
 // A: the rows past AM come from the stage's B region and only produce
 // accumulator rows >= M, which are never stored).
 template <int BN, bool PAIR, bool CS = false, int AM = 128>
 struct TcCfg {
-  static constexpr int kBLoadCols = PAIR ? BN / 2 : BN;   // B columns staged by this CTA
-  static constexpr int kBBytes = kBLoadCols * BK * 2;
+  static constexpr int kBLoadCols = PAIR ? BN / 2 : BN;   // B columns this CTA gives the MMA
+  static constexpr int kBStageCols = (kBLoadCols + 63) / 64 * 64;   // staged: whole boxes
+  static constexpr int kBBytes = kBStageCols * BK * 2;
   static constexpr int kAStageBytes = AM * BK * 2;
   static constexpr int kStageBytes = kAStageBytes + kBBytes;
   // skinny stages: as many as fit beside the epilogue tiles, at most 16
@@ -78,9 +82,11 @@ struct TcCfg {
   static constexpr int kStages =
       AM < 128 ? (kSkinnyStages < 16 ? kSkinnyStages : 16)
                : (PAIR ? ((CS && kCsBufs > 2) ? 5 : 6) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)));
-  static constexpr int kTmemCols = 2 * BN;     // two accumulators
-  static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
-  static_assert(!PAIR || BN == 256, "pairs use 256-wide tiles");
+  // TMEM columns per accumulator (a power of two) and for both of them
+  static constexpr int kAccStride = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
+  static constexpr int kTmemCols = 2 * kAccStride;
+  static_assert(PAIR ? (BN == 256 || BN == 224 || BN == 192) : (BN == 64 || BN == 128 || BN == 256),
+                "tile width");
   static_assert(AM == 128 || (!PAIR && kStageBytes >= kABytes), "skinny stages span 128 A rows");
 };
 
@@ -151,6 +157,33 @@ __device__ __forceinline__ Unit decode_unit(const TcArgs& p, int u, int bn, int 
   Unit x;
   int tile, kpb;
   const int dp_units = p.dp_tiles * p.splits;
+  if (p.tail_first) {
+    // The T tiles cut in two are the first T in visiting order (so that the
+    // first wave, their first slices beside the first whole tiles, reads the
+    // same panels of A and B as a wave of whole tiles would).  Units [0, T)
+    // are their first slices, [T, T + dp_tiles) the whole tiles T, T + 1, ...,
+    // then come their second slices.
+    const int T = (p.num_units - p.dp_tiles) >> 1;
+    x.split = 0;
+    x.ncols = bn;
+    if (u >= T && u < T + p.dp_tiles) {
+      tile_origin(p, u, bn, bm_tile, rank, x);
+      x.tail = 0;
+      x.tail_idx = 0;
+      x.npieces = 1;
+      x.kb0 = 0;
+      x.kb1 = p.kb_total;
+      return x;
+    }
+    x.tail_idx = u < T ? u : u - T - p.dp_tiles;
+    x.split = u < T ? 0 : 1;
+    x.tail = 1;
+    x.npieces = 2;
+    tile_origin(p, x.tail_idx, bn, bm_tile, rank, x);
+    x.kb0 = x.split ? p.tail_kb_per_split : 0;
+    x.kb1 = x.split ? p.kb_total : p.tail_kb_per_split;
+    return x;
+  }
   if (u < dp_units) {
     tile = u / p.splits;
     x.split = u - tile * p.splits;
@@ -198,39 +231,50 @@ __device__ __forceinline__ int sk_owner(const TcArgs& p, int x) {
   return static_cast<int>((static_cast<long long>(x + 1) * p.sk_workers - 1) / p.sk_iters);
 }
 
-// Position of one worker in its sequence of units: first the units
-// worker, worker + nworkers, ... below num_units, then the pieces of its
-// stream-K range [x, x_end).
+// Position of one worker in its sequence of units.  sk_order 0: first the
+// units worker, worker + nworkers, ... below num_units, then the pieces of its
+// stream-K range [x, x_end).  sk_order 1: first the piece [x, x_end) (part of
+// a tile that another worker finishes), then the units, then the piece
+// [fx, fx_end) that ends its tile.
 struct UnitCursor {
-  int u, x, x_end;   // the host keeps sk_iters below 2^31
+  int u, x, x_end, fx, fx_end;   // the host keeps sk_iters below 2^31
 };
 
 __device__ __forceinline__ UnitCursor first_unit(const TcArgs& p, int worker) {
   UnitCursor c;
   c.u = worker;
+  c.x = c.x_end = c.fx = c.fx_end = 0;
   if (p.sk_tiles > 0 && worker < p.sk_workers) {
-    c.x = sk_begin(p, worker);
-    c.x_end = sk_begin(p, worker + 1);
-  } else {
-    c.x = c.x_end = 0;
+    const int x0 = sk_begin(p, worker), x1 = sk_begin(p, worker + 1);
+    if (p.sk_order == 0) {
+      c.x = x0;
+      c.x_end = x1;
+    } else {
+      // the range is no longer than a tile: it ends the tile holding x0 (and
+      // may start the next one), or it lies inside one tile
+      const int tile_end = (x0 / p.kb_total + 1) * p.kb_total;
+      if (x1 >= tile_end) {
+        c.fx = x0;
+        c.fx_end = tile_end;
+        c.x = tile_end;
+        c.x_end = x1;
+      } else {
+        c.x = x0;
+        c.x_end = x1;
+      }
+    }
   }
   return c;
 }
 
-// The worker's next unit into t; false when it has none left.
-__device__ __forceinline__ bool next_unit(const TcArgs& p, UnitCursor& c, int worker,
-                                          int nworkers, int bn, int bm_tile, int rank, Unit& t) {
-  if (c.u < p.num_units) {
-    t = decode_unit(p, c.u, bn, bm_tile, rank);
-    c.u += nworkers;
-    return true;
-  }
-  if (c.x >= c.x_end) return false;
+// The stream-K piece starting at k-block x of the shared region (at most
+// x_end, within one tile) into t; returns the k-blocks it covers.
+__device__ __forceinline__ int sk_piece(const TcArgs& p, int x, int x_end, int worker, int bn,
+                                        int bm_tile, int rank, Unit& t) {
   const int kb = p.kb_total;
-  const int s = c.x / kb;   // stream-K tile
-  t.kb0 = c.x - s * kb;
-  t.kb1 = min(kb, t.kb0 + (c.x_end - c.x));
-  c.x += t.kb1 - t.kb0;
+  const int s = x / kb;   // stream-K tile
+  t.kb0 = x - s * kb;
+  t.kb1 = min(kb, t.kb0 + (x_end - x));
   const int first = sk_owner(p, s * kb);
   const int last = sk_owner(p, (s + 1) * kb - 1);
   t.npieces = last - first + 1;
@@ -239,6 +283,28 @@ __device__ __forceinline__ bool next_unit(const TcArgs& p, UnitCursor& c, int wo
   t.tail_idx = s;
   t.ncols = bn;
   tile_origin(p, p.sk_tile0 + s, bn, bm_tile, rank, t);
+  return t.kb1 - t.kb0;
+}
+
+// The worker's next unit into t; false when it has none left.
+__device__ __forceinline__ bool next_unit(const TcArgs& p, UnitCursor& c, int worker,
+                                          int nworkers, int bn, int bm_tile, int rank, Unit& t) {
+  if (p.sk_order != 0 && c.x < c.x_end) {
+    c.x += sk_piece(p, c.x, c.x_end, worker, bn, bm_tile, rank, t);
+    return true;
+  }
+  if (c.u < p.num_units) {
+    t = decode_unit(p, c.u, bn, bm_tile, rank);
+    c.u += nworkers;
+    return true;
+  }
+  if (p.sk_order != 0) {
+    if (c.fx >= c.fx_end) return false;
+    c.fx += sk_piece(p, c.fx, c.fx_end, worker, bn, bm_tile, rank, t);
+    return true;
+  }
+  if (c.x >= c.x_end) return false;
+  c.x += sk_piece(p, c.x, c.x_end, worker, bn, bm_tile, rank, t);
   return true;
 }
 
@@ -499,9 +565,10 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
               ok = false;
               break;
             }
-            // B columns this CTA stages: a half-width unit needs half of them
+            // B columns this CTA gives the MMA (a half-width unit needs half of
+            // them), staged in whole 64-column boxes
             const int bcols = PAIR ? t.ncols / 2 : t.ncols;
-            const uint32_t bytes = static_cast<uint32_t>(kAB + bcols * BK * 2);
+            const uint32_t bytes = static_cast<uint32_t>(kAB + ((bcols + 63) / 64) * kBBlockBytes);
             if (PAIR) {
               // Both CTAs' bytes are counted on the leader's barrier; only the
               // leader arms it (for the pair's total), the peer's copies just
@@ -510,7 +577,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
               if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
               tma_load_2d_pair(stage_a(stage), &tmA, fb, kb * BK, t.m0);
 #pragma unroll
-              for (int c = 0; c < Cfg::kBLoadCols / 64; ++c)
+              for (int c = 0; c < Cfg::kBStageCols / 64; ++c)
                 if (64 * c < bcols)
                   tma_load_2d_pair(stage_b(stage) + c * kBBlockBytes, &tmB, fb,
                                    t.n0 + static_cast<int>(rank) * bcols + 64 * c, kb * BK);
@@ -605,7 +672,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 3)) break;
         tc_fence_after();
         const uint32_t idesc = t.ncols == BN ? idesc_full : idesc_half;
-        const uint32_t d_tmem = tmem_base + buf * BN;
+        const uint32_t d_tmem = tmem_base + buf * Cfg::kAccStride;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!wait_parity(full_bar(stage), phase, limit, st, 4)) {
             ok = false;
@@ -665,11 +732,22 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       tmem_dealloc(tmem_base, Cfg::kTmemCols);
   } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int kWarpCols = BN * 4 / R::kEpiWarps;   // columns per epilogue warp (whole tile)
-    constexpr int kSubs = kWarpCols / kSubCols;
+    // The 32-column sub-chunks of a unit are shared out between the kParts
+    // warps of each TMEM lane quadrant: part h takes chunks [lo, hi) (the first
+    // part takes the odd one of a 224-wide tile).  kSubs: most chunks of a warp.
+    constexpr int kParts = R::kEpiWarps / 4;
+    constexpr int kSubs = (BN / kSubCols + kParts - 1) / kParts;
     const int ew = warp - R::kEpiWarp0;   // 0 .. kEpiWarps-1
     const int q = warp & 3;               // TMEM lane quadrant -> rows 32q .. 32q+31
     const int h = ew >> 2;                // column part of the tile
+    // first column (within the unit) and number of sub-chunks of this warp
+    auto warp_cols = [&](const Unit& u, int& first, int& nchunks) {
+      const int nch = u.ncols / kSubCols;
+      const int lo = (h * nch + kParts - 1) / kParts;
+      const int hi = ((h + 1) * nch + kParts - 1) / kParts;
+      first = lo * kSubCols;
+      nchunks = hi - lo;
+    };
     const bool has_c = p.beta != 0.0f;
     const uint32_t sbuf0 = base + L::kEpiOff + ew * L::kWarpEpiBytes;
     uint8_t* const sptr0 = base_ptr + L::kEpiOff + ew * L::kWarpEpiBytes;
@@ -707,8 +785,10 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       return true;
     };
     auto load_c_head = [&](const Unit& u2) {   // the first NB sub-tiles of a unit
-      const int wc = u2.ncols * 4 / R::kEpiWarps;
-      const int r0 = u2.m0 + 32 * q, cw = u2.n0 + h * wc;
+      int first2, nch2;
+      warp_cols(u2, first2, nch2);
+      const int wc = nch2 * kSubCols;
+      const int r0 = u2.m0 + 32 * q, cw = u2.n0 + first2;
       if (!has_c || r0 >= p.M || cw >= p.N) return;
 #pragma unroll
       for (int j = 0; j < NB; ++j)
@@ -725,11 +805,12 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       const int row0 = t.m0 + 32 * q;
       // tail bookkeeping is per CTA: the rows of one CTA of a pair form their own part
       const int tail_part = PAIR ? 2 * t.tail_idx + static_cast<int>(rank) : t.tail_idx;
-      const int wcols = t.ncols * 4 / R::kEpiWarps;  // this warp's columns of the unit
-      const int nsub = wcols / kSubCols;
-      const int colw = t.n0 + h * wcols;            // first column of this warp
+      int wcol0, nsub;                              // this warp's columns of the unit
+      warp_cols(t, wcol0, nsub);
+      const int wcols = nsub * kSubCols;
+      const int colw = t.n0 + wcol0;                // first column of this warp
       const int row = row0 + lane;                  // this thread's row
-      bool finish = row0 < p.M && colw < p.N;       // this warp has outputs to produce
+      bool finish = nsub > 0 && row0 < p.M && colw < p.N;   // this warp has outputs to produce
       if (EPI != kEpiPartial && has_c && finish && row < p.M) {
         // While this unit's main loop runs, bring this row's part of C into
         // L2, so that the epilogue's reads of C wait on L2 and not on DRAM.
@@ -742,13 +823,25 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         const uintptr_t last = c0 + static_cast<uintptr_t>(ncols) * (kF32C ? 4 : 2) - 1;
         for (uintptr_t a = first; a <= last; a += 128) prefetch_l2(reinterpret_cast<const void*>(a));
       }
+      // A tile's last slice reads the others' partial sums back: bring them
+      // into L2 while its main loop runs (its lane's column quad, 512 bytes
+      // per warp and slice).
+      if (EPI != kEpiPartial && t.tail && t.split == t.npieces - 1 && finish &&
+          lane < wcols / 4) {
+        for (int s2 = 0; s2 + 1 < t.npieces; ++s2) {
+          const float4* part =
+              tail_partials(p, tail_part, s2, BN) + (wcol0 / 4 + lane) * BM + 32 * q;
+#pragma unroll
+          for (int l = 0; l < 4; ++l) prefetch_l2(part + 8 * l);
+        }
+      }
       // C of the first sub-chunk is requested before the accumulator is ready.
       uint4 c_next[4];
       if (!kCs && EPI == kEpiTma && has_c && finish && !t.tail) load_c_sub(p, row, colw, c_next);
       if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 5)) break;
       tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + h * wcols;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             buf * Cfg::kAccStride + static_cast<uint32_t>(wcol0);
 
       if (EPI != kEpiPartial && t.tail && finish) {
         unsigned long long* cnt = p.tail_counters + tail_part * kTailCounters + h * 4 + q;
@@ -770,11 +863,11 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
           // slice to arrive finishes the tile.
           float4* mine = tail_partials(p, tail_part, t.split, BN) + 32 * q + lane;
           for (int k = 0; k < kSubs; ++k) {
-            if (colw + kSubCols * k >= p.N) break;
+            if (k >= nsub || colw + kSubCols * k >= p.N) break;
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tbase + kSubCols * k, acc);
             tmem_wait_regs(acc);
-            const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
+            const int cq0 = (wcol0 + kSubCols * k) / 4;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               __stcg(mine + (cq0 + i) * BM,
@@ -842,7 +935,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
             // cur := sum of every slice's partial sums in slice order; this
             // slice's own term is still in TMEM (bit-identical to what it
             // published), so only the other slices are read back.
-            const int cq0 = (h * kWarpCols + kSubCols * k) / 4;
+            const int cq0 = (wcol0 + kSubCols * k) / 4;
             const float4* part = tail_partials(p, tail_part, 0, BN) + 32 * q + lane + cq0 * BM;
             const long long slice = static_cast<long long>(BN / 4) * BM;
             if (t.split == 0) {

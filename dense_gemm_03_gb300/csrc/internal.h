@@ -64,6 +64,13 @@ struct TcArgs {
   // stride of tail_ws).
   int sk_tile0, sk_tiles, sk_workers;
   long long sk_iters;
+  // sk_order 0: a worker takes its stream-K pieces after its whole tiles, in
+  // k order.  sk_order 1 (the stream-K tiles are the last, partial wave and no
+  // range is longer than a tile, so a range touches at most two tiles): the
+  // piece that ends a tile (it finishes the tile) runs last, after the whole
+  // tiles, and the other piece runs first, so that a tile's other pieces have
+  // long published when its finisher ends.
+  int sk_order;
   // kEpiF32: C is fp32 (Cf, ldc in floats) and written straight from
   // registers, with 16-byte accesses when vec_c (Cf and ldc 16-byte aligned)
   // and predicated element accesses otherwise.
@@ -73,6 +80,14 @@ struct TcArgs {
   // computed as two units of BN/2 columns each (whole K, an MMA of N = BN/2)
   // instead of K slices.
   int tail_halves;
+  // tail_first != 0 (splits == 1, tail_splits == 2, K slices of
+  // tail_kb_per_split k-blocks and the rest): the first T tiles in visiting
+  // order are cut in two; units [0, T) are their first K slices, then come the
+  // dp_tiles whole tiles T, T + 1, ..., then the second slices.  Workers take
+  // units worker, worker + nworkers, ..., so a first slice (it publishes its
+  // partial sums) is its worker's first unit and a second slice (it finishes
+  // the tile) its worker's last, long after the first was published.
+  int tail_first;
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
   // host only: the launch directly follows this call's pre-pass kernel on the
@@ -113,12 +128,18 @@ cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int 
                               cudaStream_t stream);
 
 // The same GEMM on CTA pairs (clusters of 2 sharing tcgen05.mma.cta_group::2):
-// 256 x 256 output tiles, TMA operand loads only, epilogue kEpiTma or
-// kEpiManual.  tiles_m counts 256-row tiles; grid = 2 x (number of pairs).
-cudaError_t launch_gemm_f16_tc_pair(int epi_mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                    const CUtensorMap& tmC, const TcArgs& args, int grid,
-                                    cudaStream_t stream);
-// Pairs of that configuration that fit on the device at once (0 on error).
+// 256 x bn output tiles (bn = 256, or 224 / 192 with a half C), TMA operand
+// loads only, epilogue kEpiTma or kEpiManual (or the fp32-C ones, bn = 256).
+// tiles_m counts 256-row tiles; grid = 2 x (number of pairs).
+cudaError_t launch_gemm_f16_tc_pair(int bn, int epi_mode, const CUtensorMap& tmA,
+                                    const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                    const TcArgs& args, int grid, cudaStream_t stream);
+// The 224- and 192-wide instances (gemm_f16_pair_narrow.cu).
+cudaError_t launch_gemm_f16_tc_pair_narrow(int bn, int epi_mode, const CUtensorMap& tmA,
+                                           const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                           const TcArgs& args, int grid, cudaStream_t stream);
+// Pairs of the 256-wide configuration that fit on the device at once (0 on
+// error); the narrower tiles stage the same bytes, so the same number fits.
 int tc_pair_max_clusters(int epi_mode);
 
 // Split-K reduction: C = half(alpha * sum_s ws[s] + beta * C).

@@ -200,7 +200,15 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * half-width units); 10 = stream-K over the last waves of tiles (k-block
  * ranges shared out evenly); 11 = stream-K over all tiles, one CTA per worker
  * (chosen automatically for few tiles when it is expected to beat half-width
- * units).
+ * units); 12 / 13 = CTA-pair tiles 224 / 192 columns wide for a half C
+ * (whole tiles; the automatic choice keeps 256); 14 = the tiles of the last,
+ * partial wave shared out as stream-K pieces, each worker taking the piece
+ * that starts a tile first and the piece that ends a tile last.  The
+ * automatic choice cuts the tiles of a last, partial wave that fills at most
+ * half the workers into two K slices each, the first slice one worker's
+ * first unit and the second another worker's last (it adds the first one's
+ * partial sums, published long before); else it runs them as half-width
+ * units; 15 = half-width units for them.
  * A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
@@ -240,8 +248,10 @@ const char* gemm_last_path(void);
 /*
  * The stream-K plan the half-precision path would use for `tiles` output
  * tiles of `kb` k-blocks on at most `slots` concurrent workers (CTAs or CTA
- * pairs); `all_tiles` != 0 asks for the few-tiles form (every tile's k-blocks
- * shared out).  Writes out[0] = whole tiles computed first, out[1] = tiles
+ * pairs); `all_tiles` = 1 asks for the few-tiles form (every tile's k-blocks
+ * shared out), 2 for the tail form (the tiles of the last, partial wave
+ * shared out over at most 4 workers per tile, no range longer than a tile),
+ * 0 for the last two waves.  Writes out[0] = whole tiles computed first, out[1] = tiles
  * whose k-blocks are shared out (0 = no stream-K), out[2] = workers sharing
  * them, out[3] = most pieces one tile can be cut into.  Worker w of W takes
  * k-blocks [w*I/W, (w+1)*I/W) of the I = out[1]*kb shared ones.  Host-only

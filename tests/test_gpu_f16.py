@@ -11,7 +11,7 @@ from helpers import check, operands, padding_untouched, run, to_dev, torch
 pytestmark = pytest.mark.gpu
 
 AUTO, MANUAL, SPLITK = 0, 2, 3
-NO_TAIL, NO_PAIR, TAIL2, SK, SK_ALL = 5, 6, 9, 10, 11
+NO_TAIL, NO_PAIR, TAIL2, SK, SK_ALL, SKTAIL, HALVES = 5, 6, 9, 10, 11, 14, 15
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -202,7 +202,8 @@ def test_streams_are_respected():
 
 
 # ---------------------------------------------------------------- last-wave balancing
-@pytest.mark.parametrize("path,mark", [(AUTO, ".halves"), (TAIL2, ".tail"), (SK, ".sk")])
+@pytest.mark.parametrize("path,mark", [(AUTO, ".ktail"), (TAIL2, ".tail"), (SK, ".sk"),
+                                       (SKTAIL, ".sktail"), (HALVES, ".halves")])
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
     (2000, 2600, 4096, 4096, 2600, 2600),     # 176 tiles: the last 24 cut into 2 K slices
     (2000, 2600, 4100, 4104, 2600, 2600),     # ragged last k-block
@@ -212,9 +213,11 @@ def test_streams_are_respected():
 ])
 @pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
 def test_tail_parity(path, mark, M, N, K, lda, ldb, ldc, alpha, beta, c_fill):
-    """The last wave balanced by half-width units, by two K slices per tile or
-    by stream-K (shared k-block ranges); against the oracle and against whole
-    tiles."""
+    """The last wave balanced by two K slices per tile (the first one worker's
+    first unit, the second another worker's last), by two K slices run at the
+    end, by stream-K over the last two waves or over the last wave (each worker
+    runs the piece that starts a tile first and the piece that ends one last),
+    or by half-width units; against the oracle and against whole tiles."""
     A, B, C0 = operands(40 + M + N + lda, M, N, K, lda, ldb, ldc, np.float16, c_fill=c_fill)
     got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, lda, ldb, ldc, path=path)
     assert mark in taken, taken
@@ -230,7 +233,8 @@ def test_tail_parity(path, mark, M, N, K, lda, ldb, ldc, alpha, beta, c_fill):
     assert r["ok"], r
 
 
-@pytest.mark.parametrize("path,mark", [(AUTO, ".halves"), (TAIL2, ".tail"), (SK, ".sk")])
+@pytest.mark.parametrize("path,mark", [(AUTO, ".ktail"), (TAIL2, ".tail"), (SK, ".sk"),
+                                       (SKTAIL, ".sktail"), (HALVES, ".halves")])
 def test_tail_deterministic(path, mark):
     """Shared tiles are summed in k order whichever piece finishes last (and
     whether or not the finishing piece published its own partial sums), so
@@ -249,9 +253,14 @@ def test_tail_deterministic(path, mark):
 @pytest.mark.parametrize("M,N,K,path,mark", [
     (2000, 2600, 4096, SK, ".pair.bn256.tma.epi_tma.sk"),    # CTA pairs, last waves shared
     (2000, 2601, 2048, SK, ".epi_manual.sk"),                # N % 8 != 0, predicated epilogue
-    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 88 pair tiles: 12 halved
+    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_tma.ktail"),    # 88 pair tiles: 12 in two slices
+    (2000, 2600, 4096, SKTAIL, ".pair.bn256.tma.epi_tma.sktail"), # 12 shared out as stream-K
+    (4096, 4096, 4096, AUTO, ".pair.bn256.tma.epi_tma.ktail"),    # 256 pair tiles: 28 in two slices
+    (20000, 128, 4096, AUTO, ".bn128.tma.epi_tma.ktail"),         # 157 CTA tiles: 5 in two slices
+    (20000, 128, 2048, AUTO, ".bn128.tma.epi_tma.halves"),        # a shorter K: halved instead
     (2560, 2560, 1024, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 100 pair tiles: 24 halved
-    (2560, 2560, 1024, NO_PAIR, ".bn256.tma.epi_tma.halves"),     # 200 CTA tiles, halved tail
+    (2000, 2600, 4096, HALVES, ".pair.bn256.tma.epi_tma.halves"), # 88 pair tiles: 12 halved
+    (2560, 2560, 1024, NO_PAIR, ".bn256.tma.epi_tma.halves"),     # 200 CTA tiles
     (3300, 2001, 700, AUTO, ".epi_manual.halves"),                # predicated epilogue, halved
     (16, 8192, 8192, AUTO, ".bn128.tma.epi_tma.a32.sk"),   # skinny: every tile shared
     (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma.sk"),      # tall: every tile shared
@@ -393,3 +402,56 @@ def test_extreme_dimensions(M, N, K):
     A, B, C0 = operands(31337 + M + N, M, N, K, K, N, N, np.float16)
     got, taken = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
     check("f16", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+
+
+# ---------------------------------------------------------------- narrower CTA-pair tiles (224, 192)
+W224, W192 = 12, 13
+
+
+@pytest.mark.parametrize("width,path", [(224, W224), (192, W192)])
+@pytest.mark.parametrize("M,N,K,ldc", [
+    (512, 448, 128, 448),        # exactly two 224-wide tiles
+    (600, 1000, 300, 1000),      # ragged rows, columns and k-blocks
+    (257, 300, 640, 304),        # the second CTA of the last pair has one row; padded C
+    (1000, 1001, 700, 1001),     # N % 8 != 0: predicated epilogue
+    (4096, 4096, 512, 4096),     # several waves; the last column tile 64 (224) or 64 (192) wide
+])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
+def test_narrow_pair_tiles_parity(width, path, M, N, K, ldc, alpha, beta, c_fill):
+    """Pair tiles of 256 x 224 and 256 x 192: each CTA stages two whole
+    64-column boxes of B and the MMA reads the first 112 or 96 columns; the
+    epilogue splits the unit's 7 or 6 column chunks between two warps per row
+    quadrant."""
+    A, B, C0 = operands(70 + M + N + K + width, M, N, K, K, N, ldc, np.float16, c_fill=c_fill)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, ldc, path=path)
+    assert ".pair.bn%d." % width in taken, taken
+    big = M * N * K > 2e9
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, ldc,
+          rows=oracle.sample_rows(M) if big else None, cols=oracle.sample_cols(N) if big else None)
+    assert padding_untouched(got, C0, N)
+
+
+@pytest.mark.parametrize("path", [W224, W192])
+def test_narrow_pair_tiles_integers_exact(path):
+    M, N, K = 700, 900, 1000
+    rng = np.random.default_rng(path)
+    A = rng.integers(-1, 2, size=(M, K)).astype(np.float16)
+    B = rng.integers(-1, 2, size=(K, N)).astype(np.float16)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float16)
+    got, taken = run("f16", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=path)
+    assert ".pair.bn" in taken and ".bn256" not in taken, taken
+    ref = oracle.gemm(A, B, C0, 2.0, -1.0)
+    assert np.array_equal(got.view(np.uint16), _exact16(ref).view(np.uint16))
+
+
+def test_narrow_pair_tiles_match_256_wide_bitwise_on_integers():
+    """The same integer problem through 256-, 224- and 192-wide pair tiles gives
+    the same bits (every partial sum exact)."""
+    M, N, K = 1024, 1344, 512
+    rng = np.random.default_rng(3)
+    A = rng.integers(-2, 3, size=(M, K)).astype(np.float16)
+    B = rng.integers(-2, 3, size=(K, N)).astype(np.float16)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float16)
+    outs = [run("f16", A, B, C0, 1.0, 1.0, M, N, K, K, N, N, path=p)[0] for p in (NO_TAIL, W224, W192)]
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert np.array_equal(outs[0].view(np.uint16), outs[2].view(np.uint16))

@@ -47,8 +47,9 @@ def _c32(seed, M, ldc, fill="uniform"):
 
 @pytest.mark.parametrize("M,N,K,path,mark", [
     (256, 512, 128, AUTO, ".epi_f32"),
-    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_f32_tma.halves"),
+    (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_f32_tma.ktail"),
     (2000, 2601, 1024, AUTO, ".pair.bn256.tma.epi_f32.halves"),    # N % 4 != 0: direct stores
+    (2000, 2601, 4096, AUTO, ".pair.bn256.tma.epi_f32.ktail"),
     (2000, 2600, 2048, SK, ".pair.bn256.tma.epi_f32_tma.sk"),
     (16, 8192, 8192, AUTO, ".bn128.tma.epi_f32.a32.sk"),
     (48, 3000, 1500, AUTO, ".epi_f32.a64"),

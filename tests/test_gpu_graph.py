@@ -22,6 +22,8 @@ def _built():
     (16, 8192, 8192, AUTO, ".sk"),
     (300, 500, 3000, SPLITK, ".splitk"),
     (2000, 2600, 4096, TAIL2, ".tail"),
+    (2000, 2600, 4096, AUTO, ".ktail"),
+    (2000, 2600, 4096, 14, ".sktail"),
     (64, 128, 4096, SK_ALL, ".sk"),
 ])
 def test_graph_replays(M, N, K, path, mark):

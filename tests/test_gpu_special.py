@@ -82,7 +82,11 @@ PATHS = [
     (64, 128, 4096, 4096, 128, 128, SK_ALL, 0, ".sk"),
     (2000, 2600, 4096, 4096, 2600, 2600, SK, 0, ".pair.bn256.tma.epi_tma.sk"),
     (2000, 2600, 4096, 4096, 2600, 2600, TAIL2, 0, ".tail"),
-    (2560, 2560, 1024, 1024, 2560, 2560, AUTO, 0, ".pair.bn256.tma.epi_tma.halves"),
+    (2000, 2600, 4096, 4096, 2600, 2600, AUTO, 0, ".pair.bn256.tma.epi_tma.ktail"),
+    (2560, 2560, 1024, 1024, 2560, 2560, 15, 0, ".pair.bn256.tma.epi_tma.halves"),
+    (2000, 2600, 4096, 4096, 2600, 2600, 14, 0, ".pair.bn256.tma.epi_tma.sktail"),
+    (600, 1000, 300, 300, 1000, 1000, 12, 0, ".pair.bn224.tma.epi_tma"),
+    (600, 1001, 300, 300, 1001, 1001, 13, 0, ".pair.bn192.tma.epi_manual"),
     (16, 1000, 700, 700, 1000, 1000, AUTO, 0, ".a32"),
     (4096, 64, 2048, 2048, 64, 64, AUTO, 0, ".bn64.tma.epi_tma.sk"),
 ]
@@ -105,7 +109,7 @@ def test_overflow_rounds_to_inf_on_every_path(M, N, K, lda, ldb, ldc, path, spli
         assert np.isnan(got[:, N:]).all()
 
 
-@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,path,splits,mark", [PATHS[i] for i in (0, 1, 4, 6, 7, 10)])
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,path,splits,mark", [PATHS[i] for i in (0, 1, 4, 6, 7, 10, 11)])
 def test_infinite_operands_follow_ieee(M, N, K, lda, ldb, ldc, path, splits, mark):
     A, B, C0 = _operands(11 + M + N + K, M, N, K, lda, ldb, ldc)
     rng = np.random.default_rng(M * N)

@@ -102,3 +102,72 @@ def test_few_tiles_share_all_k_blocks():
 def test_null_out_is_an_error():
     L = g.lib()
     assert L.gemm_plan_stream_k(10, 10, 10, 0, None) == -1
+
+
+# ---------------------------------------------------------------- stream-K tail (publishers first)
+
+def _tail_pieces(plan, kb):
+    """Each worker's pieces as the kernel orders them with sk_order 1: the part
+    of its range that does not end a tile first, the part that ends one last.
+    Returns {worker: [(tile, kb0, kb1, ends_tile)]} in running order."""
+    iters = plan["sk_tiles"] * kb
+    W = plan["workers"]
+    out = {}
+    for w in range(W):
+        x0, x1 = _begin(w, iters, W), _begin(w + 1, iters, W)
+        tile_end = (x0 // kb + 1) * kb
+        seq = []
+        if x1 >= tile_end:
+            first, last = (tile_end, x1), (x0, tile_end)
+        else:
+            first, last = (x0, x1), None
+        if first[0] < first[1]:
+            s = first[0] // kb
+            seq.append((s, first[0] - s * kb, first[1] - s * kb, first[1] == (s + 1) * kb))
+        if last is not None:
+            s = last[0] // kb
+            seq.append((s, last[0] - s * kb, last[1] - s * kb, True))
+        out[w] = seq
+    return out
+
+
+TAIL_CASES = list(itertools.product([77, 100, 104, 152 + 1, 256, 300, 1000, 1024],   # tiles
+                                    [74, 76, 148, 152],                             # slots
+                                    [1, 4, 8, 13, 16, 64, 65, 128]))                 # k-blocks
+
+
+@pytest.mark.parametrize("tiles,slots,kb", TAIL_CASES)
+def test_tail_plan_partition(tiles, slots, kb):
+    """The tail form shares out exactly the last partial wave; every range is
+    no longer than a tile (so it ends at most one tile and starts at most one);
+    every k-block is covered once; each tile has one piece that ends it, run
+    last by its worker, and every other piece runs first."""
+    plan = g.plan_stream_k(tiles, slots, kb, tail=True)
+    rem = tiles % slots
+    if plan["sk_tiles"] == 0:
+        assert rem == 0 or tiles <= slots or kb < 8 or rem * kb < 4 * (rem + 1)
+        return
+    W = plan["workers"]
+    assert plan["sk_tiles"] == rem and plan["dp_tiles"] == tiles - rem
+    assert rem < W <= min(slots, 4 * rem)
+    iters = rem * kb
+    assert -(-iters // W) <= kb                 # no range longer than a tile
+    assert iters // W >= 4
+    covered = [[0] * kb for _ in range(rem)]
+    enders = [0] * rem
+    pieces_per_tile = [set() for _ in range(rem)]
+    for w, seq in _tail_pieces(plan, kb).items():
+        assert 1 <= len(seq) <= 2
+        for i, (s, k0, k1, ends) in enumerate(seq):
+            assert 0 <= k0 < k1 <= kb
+            for k in range(k0, k1):
+                covered[s][k] += 1
+            pieces_per_tile[s].add(w)
+            if ends:
+                enders[s] += 1
+                assert i == len(seq) - 1      # the finishing piece runs last
+            else:
+                assert i == 0                 # the others run first
+    assert all(c == 1 for row in covered for c in row)
+    assert enders == [1] * rem
+    assert max(len(x) for x in pieces_per_tile) <= plan["max_pieces"]
