@@ -11,9 +11,12 @@
 //      lda*2, ldb*2 are multiples of 16 bytes (the run-time alignment check
 //      of the "advanced SGEMM" page, kernel selection section, extended to
 //      the 16-byte rule of TMA); an operand that breaks it is first copied to
-//      16-byte rows (one launch for both), else predicated element loads
+//      16-byte rows (one launch for all), else predicated element loads
 //   5. epilogue: TMA for a half C under the same rule when N is a multiple of
-//      8, else predicated accesses; a float C is written from registers
+//      8; otherwise C is copied to 16-byte rows in the same launch (when
+//      beta != 0), the TMA epilogue writes the copy and a last kernel copies
+//      it back; predicated accesses when that is forced or too large; a float
+//      C is written from registers
 //   6. few tiles for many SMs with a long K: stream-K over all tiles when it
 //      is expected to beat half-width units (few_tiles_prefer_stream_k)
 //   7. CTA pairs (256 x 256 tiles) for 256-wide TMA shapes with at least two
@@ -506,54 +509,75 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   if (bn == 256 && M <= kBM && 1ll * ((N + 255) / 256) * 2 <= d->sm_count) bn = 128;
   const bool a_tma = aligned16(A) && (lda * 2) % 16 == 0;
   const bool b_tma = aligned16(B) && (ldb * 2) % 16 == 0;
+  // A TMA store writes whole 16-byte pieces of a row: when N is not a multiple
+  // of 8 halves it would also write the elements just past column N (measured
+  // on GB300), which may belong to the caller.
+  bool c_tma = !c_f32 && aligned16(C) && (ldc * 2) % 16 == 0 && N % 8 == 0;
   // An operand whose rows break the 16-byte rule is first copied into an
-  // aligned layout (one bandwidth-bound pass) unless the predicated-load path
-  // is forced or the copy would be very large.
+  // aligned layout (one bandwidth-bound launch for all of them) unless the
+  // predicated path is forced or the copies would be very large.  Such a half
+  // C is copied in (when beta != 0), written by the TMA epilogue into its
+  // aligned copy (rows padded to a multiple of 8, so the pieces past N land
+  // in the padding) and copied back by a last kernel.
   const char* how = "";
-  if ((!a_tma || !b_tma) && force != 2) {
-    const long long lda2 = (K + 7) / 8 * 8, ldb2 = (N + 7) / 8 * 8;
-    const size_t a_bytes = a_tma ? 0 : static_cast<size_t>(M) * lda2 * 2;
-    const size_t b_bytes = b_tma ? 0 : static_cast<size_t>(K) * ldb2 * 2;
-    if (a_bytes + b_bytes <= (static_cast<size_t>(1) << 31)) {
+  bool prepass = false;         // a realignment kernel was launched just before the GEMM
+  uint16_t* c_user = nullptr;   // the caller's C when the GEMM writes an aligned copy
+  long long ldc_user = 0;
+  if ((!a_tma || !b_tma || (!c_f32 && !c_tma)) && force != 2) {
+    const long long lda2 = (K + 7) / 8 * 8, ldb2 = (N + 7) / 8 * 8, ldc2 = (N + 7) / 8 * 8;
+    auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t a_bytes = a_tma ? 0 : round256(static_cast<size_t>(M) * lda2 * 2);
+    const size_t b_bytes = b_tma ? 0 : round256(static_cast<size_t>(K) * ldb2 * 2);
+    const size_t c_bytes = (c_f32 || c_tma) ? 0 : round256(static_cast<size_t>(M) * ldc2 * 2);
+    if (a_bytes + b_bytes + c_bytes <= (static_cast<size_t>(1) << 31)) {
       std::lock_guard<std::mutex> lk(g_mu);
       StreamWs& w = d->ws[reinterpret_cast<uintptr_t>(stream)];
-      if (int rc = ensure_buffer(&w.realigned, &w.realigned_bytes, a_bytes + b_bytes + 256))
+      if (int rc = ensure_buffer(&w.realigned, &w.realigned_bytes, a_bytes + b_bytes + c_bytes))
         return rc;
-      uint16_t* buf = static_cast<uint16_t*>(w.realigned);
-      // one launch copies whichever of A and B breaks the rule
-      RealignJob jobs[2];
-      int grids[2];
-      int njobs = 0;
+      uint8_t* buf = static_cast<uint8_t*>(w.realigned);
+      RealignBatch batch{};
+      auto add = [&](const RealignJob& j, long long groups) {
+        batch.job[batch.n] = j;
+        batch.end[batch.n] = (batch.n ? batch.end[batch.n - 1] : 0) + scale_grid(*d, groups);
+        ++batch.n;
+      };
       if (!a_tma) {
-        jobs[njobs] = RealignJob{A, lda, buf, lda2, M, K};
-        grids[njobs++] = scale_grid(*d, 1ll * M * lda2 / 8);
-        A = buf;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(buf);
+        add(RealignJob{A, lda, dst, lda2, M, K}, 1ll * M * lda2 / 8);
+        A = dst;
         lda = lda2;
-        buf += (a_bytes / 2 + 127) / 128 * 128;   // keep the next copy 256-byte aligned
+        buf += a_bytes;
       }
       if (!b_tma) {
-        jobs[njobs] = RealignJob{B, ldb, buf, ldb2, K, N};
-        grids[njobs++] = scale_grid(*d, 1ll * K * ldb2 / 8);
-        B = buf;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(buf);
+        add(RealignJob{B, ldb, dst, ldb2, K, N}, 1ll * K * ldb2 / 8);
+        B = dst;
         ldb = ldb2;
+        buf += b_bytes;
       }
-      if (launch_realign_f16(jobs[0], njobs > 1 ? &jobs[1] : nullptr, grids[0],
-                             njobs > 1 ? grids[1] : 0, stream) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-      how = ".realigned";
+      if (c_bytes) {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(buf);
+        if (beta != 0.0f)
+          add(RealignJob{static_cast<uint16_t*>(C), ldc, dst, ldc2, M, N}, 1ll * M * ldc2 / 8);
+        c_user = static_cast<uint16_t*>(C);
+        ldc_user = ldc;
+        C = dst;
+        ldc = ldc2;
+        c_tma = true;
+      }
+      if (batch.n > 0) {
+        if (launch_realign_f16(batch, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        prepass = true;
+      }
+      how = c_user ? (batch.n > 0 ? ".realigned.c" : ".c") : ".realigned";
     }
   }
   const bool ab_tma = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
-  // A TMA store writes whole 16-byte pieces of a row: when N is not a multiple
-  // of 8 halves it would also write the elements just past column N (measured
-  // on GB300), which may belong to the caller.  Such shapes take the predicated
-  // epilogue.
-  const bool c_tma = !c_f32 && aligned16(C) && (ldc * 2) % 16 == 0 && N % 8 == 0;
   int load = (ab_tma && force != 2) ? kLoadTma : kLoadManual;
   int epi = c_f32 ? kEpiF32 : ((c_tma && force != 2) ? kEpiTma : kEpiManual);
 
   TcArgs a{};
-  a.pdl = *how != '\0';   // the realignment copy was launched just before
+  a.pdl = prepass;   // the realignment copy was launched just before
   a.A = A;
   a.B = B;
   a.C = c_f32 ? nullptr : static_cast<uint16_t*>(C);
@@ -756,6 +780,15 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
     // the same 64-byte rows: 32 rows x 16 floats
     if (int rc = make_map_f32(&tmC, a.Cf, M, N, ldc, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
   }
+  // a C with rows off the 16-byte grid: the kernel wrote its aligned copy,
+  // which goes back to the caller's C last
+  auto copy_back = [&]() -> int {
+    if (!c_user) return GEMM_OK;
+    const RealignJob j{a.C, ldc, c_user, ldc_user, M, N};
+    return launch_unalign_f16(j, scale_grid(*d, 1ll * M * (N / 8 + 2)), stream) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+  };
   // one CTA (pair) per worker; with stream-K over all tiles or the last waves
   // exactly sk_workers of them, with the stream-K tail every worker
   const long long nw = a.sk_tiles > 0 ? (a.sk_order ? workers : a.sk_workers)
@@ -769,7 +802,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
     t_last_path = t_path_buf;
     if (launch_gemm_f16_tc_pair(bn, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
-    return GEMM_OK;
+    return copy_back();
   }
   const int grid = static_cast<int>(nw);
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
@@ -784,7 +817,8 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   const cudaError_t e = am < kBM
                             ? launch_gemm_f16_tc_skinny(am, epi, tmA, tmB, tmC, a, grid, stream)
                             : launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream);
-  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  if (e != cudaSuccess) return GEMM_ERR_CUDA;
+  return copy_back();
 }
 
 int gemm_f16_device(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K,

@@ -2,7 +2,8 @@
 //   * split-K reduction: C = half(alpha * sum_s P_s + beta * C), slices summed
 //     in ascending order (deterministic), fp32 arithmetic, one rounding;
 //   * realignment of an operand whose rows are not 16-byte aligned into an
-//     aligned copy, so that the tensor-core kernel can load it by TMA;
+//     aligned copy, so that the tensor-core kernel can load it by TMA, and the
+//     copy of such a C back from the aligned copy the kernel wrote by TMA;
 //   * the big/small tf32 split of fp32 operands for the 3xTF32 SGEMM;
 //   * scale-only update for alpha == 0 or K == 0: C := beta*C (C := 0 when
 //     beta == 0, without reading C -- the convention of the "LeetGPU GEMM T4"
@@ -134,20 +135,53 @@ __device__ __forceinline__ void realign_rows(const uint16_t* __restrict__ src, l
   }
 }
 
-// Both operands in one launch: blocks [0, grid_a) copy the first, the others
-// the second (rows2 == 0: none).
-__global__ void realign_f16_kernel(const uint16_t* __restrict__ src1, long long lds1,
-                                   uint16_t* __restrict__ dst1, long long ldd1, int rows1, int cols1,
-                                   const uint16_t* __restrict__ src2, long long lds2,
-                                   uint16_t* __restrict__ dst2, long long ldd2, int rows2, int cols2,
-                                   int grid_1) {
-  if (static_cast<int>(blockIdx.x) < grid_1)
-    realign_rows(src1, lds1, dst1, ldd1, rows1, cols1, blockIdx.x, grid_1);
-  else
-    realign_rows(src2, lds2, dst2, ldd2, rows2, cols2, blockIdx.x - grid_1, gridDim.x - grid_1);
+// Up to three copies in one launch: blocks [end[i-1], end[i]) copy job i.
+__global__ void realign_f16_kernel(const RealignBatch b) {
+  int i = 0;
+  while (i + 1 < b.n && static_cast<int>(blockIdx.x) >= b.end[i]) ++i;
+  const int first = i ? b.end[i - 1] : 0;
+  const RealignJob& j = b.job[i];
+  realign_rows(j.src, j.lds, j.dst, j.ldd, j.rows, j.cols, blockIdx.x - first, b.end[i] - first);
   // this block's copies are issued: the GEMM launched next may be scheduled
   // (it waits for this kernel's completion before reading the copies)
   griddep_launch_dependents();
+}
+
+// dst[r][c] := src[r][c] for c < cols; src rows 16-byte aligned with
+// lds >= cols rounded up to 8, dst rows at any 2-byte alignment.  One thread
+// writes one 16-byte-aligned piece of a destination row, so that a warp's
+// stores are contiguous: a piece inside the row's columns with one 16-byte
+// store (its 8 halves read as the two aligned 16-byte blocks of the source
+// row that hold them, which lie within the row's lds, and shifted into
+// place), the pieces at the two ends of the row element by element (nothing
+// outside the row's columns is written).
+__global__ void unalign_f16_kernel(const uint16_t* __restrict__ src, long long lds,
+                                   uint16_t* __restrict__ dst, long long ldd, int rows, int cols) {
+  griddep_wait();   // the kernel that writes src may still be running
+  const long long pieces = cols / 8 + 2;   // enough for any alignment of a row
+  const long long total = static_cast<long long>(rows) * pieces;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(g / pieces);
+    const int j = static_cast<int>(g % pieces);
+    uint16_t* const d = dst + static_cast<long long>(r) * ldd;
+    const int md = static_cast<int>(reinterpret_cast<uintptr_t>(d) & 15u);   // even
+    const int e0 = 8 * j - md / 2;   // first element of the row in piece j
+    if (e0 >= cols) continue;
+    const uint16_t* const s = src + static_cast<long long>(r) * lds;
+    if (e0 >= 0 && e0 + 8 <= cols) {
+      const uint4* const blk = reinterpret_cast<const uint4*>(s + (e0 & ~7));
+      const uint32_t m = static_cast<uint32_t>(e0 & 7) * 2u;
+      const uint4 v = (m == 0) ? __ldg(blk) : shift_bytes(__ldg(blk), __ldg(blk + 1), m);
+      __stcs(reinterpret_cast<uint4*>(d + e0), v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = e0 + i;
+        if (e >= 0 && e < cols) d[e] = __ldg(s + e);
+      }
+    }
+  }
 }
 
 // tf32 value nearest to x (ties away from zero), as fp32 bits with the low 13
@@ -336,13 +370,25 @@ cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float
 }
 
 
-cudaError_t launch_realign_f16(const RealignJob& first, const RealignJob* second, int grid_1,
-                               int grid_2, cudaStream_t stream) {
-  const RealignJob none{};
-  const RealignJob& b = second ? *second : none;
-  realign_f16_kernel<<<grid_1 + (second ? grid_2 : 0), 256, 0, stream>>>(
-      first.src, first.lds, first.dst, first.ldd, first.rows, first.cols, b.src, b.lds, b.dst, b.ldd,
-      b.rows, b.cols, grid_1);
+cudaError_t launch_realign_f16(const RealignBatch& batch, cudaStream_t stream) {
+  if (batch.n < 1 || batch.n > 3) return cudaErrorInvalidValue;
+  realign_f16_kernel<<<batch.end[batch.n - 1], 256, 0, stream>>>(batch);
+  return counted_launch(cudaGetLastError());
+}
+
+cudaError_t launch_unalign_f16(const RealignJob& job, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, unalign_f16_kernel, static_cast<const uint16_t*>(job.src),
+                                           job.lds, job.dst, job.ldd, job.rows, job.cols);
+  if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());
 }
 

@@ -545,6 +545,9 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   // here on global memory is read and written, once a pre-pass launched just
   // before this kernel has completed
   griddep_wait();
+  // a copy-back kernel launched after this one may be scheduled now (it waits
+  // for this kernel's completion before reading anything this kernel writes)
+  griddep_launch_dependents();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + L::kTmemPtrOff);
 
   const unsigned long long limit = p.wait_limit_ns;

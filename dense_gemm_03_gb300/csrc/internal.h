@@ -156,10 +156,19 @@ struct RealignJob {
   long long ldd;
   int rows, cols;
 };
-// One launch for one or two copies (second may be null): grid_1 blocks on the
-// first, grid_2 on the second.
-cudaError_t launch_realign_f16(const RealignJob& first, const RealignJob* second, int grid_1,
-                               int grid_2, cudaStream_t stream);
+// One launch for up to three copies: blocks [end[i-1], end[i]) copy jobs[i].
+struct RealignBatch {
+  RealignJob job[3];
+  int end[3];
+  int n;
+};
+cudaError_t launch_realign_f16(const RealignBatch& batch, cudaStream_t stream);
+
+// The copy back: dst (rows x cols, any 2-byte alignment and leading dimension
+// ldd) := src (16-byte-aligned rows, lds >= cols rounded up to 8).  Launched
+// after the kernel that writes src, which it may overlap (programmatic
+// dependent launch; it waits for that kernel's completion before reading).
+cudaError_t launch_unalign_f16(const RealignJob& job, int grid, cudaStream_t stream);
 
 // Both splits of a 3xTF32 product in one launch: A (M x K) into Ab, As and
 // B^T (B is K x N) into Bb, Bs, all with leading dimension ld2 (>= K, % 4 == 0);

@@ -98,7 +98,8 @@ def test_leading_dimensions(M, N, K, lda, ldb, ldc, alpha, beta):
 
 
 def test_misaligned_base_pointers():
-    """Operands starting 2 bytes past a 16-byte boundary take the predicated path."""
+    """Operands starting 2 bytes past a 16-byte boundary: A and B go through
+    aligned copies, and C through an aligned copy that is copied back."""
     t = torch()
     M, N, K = 150, 200, 90
     A, B, C0 = operands(31, M, N, K, K, N, N, np.float16)
@@ -109,7 +110,7 @@ def test_misaligned_base_pointers():
     es = bufs[0].element_size()
     g.gemm_f16(bufs[0].data_ptr() + es, bufs[1].data_ptr() + es, bufs[2].data_ptr() + es,
                1.5, 0.5, M=M, N=N, K=K)
-    assert "manual" in g.last_path()
+    assert g.last_path().endswith(".realigned.c"), g.last_path()
     t.cuda.synchronize()
     got = bufs[2][1:1 + C0.size].cpu().numpy().reshape(M, N)
     check("f16", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
@@ -252,7 +253,7 @@ def test_tail_deterministic(path, mark):
 
 @pytest.mark.parametrize("M,N,K,path,mark", [
     (2000, 2600, 4096, SK, ".pair.bn256.tma.epi_tma.sk"),    # CTA pairs, last waves shared
-    (2000, 2601, 2048, SK, ".epi_manual.sk"),                # N % 8 != 0, predicated epilogue
+    (2000, 2601, 2048, SK, ".epi_tma.sk.realigned.c"),      # N % 8 != 0: C through an aligned copy
     (2000, 2600, 4096, AUTO, ".pair.bn256.tma.epi_tma.ktail"),    # 88 pair tiles: 12 in two slices
     (2000, 2600, 4096, SKTAIL, ".pair.bn256.tma.epi_tma.sktail"), # 12 shared out as stream-K
     (4096, 4096, 4096, AUTO, ".pair.bn256.tma.epi_tma.ktail"),    # 256 pair tiles: 28 in two slices
@@ -261,7 +262,8 @@ def test_tail_deterministic(path, mark):
     (2560, 2560, 1024, AUTO, ".pair.bn256.tma.epi_tma.halves"),   # 100 pair tiles: 24 halved
     (2000, 2600, 4096, HALVES, ".pair.bn256.tma.epi_tma.halves"), # 88 pair tiles: 12 halved
     (2560, 2560, 1024, NO_PAIR, ".bn256.tma.epi_tma.halves"),     # 200 CTA tiles
-    (3300, 2001, 700, AUTO, ".epi_manual.halves"),                # predicated epilogue, halved
+    (3300, 2001, 700, AUTO, ".halves.realigned.c"),               # every operand realigned, halved
+    (3300, 2001, 700, MANUAL, ".manual.epi_manual"),              # predicated loads and epilogue
     (16, 8192, 8192, AUTO, ".bn128.tma.epi_tma.a32.sk"),   # skinny: every tile shared
     (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma.sk"),      # tall: every tile shared
     (64, 128, 4096, SK_ALL, ".sk"),                      # one tile cut into 16 pieces
@@ -353,7 +355,7 @@ def test_realigned_base_offsets(offset_elems, M, N, K):
     es = 2
     g.gemm_f16(bufs[0].data_ptr() + es * offset_elems, bufs[1].data_ptr() + es * offset_elems, dC,
                0.75, -0.25, M=M, N=N, K=K)
-    assert g.last_path().endswith(".realigned"), g.last_path()
+    assert ".realigned" in g.last_path(), g.last_path()
     t.cuda.synchronize()
     check("f16", dC.cpu().numpy(), A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
 
@@ -378,7 +380,7 @@ def test_odd_pointers_are_rejected():
     (32, 1000, 700, ".a32"),
     (33, 1000, 700, ".a64"),
     (64, 4096, 1024, ".a64"),
-    (17, 1001, 513, ".epi_manual.a32"),     # N % 8 != 0: predicated epilogue
+    (17, 1001, 513, ".a32"),                # N % 8 != 0: C through an aligned copy
 ])
 @pytest.mark.parametrize("alpha,beta,c_fill", [(1.5, 0.5, "uniform"), (1.0, 0.0, "nan")])
 def test_skinny_parity(M, N, K, mark, alpha, beta, c_fill):
@@ -455,3 +457,38 @@ def test_narrow_pair_tiles_match_256_wide_bitwise_on_integers():
     outs = [run("f16", A, B, C0, 1.0, 1.0, M, N, K, K, N, N, path=p)[0] for p in (NO_TAIL, W224, W192)]
     assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
     assert np.array_equal(outs[0].view(np.uint16), outs[2].view(np.uint16))
+
+
+# ---------------------------------------------------------------- C off the 16-byte grid: copied back
+@pytest.mark.parametrize("offset_elems", [1, 3, 7])
+@pytest.mark.parametrize("M,N,ldc", [(300, 1000, 1003), (257, 9, 13), (64, 1, 1), (130, 520, 523),
+                                     (600, 1024, 1025)])
+@pytest.mark.parametrize("beta", [0.5, 0.0])
+def test_unaligned_c_copied_back(offset_elems, M, N, ldc, beta):
+    """C starts 2, 6 or 14 bytes past a 16-byte boundary with an odd leading
+    dimension: the kernel writes an aligned copy by TMA and a last kernel
+    copies it back.  Every element outside C's columns -- before its first
+    row, between its rows and after its last row -- keeps its sentinel."""
+    import dense_gemm_03_gb300 as g
+    t = torch()
+    K = 200
+    A, B, C0 = operands(90 + offset_elems + M + N, M, N, K, K, N, ldc, np.float16)
+    pad = 64
+    buf = np.full(C0.size + 2 * pad, np.nan, dtype=np.float16)
+    buf.view(np.uint16)[:] = 0x7E55
+    buf[pad + offset_elems:pad + offset_elems + C0.size] = C0.reshape(-1)
+    dbuf = to_dev(buf)
+    dA, dB = to_dev(A), to_dev(B)
+    g.gemm_f16(dA, dB, dbuf.data_ptr() + 2 * (pad + offset_elems), 0.75, beta, M=M, N=N, K=K,
+               lda=K, ldb=N, ldc=ldc)
+    assert g.last_path().endswith(".c"), g.last_path()
+    t.cuda.synchronize()
+    assert g.debug_status() == 0
+    out = dbuf.cpu().numpy()
+    got = out[pad + offset_elems:pad + offset_elems + C0.size].reshape(M, ldc)
+    check("f16", got, A, B, C0, 0.75, beta, M, N, K, K, N, ldc)
+    assert padding_untouched(got, C0, N)
+    ref_bits = buf.view(np.uint16)
+    out_bits = out.view(np.uint16)
+    assert np.array_equal(out_bits[:pad + offset_elems], ref_bits[:pad + offset_elems])
+    assert np.array_equal(out_bits[pad + offset_elems + C0.size:], ref_bits[pad + offset_elems + C0.size:])

@@ -73,9 +73,10 @@ def _same_bits_or_both_nan(got, want):
 # (M, N, K, lda, ldb, ldc, forced path, splits, mark in the reported path)
 PATHS = [
     (512, 512, 64, 64, 512, 512, NO_TAIL, 0, ".pair.bn256.tma.epi_tma"),
-    (512, 1001, 64, 64, 1001, 1001, NO_TAIL, 0, ".pair.bn256.tma.epi_manual"),
+    (512, 1001, 64, 64, 1001, 1001, NO_TAIL, 0, ".pair.bn256.tma.epi_tma.realigned.c"),
     (300, 384, 64, 64, 384, 384, NO_PAIR, 0, ".bn256.tma.epi_tma"),
-    (300, 100, 200, 200, 100, 100, AUTO, 0, ".bn128.tma.epi_manual"),
+    (300, 100, 200, 200, 100, 100, AUTO, 0, ".bn128.tma.epi_tma.halves.realigned.c"),
+    (300, 1001, 200, 200, 1001, 1001, MANUAL, 0, ".manual.epi_manual"),
     (300, 400, 200, 200, 400, 400, MANUAL, 0, ".manual."),
     (300, 520, 200, 201, 520, 523, AUTO, 0, ".realigned"),
     (200, 300, 1024, 1024, 300, 300, SPLITK, 3, ".splitk"),
@@ -86,7 +87,7 @@ PATHS = [
     (2560, 2560, 1024, 1024, 2560, 2560, 15, 0, ".pair.bn256.tma.epi_tma.halves"),
     (2000, 2600, 4096, 4096, 2600, 2600, 14, 0, ".pair.bn256.tma.epi_tma.sktail"),
     (600, 1000, 300, 300, 1000, 1000, 12, 0, ".pair.bn224.tma.epi_tma"),
-    (600, 1001, 300, 300, 1001, 1001, 13, 0, ".pair.bn192.tma.epi_manual"),
+    (600, 1001, 300, 300, 1001, 1001, 13, 0, ".pair.bn192.tma.epi_tma"),
     (16, 1000, 700, 700, 1000, 1000, AUTO, 0, ".a32"),
     (4096, 64, 2048, 2048, 64, 64, AUTO, 0, ".bn64.tma.epi_tma.sk"),
 ]
@@ -109,7 +110,7 @@ def test_overflow_rounds_to_inf_on_every_path(M, N, K, lda, ldb, ldc, path, spli
         assert np.isnan(got[:, N:]).all()
 
 
-@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,path,splits,mark", [PATHS[i] for i in (0, 1, 4, 6, 7, 10, 11)])
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,path,splits,mark", [PATHS[i] for i in (0, 1, 4, 5, 7, 8, 11, 12)])
 def test_infinite_operands_follow_ieee(M, N, K, lda, ldb, ldc, path, splits, mark):
     A, B, C0 = _operands(11 + M + N + K, M, N, K, lda, ldb, ldc)
     rng = np.random.default_rng(M * N)
