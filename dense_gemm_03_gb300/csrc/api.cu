@@ -753,6 +753,11 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
       a.sk_tiles = static_cast<int>(sk.sk_tiles);
       a.sk_workers = static_cast<int>(sk.workers);
       a.sk_iters = sk.sk_tiles * a.kb_total;
+      // no range longer than a tile (fewer tiles than workers): each worker
+      // runs the piece that starts a tile first and the piece that ends one
+      // last, so a tile's finishing piece finds the others published (and
+      // brings their partial sums into L2 while its own main loop runs)
+      a.sk_order = sk.sk_tiles <= sk.workers ? 1 : 0;
       a.tail_splits = static_cast<int>(sk.max_pieces);
       workers = sk.workers;
       if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
