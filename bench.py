@@ -894,6 +894,44 @@ def run_sweep_f16(args):
                       "auto_best": best_is_auto, "auto_within_2pct": within, "clocks": clocks}))
 
 
+# ---------------------------------------------------------------- profiler cases
+
+def run_ncu_case(case):
+    """One workload of the line, five calls with the L2 flushed before each and
+    nothing else: the program a profiler capture of one kernel attaches to."""
+    import torch
+    import dense_gemm_03_gb300 as g
+    import synthetic
+    from dense_gemm_03_gb300 import build as _b
+    _b.build()
+    torch.cuda.set_device(0)
+    if case in ("f16", "f32", "ffma"):
+        dt = np.float16 if case == "f16" else np.float32
+        seed = synthetic.config_seed(2 if case == "f16" else 1)
+        A, _ = _fill_device((4096, 4096), dt, seed, synthetic.STREAM_A)
+        B, _ = _fill_device((4096, 4096), dt, seed, synthetic.STREAM_B)
+        C, _ = _fill_device((4096, 4096), dt, seed, synthetic.STREAM_C)
+        if case == "f16":
+            fn = lambda: g.gemm_f16(A, B, C, F16_CFG["alpha"], F16_CFG["beta"])
+        else:
+            fn = lambda: g.sgemm_f32(A, B, C, 1.0, 0.0)
+        if case == "ffma":
+            g.force_path(PATH_FFMA_ONLY)
+    else:
+        sM, sN, sK, slda, alpha, beta, _ = EDGE_SHAPES[["edge", "skinny", "tall"].index(case)]
+        seed = synthetic.config_seed(4)
+        A, _ = _fill_device((sM * slda,), np.float16, seed, synthetic.STREAM_A)
+        B, _ = _fill_device((sK, sN), np.float16, seed, synthetic.STREAM_B)
+        C, _ = _fill_device((sM, sN), np.float16, seed, synthetic.STREAM_C)
+        fn = lambda: g.gemm_f16(A, B, C, alpha, beta, M=sM, N=sN, K=sK, lda=slda, ldb=sN, ldc=sN)
+    for _ in range(5):
+        g.l2_flush(0)
+        fn()
+    torch.cuda.synchronize()
+    assert g.debug_status() == 0
+    print(json.dumps({"ncu_case": case, "kernel_path": g.last_path()}))
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -911,6 +949,10 @@ def main():
                     help="skip measuring the dense tf32 rate (3xTF32 denominator)")
     ap.add_argument("--f32-ffma", action="store_true",
                     help="time the fp32 leg on the CUDA-core FFMA kernel instead of 3xTF32")
+    ap.add_argument("--ncu-case", choices=["f16", "f32", "ffma", "skinny", "tall", "edge"],
+                    default=None,
+                    help="run one workload five times (L2 flushed before each) and exit: the "
+                         "small case a profiler capture attaches to")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-f16", action="store_true",
                     help="fp16 sweep: the automatic path beside the forced alternatives")
@@ -920,6 +962,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
