@@ -26,9 +26,10 @@
 //      ends a tile last, plan_tail_stream_k) when that is expected to beat two
 //      half-width units per tile, which are used otherwise when the halves fit
 //      in one wave
-// The fp32 GEMM (sgemm_f32_ld) takes the 3xTF32 tensor-core path for
-// K >= 64 (with K slices when few tiles meet a long K, plan_tf32_slices),
-// else the FFMA kernel.
+// The fp32 GEMM (sgemm_f32_ld) takes the tensor-core path for K >= 64: three
+// products of operands split into two scaled half parts (3xFP16; 3xTF32 with
+// tf32 parts when forced), with K slices when few tiles meet a long K
+// (plan_tf32_slices); else the FFMA kernel.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -848,47 +849,96 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
                : GEMM_ERR_CUDA;
   }
   const int force = g_force_path.load();
-  // 3xTF32 on the tensor cores whenever K has at least two 32-deep k-blocks:
-  // measured faster than the FFMA kernel at every M and N tried, skinny and
-  // tiny shapes included (16 x 8192 x 8192: 274 us against 830 us; 128^3:
-  // 14 us against 18 us); a shorter K stays on the FFMA kernel.
-  if (force != 4 && force != 7 && (force == 8 || K >= 64)) {
+  // Three tensor-core products of split operands whenever K has at least 64
+  // elements: measured faster than the FFMA kernel at every M and N tried,
+  // skinny and tiny shapes included (3xTF32: 16 x 8192 x 8192 274 us against
+  // 830 us; 128^3: 14 us against 18 us); a shorter K stays on the FFMA kernel.
+  // The parts are scaled halves (3xFP16, twice the tf32 rate) unless 3xTF32 is
+  // forced (path 8); path 16 forces 3xFP16.
+  if (force != 4 && force != 7 && (force == 8 || force == 16 || K >= 64)) {
+    const bool x16 = force != 8;
     const int pairs = sgemm_3xtf32_max_pairs();
+    auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
     const long long K2 = (K + 3) / 4 * 4;
-    const size_t a_part = static_cast<size_t>(M) * K2 * 4, b_part = static_cast<size_t>(N) * K2 * 4;
-    if (pairs > 0 && 2 * (a_part + b_part) <= (static_cast<size_t>(16) << 30)) {
-      float* buf = nullptr;
+    const long long lda2 = (K + 7) / 8 * 8, ldb2 = (N + 7) / 8 * 8;
+    const size_t a_part = x16 ? round256(static_cast<size_t>(M) * lda2 * 2)
+                              : static_cast<size_t>(M) * K2 * 4;
+    const size_t b_part = x16 ? round256(static_cast<size_t>(K) * ldb2 * 2)
+                              : static_cast<size_t>(N) * K2 * 4;
+    const size_t e_bytes = x16 ? round256(static_cast<size_t>(M) * 4) +
+                                     2 * round256((static_cast<size_t>(N) + 8) * 4)
+                               : 0;
+    const size_t need = 2 * (a_part + b_part) + e_bytes + 1024;
+    if (pairs > 0 && need <= (static_cast<size_t>(16) << 30)) {
+      uint8_t* buf = nullptr;
       {
         std::lock_guard<std::mutex> lk(g_mu);
         StreamWs& w = d->ws[reinterpret_cast<uintptr_t>(stream)];
-        if (int rc = ensure_buffer(&w.split, &w.split_bytes, 2 * (a_part + b_part) + 1024))
-          return rc;
-        buf = static_cast<float*>(w.split);
+        if (int rc = ensure_buffer(&w.split, &w.split_bytes, need)) return rc;
+        buf = static_cast<uint8_t*>(w.split);
       }
-      float* Ab = buf;
-      float* As = Ab + a_part / 4;
-      float* Bb = As + a_part / 4;
-      float* Bs = Bb + b_part / 4;
-      // one launch splits both operands, the blocks shared in proportion to the bytes
-      const long long ttiles = ((K2 + 31) / 32) * ((N + 31) / 32);
-      const int grid_a = scale_grid(*d, 1ll * M * K2 / 4);
-      const int grid_b = static_cast<int>(std::min<long long>(ttiles, 8ll * d->sm_count));
-      if (launch_split_tf32_ab(A, lda, Ab, As, B, ldb, Bb, Bs, K2, M, N, K, grid_a, grid_b,
-                               stream) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-      CUtensorMap mAb{}, mAs{}, mBb{}, mBs{}, mBbh{}, mBsh{};
-      if (int rc = make_map_f32(&mAb, Ab, M, K, K2, 32, 128)) return rc;
-      if (int rc = make_map_f32(&mAs, As, M, K, K2, 32, 128)) return rc;
-      if (int rc = make_map_f32(&mBb, Bb, N, K, K2, 32, 128)) return rc;
-      if (int rc = make_map_f32(&mBs, Bs, N, K, K2, 32, 128)) return rc;
-      if (int rc = make_map_f32(&mBbh, Bb, N, K, K2, 32, 64)) return rc;
-      if (int rc = make_map_f32(&mBsh, Bs, N, K, K2, 32, 64)) return rc;
       Tf32Args t{};
       t.pdl = true;   // the split pre-pass was launched just before
-      t.Ab = Ab;
-      t.As = As;
-      t.Bb = Bb;
-      t.Bs = Bs;
+      CUtensorMap m1{}, m2{}, m3{}, m4{}, m5{}, m6{};
+      if (x16) {
+        F16x3Parts parts{};
+        parts.A1 = reinterpret_cast<uint16_t*>(buf);
+        parts.A2 = reinterpret_cast<uint16_t*>(buf + a_part);
+        parts.B1 = reinterpret_cast<uint16_t*>(buf + 2 * a_part);
+        parts.B2 = reinterpret_cast<uint16_t*>(buf + 2 * a_part + b_part);
+        uint8_t* const eptr = buf + 2 * (a_part + b_part);
+        parts.ea = reinterpret_cast<int*>(eptr);
+        parts.eb = reinterpret_cast<int*>(eptr + round256(static_cast<size_t>(M) * 4));
+        parts.colmax = reinterpret_cast<unsigned int*>(
+            eptr + round256(static_cast<size_t>(M) * 4) + round256((static_cast<size_t>(N) + 8) * 4));
+        parts.lda2 = lda2;
+        parts.ldb2 = ldb2;
+        // first launch: one block per row of A, and B's column maxima over
+        // bands of 16 rows; second: B's parts, 4 columns per thread over a
+        // share of rows
+        const int grid_a = static_cast<int>(std::min<long long>(M, 8ll * d->sm_count));
+        const int grid_bmax = scale_grid(*d, ((N + 3) / 4) * ((K + 15) / 16ll));
+        const int grid_b = scale_grid(*d, ((N + 3) / 4) * static_cast<long long>(K));
+        if (launch_f16x3_split(A, lda, B, ldb, parts, M, N, K, grid_a, grid_bmax, grid_b, stream) !=
+            cudaSuccess)
+          return GEMM_ERR_CUDA;
+        // k-blocks of 32 halves: A parts in 64-byte rows, B parts as 64-column
+        // boxes of 32 k-rows
+        if (int rc = make_map_f16(&m1, parts.A1, M, K, lda2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+          return rc;
+        if (int rc = make_map_f16(&m2, parts.A2, M, K, lda2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+          return rc;
+        if (int rc = make_map_f16(&m3, parts.B1, K, N, ldb2, 64, 32)) return rc;
+        if (int rc = make_map_f16(&m4, parts.B2, K, N, ldb2, 64, 32)) return rc;
+        t.ea = parts.ea;
+        t.eb = parts.eb;
+        t.kb_total = (K + 31) / 32;
+      } else {
+        float* Ab = reinterpret_cast<float*>(buf);
+        float* As = Ab + a_part / 4;
+        float* Bb = As + a_part / 4;
+        float* Bs = Bb + b_part / 4;
+        // one launch splits both operands, the blocks shared in proportion to the bytes
+        const long long ttiles = ((K2 + 31) / 32) * ((N + 31) / 32);
+        const int grid_a = scale_grid(*d, 1ll * M * K2 / 4);
+        const int grid_b = static_cast<int>(std::min<long long>(ttiles, 8ll * d->sm_count));
+        if (launch_split_tf32_ab(A, lda, Ab, As, B, ldb, Bb, Bs, K2, M, N, K, grid_a, grid_b,
+                                 stream) != cudaSuccess)
+          return GEMM_ERR_CUDA;
+        // k-blocks of 16 floats: every part in 64-byte rows
+        const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
+        if (int rc = make_map_f32(&m1, Ab, M, K, K2, 16, 128, sw)) return rc;
+        if (int rc = make_map_f32(&m2, As, M, K, K2, 16, 128, sw)) return rc;
+        if (int rc = make_map_f32(&m3, Bb, N, K, K2, 16, 128, sw)) return rc;
+        if (int rc = make_map_f32(&m4, Bs, N, K, K2, 16, 128, sw)) return rc;
+        if (int rc = make_map_f32(&m5, Bb, N, K, K2, 16, 64, sw)) return rc;
+        if (int rc = make_map_f32(&m6, Bs, N, K, K2, 16, 64, sw)) return rc;
+        t.Ab = Ab;
+        t.As = As;
+        t.Bb = Bb;
+        t.Bs = Bs;
+        t.kb_total = (K + 15) / 16;
+      }
       t.C = C;
       t.M = M;
       t.N = N;
@@ -898,21 +948,23 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       t.beta = beta;
       t.tiles_m = (M + 255) / 256;
       t.tiles_n = (N + 255) / 256;
-      t.kb_total = (K + 31) / 32;
       const int tiles = t.tiles_m * t.tiles_n;
       // Few tiles for the pairs and a long K: every tile is cut into equal K
-      // slices (whole 4-k-block accumulation chunks) that fill about one
-      // wave; each slice publishes fp32 partial sums and the last to finish
-      // adds them up.  Otherwise the tiles of the last, partial wave run as
-      // two half-width units each when the halves fit in one wave.
-      // gemm_force_splits: 1 keeps whole-K units, > 1 sets the slice count.
+      // slices (whole 4-k-block chunks) that fill about one wave; each slice
+      // publishes fp32 partial sums and the last to finish adds them up.
+      // Otherwise the tiles of the last, partial wave run as two half-width
+      // units each when the halves fit in one wave.  The plan counts in
+      // 128-byte rows of K (32 floats or 64 halves, the same MMA work for
+      // either kind): two of the kernel's 64-byte k-blocks, four of them one
+      // accumulation chunk.  gemm_force_splits: 1 keeps whole-K units, > 1
+      // sets the slice count.
       const int fs = g_force_splits.load();
       int splits = 1;
       if (force != 5) {
-        const TailSplit ts = tf32_slice_plan(tiles, pairs, t.kb_total, fs);
+        const TailSplit ts = tf32_slice_plan(tiles, pairs, (t.kb_total + 1) / 2, fs);
         if (ts.splits > 1) {
           splits = ts.splits;
-          t.kb_per_split = ts.kb_per_split;
+          t.kb_per_split = 2 * ts.kb_per_split;
         }
       }
       bool halves = false;
@@ -922,10 +974,10 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
         t.dp_tiles = tiles;
         t.num_units = tiles * splits;
         // per tile: 2 CTAs x 8 epilogue warps x splits x (32 rows x 128 fp32)
-        const size_t need = static_cast<size_t>(tiles) * splits * 2 * 8 * 32 * 128 * sizeof(float);
+        const size_t wneed = static_cast<size_t>(tiles) * splits * 2 * 8 * 32 * 128 * sizeof(float);
         std::lock_guard<std::mutex> lk(g_mu);
         StreamWs* w = nullptr;
-        if (int rc = stream_scratch(d, stream, need, static_cast<size_t>(tiles) * 16, &w))
+        if (int rc = stream_scratch(d, stream, wneed, static_cast<size_t>(tiles) * 16, &w))
           return rc;
         t.part_ws = static_cast<float4*>(w->ptr);
         t.counters = static_cast<unsigned long long*>(w->counters);
@@ -943,11 +995,15 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       t.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
       t.status = d->status;
       const int grid = 2 * std::min(t.num_units, pairs);
-      t_last_path = splits > 1 ? "f32.3xtf32.pair.ksplit"
-                               : (halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair");
-      return launch_sgemm_3xtf32(mAb, mAs, mBb, mBs, mBbh, mBsh, t, grid, stream) == cudaSuccess
-                 ? GEMM_OK
-                 : GEMM_ERR_CUDA;
+      if (x16)
+        t_last_path = splits > 1 ? "f32.3xf16.pair.ksplit"
+                                 : (halves ? "f32.3xf16.pair.halves" : "f32.3xf16.pair");
+      else
+        t_last_path = splits > 1 ? "f32.3xtf32.pair.ksplit"
+                                 : (halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair");
+      const cudaError_t e = x16 ? launch_sgemm_3xf16(m1, m2, m3, m4, t, grid, stream)
+                                : launch_sgemm_3xtf32(m1, m2, m3, m4, m5, m6, t, grid, stream);
+      return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
   }
   const bool vec = force != 4 && aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 &&
@@ -1144,7 +1200,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 15) return GEMM_ERR_ARG;
+  if (path < 0 || path > 16) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 

@@ -4,7 +4,8 @@
 //   * realignment of an operand whose rows are not 16-byte aligned into an
 //     aligned copy, so that the tensor-core kernel can load it by TMA, and the
 //     copy of such a C back from the aligned copy the kernel wrote by TMA;
-//   * the big/small tf32 split of fp32 operands for the 3xTF32 SGEMM;
+//   * the big/small tf32 split of fp32 operands for the 3xTF32 SGEMM, and the
+//     scaled two-part fp16 split for the 3xFP16 SGEMM;
 //   * scale-only update for alpha == 0 or K == 0: C := beta*C (C := 0 when
 //     beta == 0, without reading C -- the convention of the "LeetGPU GEMM T4"
 //     WMMA sections and the "advanced SGEMM" page for beta == 0).
@@ -305,6 +306,216 @@ __global__ void split_tf32_ab_kernel(const float* __restrict__ A, long long lda,
   griddep_launch_dependents();
 }
 
+// ---- fp32 operands as two scaled fp16 parts (the 3xFP16 SGEMM) ----------
+// x * 2^e = h1 + h2 + r with h1 = half(x * 2^e) and h2 = half(x * 2^e - h1),
+// both rounded to nearest: |r| <= 2^-22 |x * 2^e| (the same 11 + 11
+// significand bits as the tf32 split).  e is a power-of-two exponent per row
+// of A and per column of B, chosen so that the largest magnitude of the row
+// (column) lands in [2^14, 2^15): no part overflows half, and the scaling and
+// its undoing in the epilogue are exact.
+
+// Exponent that takes the largest magnitude m into [2^14, 2^15); 0 when m is
+// zero or not finite (the parts then carry the Inf or NaN).
+__device__ __forceinline__ int f16x3_exponent(float m) {
+  return (m > 0.0f && isfinite(m)) ? 14 - ilogbf(m) : 0;
+}
+
+// 2^e as two normal powers of two whose product is 2^e (e in [-113, 163]):
+// x * f.x * f.y is then exact for every x the scaling is meant for.
+__device__ __forceinline__ float2 f16x3_factors(int e) {
+  const int e1 = max(-126, min(127, e));
+  const int e2 = e - e1;   // 0 unless e > 127
+  return make_float2(__int_as_float((e1 + 127) << 23), __int_as_float((e2 + 127) << 23));
+}
+
+__device__ __forceinline__ uint32_t f16x3_parts(float x, float2 f, uint32_t* lo) {
+  const float y = (x * f.x) * f.y;
+  const __half h1 = __float2half_rn(y);
+  const __half h2 = __float2half_rn(y - __half2float(h1));
+  *lo = __half_as_ushort(h2);
+  return __half_as_ushort(h1);
+}
+
+// Rows of A, one block of 256 threads per row (grid-stride over rows): the
+// row's largest magnitude, then its two parts with that row's exponent;
+// ea[row] = the exponent.  A row of up to kRowRegs * 256 elements is read once
+// and kept in registers between the two steps; with many rows in flight a
+// second read of each row missed L2 and doubled the traffic.  Longer rows
+// are read a second time.  A is read with the streaming hint (used once), so
+// that B, read by the other blocks of this launch and again by the next one,
+// stays in L2.
+constexpr int kRowVec = 8;   // float4 per thread held in registers: K <= 8192
+__device__ __forceinline__ void f16x3_split_rows(const float* __restrict__ A, long long lda,
+                                                 uint16_t* __restrict__ A1,
+                                                 uint16_t* __restrict__ A2, long long ld2,
+                                                 int* __restrict__ ea, int M, int K,
+                                                 long long block, long long nblocks,
+                                                 float* red) {
+  const int tid = static_cast<int>(threadIdx.x);
+  const int lane = tid & 31, warp = tid >> 5;
+  const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0;
+  const bool held = K <= kRowVec * 4 * 256;
+  auto load4 = [&](const float* a, int k) -> float4 {
+    if (vec && k + 4 <= K) return __ldcs(reinterpret_cast<const float4*>(a + k));
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = (k + i < K) ? __ldcs(a + k + i) : 0.0f;
+    return make_float4(x[0], x[1], x[2], x[3]);
+  };
+  for (long long r = block; r < M; r += nblocks) {
+    const float* const a = A + r * lda;
+    float4 v[kRowVec];
+    float m = 0.0f;
+    if (held) {
+#pragma unroll
+      for (int i = 0; i < kRowVec; ++i) {
+        const int k = 4 * (tid + 256 * i);
+        v[i] = k < K ? load4(a, k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kRowVec; ++i)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+    } else {
+      for (int k = 4 * tid; k < K; k += 1024) {
+        const float4 w = load4(a, k);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+      }
+    }
+    // block maximum (NaN does not propagate through fmaxf: a NaN element is
+    // carried into its parts by the split below whatever the exponent)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+    __syncthreads();   // red is reused by the next row
+    const int e = f16x3_exponent(m);
+    const float2 f = f16x3_factors(e);
+    if (tid == 0) ea[r] = e;
+    uint16_t* const d1 = A1 + r * ld2;
+    uint16_t* const d2 = A2 + r * ld2;
+    // groups of 4 elements: one 8-byte store per part (ld2 % 8 == 0; the
+    // padding columns of the last group get zeros)
+    auto put = [&](int k, float4 w) {
+      uint32_t h[4], l[4];
+      h[0] = f16x3_parts(w.x, f, &l[0]);
+      h[1] = f16x3_parts(w.y, f, &l[1]);
+      h[2] = f16x3_parts(w.z, f, &l[2]);
+      h[3] = f16x3_parts(w.w, f, &l[3]);
+      __stcs(reinterpret_cast<uint2*>(d1 + k), make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16)));
+      __stcs(reinterpret_cast<uint2*>(d2 + k), make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16)));
+    };
+    if (held) {
+#pragma unroll
+      for (int i = 0; i < kRowVec; ++i) {
+        const int k = 4 * (tid + 256 * i);
+        if (k < K) put(k, v[i]);
+      }
+    } else {
+      for (int k = 4 * tid; k < K; k += 1024) put(k, load4(a, k));
+    }
+  }
+}
+
+// Largest magnitude of each column of B (K x N): each thread takes 4
+// consecutive columns over a band of 16 rows (all 16 loads in flight) and
+// folds its maxima into colmax (the magnitudes' bit patterns, which order
+// like the values; colmax starts at zero).
+__device__ __forceinline__ void f16x3_column_max(const float* __restrict__ B, long long ldb,
+                                                 unsigned int* __restrict__ colmax, int K, int N,
+                                                 long long block, long long nblocks) {
+  const long long groups = (N + 3) / 4;
+  const long long bands = (K + 15) / 16;
+  const bool vec = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0;
+  for (long long g = block * blockDim.x + threadIdx.x; g < groups * bands;
+       g += nblocks * blockDim.x) {
+    const int c0 = static_cast<int>(g % groups) * 4;
+    const int k0 = static_cast<int>(g / groups) * 16;
+    float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 16
+    for (int i = 0; i < 16; ++i) {
+      const int k = k0 + i;
+      if (k >= K) break;
+      const float* const b = B + static_cast<long long>(k) * ldb + c0;
+      if (vec && c0 + 4 <= N) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(b));
+        m[0] = fmaxf(m[0], fabsf(v.x)); m[1] = fmaxf(m[1], fabsf(v.y));
+        m[2] = fmaxf(m[2], fabsf(v.z)); m[3] = fmaxf(m[3], fabsf(v.w));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (c0 + i < N) m[i] = fmaxf(m[i], fabsf(__ldg(b + i)));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (c0 + i < N && m[i] > 0.0f) atomicMax(colmax + c0 + i, __float_as_uint(m[i]));
+  }
+}
+
+// First launch: blocks [0, grid_a) split the rows of A, the others take the
+// column maxima of B.
+__global__ void f16x3_split_a_kernel(const float* __restrict__ A, long long lda,
+                                     uint16_t* __restrict__ A1, uint16_t* __restrict__ A2,
+                                     long long lda2, int* __restrict__ ea, const float* __restrict__ B,
+                                     long long ldb, unsigned int* __restrict__ colmax, int M, int N,
+                                     int K, int grid_a) {
+  __shared__ float red[8];
+  if (static_cast<int>(blockIdx.x) < grid_a)
+    f16x3_split_rows(A, lda, A1, A2, lda2, ea, M, K, blockIdx.x, grid_a, red);
+  else
+    f16x3_column_max(B, ldb, colmax, K, N, blockIdx.x - grid_a, gridDim.x - grid_a);
+  griddep_launch_dependents();
+}
+
+// Second launch: B's two parts with each column's exponent, 4 columns per
+// thread: each work item is one group of columns (its factors computed once)
+// and every per_group-th row; the items that start at row 0 write eb.  A grid
+// smaller than the column groups takes several items per thread.
+__global__ void f16x3_split_b_kernel(const float* __restrict__ B, long long ldb,
+                                     uint16_t* __restrict__ B1, uint16_t* __restrict__ B2,
+                                     long long ldb2, const unsigned int* __restrict__ colmax,
+                                     int* __restrict__ eb, int K, int N) {
+  griddep_wait();   // the column maxima of the launch before
+  const long long groups = (N + 3) / 4;
+  const bool vec = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0;
+  const long long threads = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  // threads per column group: the rows are shared out among them
+  const long long per_group = max(1ll, threads / groups);
+  for (long long u = t; u < per_group * groups; u += threads) {
+  const int c0 = static_cast<int>(u % groups) * 4;
+  float2 f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = (c0 + i < N) ? f16x3_exponent(__uint_as_float(__ldg(colmax + c0 + i))) : 0;
+    f[i] = f16x3_factors(e);
+    if (u < groups && c0 + i < N) eb[c0 + i] = e;
+  }
+#pragma unroll 4
+  for (long long k = u / groups; k < K; k += per_group) {
+    const float* const b = B + k * ldb + c0;
+    float x[4];
+    if (vec && c0 + 4 <= N) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(b));
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = (c0 + i < N) ? __ldg(b + i) : 0.0f;
+    }
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = f16x3_parts(x[i], f[i], &l[i]);
+    const long long o = k * ldb2 + c0;
+    *reinterpret_cast<uint2*>(B1 + o) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    *reinterpret_cast<uint2*>(B2 + o) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+  }
+  }
+  griddep_launch_dependents();
+}
+
 // dst[i] = src[i] rounded to the nearest half (ties to even), eight elements
 // per thread and step: two 16-byte loads and one 16-byte store when both
 // pointers are 16-byte aligned (VEC), element accesses otherwise.
@@ -369,6 +580,32 @@ cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float
   return counted_launch(cudaGetLastError());
 }
 
+
+cudaError_t launch_f16x3_split(const float* A, long long lda, const float* B, long long ldb,
+                               const F16x3Parts& p, int M, int N, int K, int grid_a, int grid_bmax,
+                               int grid_b, cudaStream_t stream) {
+  if (cudaMemsetAsync(p.colmax, 0, static_cast<size_t>(N) * sizeof(unsigned int), stream) !=
+      cudaSuccess)
+    return cudaErrorUnknown;
+  f16x3_split_a_kernel<<<grid_a + grid_bmax, 256, 0, stream>>>(A, lda, p.A1, p.A2, p.lda2, p.ea, B,
+                                                               ldb, p.colmax, M, N, K, grid_a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  counted_launch(e);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid_b), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, f16x3_split_b_kernel, B, ldb, p.B1, p.B2, p.ldb2,
+                         static_cast<const unsigned int*>(p.colmax), p.eb, K, N);
+  if (e != cudaSuccess) return e;
+  return counted_launch(cudaGetLastError());
+}
 
 cudaError_t launch_realign_f16(const RealignBatch& batch, cudaStream_t stream) {
   if (batch.n < 1 || batch.n > 3) return cudaErrorInvalidValue;

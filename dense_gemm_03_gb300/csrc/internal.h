@@ -177,6 +177,23 @@ cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float
                                  const float* B, long long ldb, float* Bb, float* Bs, long long ld2,
                                  int M, int N, int K, int grid_a, int grid_b, cudaStream_t stream);
 
+// The fp16 parts of the 3xFP16 SGEMM: x * 2^e = h1 + h2 (+ 2^-22 relative),
+// with e per row of A (ea) and per column of B (eb); A1, A2 are M x lda2,
+// B1, B2 are K x ldb2 (row-major, lda2 and ldb2 multiples of 8); colmax holds
+// B's column maxima between the two launches.
+struct F16x3Parts {
+  uint16_t *A1, *A2, *B1, *B2;
+  long long lda2, ldb2;
+  int* ea;
+  int* eb;
+  unsigned int* colmax;
+};
+// Two launches (a memset of colmax first): A's rows and B's column maxima,
+// then B's parts (a programmatic dependent of the first).
+cudaError_t launch_f16x3_split(const float* A, long long lda, const float* B, long long ldb,
+                               const F16x3Parts& parts, int M, int N, int K, int grid_a,
+                               int grid_bmax, int grid_b, cudaStream_t stream);
+
 // 3xTF32 SGEMM on CTA pairs: C = alpha*(Ab*Bb + Ab*Bs + As*Bb) + beta*C with
 // the split operands dense and K-contiguous: A parts M x roundup(K,4), B parts
 // transposed, N x roundup(K,4).
@@ -210,6 +227,10 @@ struct Tf32Args {
   unsigned long long* counters;     // [tile][rank][warp]: (epoch << 32) | arrivals
   unsigned int epoch;
   bool pdl;                         // host only: as TcArgs::pdl (after the split pre-pass)
+  // 3xFP16 only: the power-of-two exponent of each row of A and of each column
+  // of B (eb padded to a multiple of 4 entries) that the parts were scaled by
+  const int* ea;
+  const int* eb;
 };
 // tmBbh / tmBsh: the B parts with 64-row boxes, for the half-width units.
 cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,
@@ -217,6 +238,12 @@ cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs
                                 const CUtensorMap& tmBbh, const CUtensorMap& tmBsh,
                                 const Tf32Args& args, int grid, cudaStream_t stream);
 int sgemm_3xtf32_max_pairs();
+// The same kernel on the 3xFP16 parts (A1, A2: M x lda2 halves, boxes of 64
+// columns x 128 rows; B1, B2: K x ldb2 halves, boxes of 64 columns x 64 rows);
+// k-blocks of 64.
+cudaError_t launch_sgemm_3xf16(const CUtensorMap& tmA1, const CUtensorMap& tmA2,
+                               const CUtensorMap& tmB1, const CUtensorMap& tmB2,
+                               const Tf32Args& args, int grid, cudaStream_t stream);
 
 // C := beta * C (C := 0 when beta == 0): the alpha == 0 / K == 0 case.
 cudaError_t launch_scale_f16(uint16_t* C, long long ldc, int M, int N, float beta, int grid,

@@ -10,25 +10,39 @@
 // Accumulation.  The tensor core's fp32 accumulation does not round to
 // nearest: summed over a long K in tensor memory, the result drifts toward
 // zero by a bias that grows like K*|C| (measured: at K = 16384 it exceeds the
-// fp32 error bound).  So the MMA accumulates only chunks of 128 along K into
-// tensor memory (alternating between two buffers), and the epilogue warps add
+// fp32 error bound).  So the MMA accumulates only chunks of 128 along K (256
+// for the 3xFP16 form below) into tensor memory (alternating between two buffers), and the epilogue warps add
 // each chunk into fp32 registers with ordinary round-to-nearest adds; the
 // result is then as accurate as the FFMA kernel's.
 //
 // Kernel: CTA pairs (clusters of 2) share tcgen05.mma.cta_group::2.kind::tf32
 // with M = 256 (128 rows of A in each CTA) and N = 256 (each CTA stages 128 of
-// the columns of B); per 32-deep k-block each CTA stages Ab, As (128 x 32) and
-// Bb, Bs (128 columns x 32) by TMA into a 3-stage ring (64 KB per stage), and
-// the leader issues 3 MMAs per 8-deep K step.  Warp roles and barriers follow
+// the columns of B); per 16-deep k-block each CTA stages Ab, As (128 x 16) and
+// Bb, Bs (128 columns x 16) by TMA into a 6-stage ring (32 KB per stage), and
+// the leader issues 3 MMAs per 8-deep K step.  Small stages keep five of the
+// six in flight while one is consumed: with 64 KB stages (three of them) a
+// load took ~2.3 us from issue to arrival and the pipeline ran at the rate of
+// the loads, not of the MMAs.  Warp roles and barriers follow
 // the fp16 tensor-core kernel; the 8 epilogue warps keep fp32 row sums in
 // registers and write C through a small shared-memory tile each, so that
 // stores cover whole 64-byte row pieces.  Both operands are K-major (the pre-pass stores the B
-// parts transposed): 128-byte swizzle, 32 floats per row, SBO 1024 B.
+// parts transposed): 64-byte swizzle, 16 floats per row, SBO 512 B.
 //
 // Units: whole 256 x 256 tiles; the tiles of a last, partial wave as two
 // half-width units each; or, when few tiles meet a long K, equal K slices of
 // every tile (whole accumulation chunks), whose fp32 partial sums the last
 // slice of a tile to arrive adds up in slice order before writing C.
+//
+// 3xFP16 (the same kernel, F16 = true): the parts are halves instead of tf32
+// values -- x * 2^e = h1 + h2 with e a power-of-two exponent per row of A and
+// per column of B that keeps the parts inside the half range (the same 11 + 11
+// significand bits as the tf32 split), written by the split pre-pass -- and
+// the three products run as kind::f16 MMAs at twice the tf32 rate.  A k-block
+// is then 32 deep (one 64-byte row of halves), B is staged N-major as 64-
+// column blocks of 32 k-rows (128-byte swizzle, no transpose), chunks are 8
+// k-blocks (256 deep: a 128-deep chunk left the fold of the chunks into
+// registers, not the MMAs, setting the pace), and the
+// epilogue undoes the scaling (an exact multiply by 2^-(e_row + e_col)).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,16 +51,16 @@ namespace {
 
 constexpr int BM = 128;                     // rows per CTA
 constexpr int BN = 256;                     // pair tile width
-constexpr int BK = 32;                      // floats per k-block (one 128-byte row)
-constexpr int kMmaK = 8;                    // K of one kind::tf32 MMA
-constexpr int kATile = BM * BK * 4;         // 16 KB per part
+constexpr int kRowBytes = 64;               // bytes of K per k-block row: 16 floats or 32 halves
+constexpr int kATile = BM * kRowBytes;      // 8 KB per part (128 rows of 64 bytes)
 constexpr int kBCols = BN / 2;              // B columns staged by each CTA
-constexpr int kBTile = kBCols * BK * 4;     // 16 KB per part
+constexpr int kBTile = kBCols * kRowBytes;  // 8 KB per part
+constexpr int kBBlock = 32 * 128;           // 3xFP16: one 64-column block of a B part (32 k-rows)
 constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
-constexpr int kStages = 3;
+constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;
 constexpr int kCols = BN / 2;               // accumulator columns per epilogue thread
-constexpr int kChunkKb = 4;                 // k-blocks per TMEM accumulation chunk (K = 128)
+constexpr int kChunkKb = 8;                 // k-blocks per TMEM accumulation chunk (K = 128 floats, 256 halves)
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kBarOff = kStages * kStageBytes;
@@ -56,7 +70,9 @@ constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
 // sums into row-contiguous stores of C
 constexpr int kEpiOff = (kTmemPtrOff + 16 + 127) / 128 * 128;
 constexpr int kEpiTileF4 = 32 * 4;
-constexpr int kSmemAlloc = kEpiOff + kEpiWarps * kEpiTileF4 * 16 + 1024;
+// 3xFP16: per epilogue warp the exponents of its 128 columns (32 int4)
+constexpr int kEpiExpOff = kEpiOff + kEpiWarps * kEpiTileF4 * 16;
+constexpr int kSmemAlloc = kEpiExpOff + kEpiWarps * 32 * 16 + 1024;
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
@@ -132,8 +148,24 @@ __device__ __forceinline__ bool publish_slice(const Tf32Args& p, int u, int rank
   return true;
 }
 
+// Multiplies four values of the scaled 3xFP16 domain by 2^-E (exact unless a
+// result is subnormal or overflows).  When every E of the warp is within
+// +-126 -- all but extreme inputs -- 2^-E is a normal float and one multiply
+// does it; otherwise ldexpf.  The vote keeps the ldexpf code off the common
+// path: as a per-element select it made the whole store phase ~4x slower.
+// Warp-uniform calls only.
+__device__ __forceinline__ float4 unscale4(float4 v, int e_row, int4 ec) {
+  const int E0 = e_row + ec.x, E1 = e_row + ec.y, E2 = e_row + ec.z, E3 = e_row + ec.w;
+  auto in = [](int E) { return static_cast<unsigned>(E + 126) <= 252u; };
+  if (__all_sync(0xffffffffu, in(E0) && in(E1) && in(E2) && in(E3)))
+    return make_float4(v.x * __int_as_float((127 - E0) << 23), v.y * __int_as_float((127 - E1) << 23),
+                       v.z * __int_as_float((127 - E2) << 23), v.w * __int_as_float((127 - E3) << 23));
+  return make_float4(ldexpf(v.x, -E0), ldexpf(v.y, -E1), ldexpf(v.z, -E2), ldexpf(v.w, -E3));
+}
+
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
-    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAb,
+    sgemm_split_kernel(const __grid_constant__ CUtensorMap tmAb,
                         const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBb,
                         const __grid_constant__ CUtensorMap tmBs,
@@ -232,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_of(u, m0, n0, ncols, kb0, kb1);
         // B rows (columns of B) this CTA stages: half of the unit's
         const int bcols = ncols / 2;
-        const uint32_t bytes = static_cast<uint32_t>(2 * kATile + 2 * bcols * BK * 4);
+        const uint32_t bytes = static_cast<uint32_t>(2 * kATile + 2 * bcols * kRowBytes);
         const CUtensorMap* mb = bcols == kBCols ? &tmBb : &tmBbh;
         const CUtensorMap* ms = bcols == kBCols ? &tmBs : &tmBsh;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -243,11 +275,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = map_to_cta(full_bar(s), 0);
           if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
           const uint32_t sa = stage(s);
-          tma_load_2d_pair(sa, &tmAb, fb, kb * BK, m0);
-          tma_load_2d_pair(sa + kATile, &tmAs, fb, kb * BK, m0);
+          constexpr int kbk = F16 ? 32 : 16;   // elements per k-block
+          tma_load_2d_pair(sa, &tmAb, fb, kb * kbk, m0);
+          tma_load_2d_pair(sa + kATile, &tmAs, fb, kb * kbk, m0);
           const int nb = n0 + static_cast<int>(rank) * bcols;
-          tma_load_2d_pair(sa + 2 * kATile, mb, fb, kb * BK, nb);
-          tma_load_2d_pair(sa + 2 * kATile + kBTile, ms, fb, kb * BK, nb);
+          if (F16) {
+            // B parts N-major: one 64-column block (32 k-rows) per box
+            for (int c = 0; c < bcols / 64; ++c) {
+              tma_load_2d_pair(sa + 2 * kATile + c * kBBlock, &tmBb, fb, nb + 64 * c, kb * kbk);
+              tma_load_2d_pair(sa + 2 * kATile + kBTile + c * kBBlock, &tmBs, fb, nb + 64 * c,
+                               kb * kbk);
+            }
+          } else {
+            tma_load_2d_pair(sa + 2 * kATile, mb, fb, kb * kbk, nb);
+            tma_load_2d_pair(sa + 2 * kATile + kBTile, ms, fb, kb * kbk, nb);
+          }
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -266,8 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk starts a fresh accumulation and the epilogue folds it into its
     // fp32 register accumulators.
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc_full = make_idesc(2u, 2 * BM, BN, 0u, 0u);
-      constexpr uint32_t idesc_half = make_idesc(2u, 2 * BM, BN / 2, 0u, 0u);
+      // tf32: both operands K-major; f16: B N-major
+      constexpr uint32_t idesc_full = F16 ? make_idesc(0u, 2 * BM, BN, 0u, 1u)
+                                          : make_idesc(2u, 2 * BM, BN, 0u, 0u);
+      constexpr uint32_t idesc_half = F16 ? make_idesc(0u, 2 * BM, BN / 2, 0u, 1u)
+                                          : make_idesc(2u, 2 * BM, BN / 2, 0u, 0u);
+      constexpr int kChunk = kChunkKb;
       int s = 0;
       uint32_t phase = 0, chunk = 0;
       bool ok = true;
@@ -275,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m0, n0, ncols, kb0, kb1;
         tile_of(u, m0, n0, ncols, kb0, kb1);
         const uint32_t idesc = ncols == BN ? idesc_full : idesc_half;
-        for (int kc = kb0; ok && kc < kb1; kc += kChunkKb, ++chunk) {
+        for (int kc = kb0; ok && kc < kb1; kc += kChunk, ++chunk) {
           const uint32_t buf = chunk & 1u, use = chunk >> 1;
           if (!wait_parity(acce_bar(buf), (use & 1u) ^ 1u, limit, st, 23)) {
             ok = false;
@@ -283,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + buf * BN;
-          const int kend = min(kc + kChunkKb, kb1);
+          const int kend = min(kc + kChunk, kb1);
           for (int kb = kc; kb < kend; ++kb) {
             if (!wait_parity(full_bar(s), phase, limit, st, 24)) {
               ok = false;
@@ -293,15 +339,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a_big = stage(s), a_small = a_big + kATile;
             const uint32_t b_big = a_big + 2 * kATile, b_small = b_big + kBTile;
 #pragma unroll
-            for (int kk = 0; kk < BK / kMmaK; ++kk) {
-              const uint64_t adb = smem_desc_sw128(a_big + kk * (kMmaK * 4), 16u, 1024u);
-              const uint64_t ads = smem_desc_sw128(a_small + kk * (kMmaK * 4), 16u, 1024u);
-              const uint64_t bdb = smem_desc_sw128(b_big + kk * (kMmaK * 4), 16u, 1024u);
-              const uint64_t bds = smem_desc_sw128(b_small + kk * (kMmaK * 4), 16u, 1024u);
+            for (int kk = 0; kk < 2; ++kk) {   // 2 MMA K steps per 64-byte k-block
+              // K-major parts (64-byte swizzle, 8-row groups 512 bytes apart)
+              // advance 32 bytes per step (8 floats or 16 halves); an N-major
+              // B part (128-byte swizzle) advances 16 k-rows (2 KB)
+              const uint64_t adb = smem_desc_sw64(a_big + kk * 32, 16u, 512u);
+              const uint64_t ads = smem_desc_sw64(a_small + kk * 32, 16u, 512u);
+              const uint64_t bdb = F16 ? smem_desc_sw128(b_big + kk * 2048, kBBlock, 1024u)
+                                       : smem_desc_sw64(b_big + kk * 32, 16u, 512u);
+              const uint64_t bds = F16 ? smem_desc_sw128(b_small + kk * 2048, kBBlock, 1024u)
+                                       : smem_desc_sw64(b_small + kk * 32, 16u, 512u);
               // the two small terms first, then the big one
-              mma_tf32_ss_pair(d, ads, bdb, idesc, (kb > kc || kk > 0) ? 1u : 0u);
-              mma_tf32_ss_pair(d, adb, bds, idesc, 1u);
-              mma_tf32_ss_pair(d, adb, bdb, idesc, 1u);
+              if (F16) {
+                mma_f16_ss_pair(d, ads, bdb, idesc, (kb > kc || kk > 0) ? 1u : 0u);
+                mma_f16_ss_pair(d, adb, bds, idesc, 1u);
+                mma_f16_ss_pair(d, adb, bdb, idesc, 1u);
+              } else {
+                mma_tf32_ss_pair(d, ads, bdb, idesc, (kb > kc || kk > 0) ? 1u : 0u);
+                mma_tf32_ss_pair(d, adb, bds, idesc, 1u);
+                mma_tf32_ss_pair(d, adb, bdb, idesc, 1u);
+              }
             }
             mma_commit_pair_multicast(empty_bar(s), 3);
             if (++s == kStages) {
@@ -342,6 +399,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = row0 + lane;
       const int colw = n0 + h * wcols;
       const bool active = row0 < p.M && colw < p.N;   // warp-uniform
+      // 3xFP16: this row's exponent, and the exponents of the warp's columns
+      // into shared memory (lane l: columns colw + 4l .. +3) -- loaded now,
+      // while the MMAs run, since loads issued among the stores of C below
+      // would each wait a full round trip (that made the store phase ~8x
+      // slower)
+      int e_row = 0;
+      int4* const e_col = reinterpret_cast<int4*>(base_ptr + kEpiExpOff) + ew * 32;
+      if (F16 && active) {
+        if (row < p.M) e_row = __ldg(p.ea + row);
+        if (colw + 4 * lane < p.N)   // eb holds N + 8 entries: the int4 stays inside
+          e_col[lane] = __ldg(reinterpret_cast<const int4*>(p.eb + colw + 4 * lane));
+        __syncwarp();
+      }
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
@@ -371,6 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok || !active) continue;
       float* const crow = p.C + static_cast<long long>(row) * p.ldc;
+      // 3xFP16: sums of quad g (columns colw + 4g ..) back from the scaled
+      // domain
+      auto descale = [&](int g, float4 v) -> float4 {
+        if (!F16 || colw + 4 * g >= p.N) return v;
+        return unscale4(v, e_row, e_col[g]);
+      };
       // C[row][colw + 4g ..] := alpha * v + beta * C (columns past N and rows
       // past M are not written)
       float4* const tile = reinterpret_cast<float4*>(base_ptr + kEpiOff) + ew * kEpiTileF4;
@@ -461,7 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int jj = 0; jj < kSumQuads / 4; ++jj) {
-            const float4 v4[4] = {sum[4 * jj], sum[4 * jj + 1], sum[4 * jj + 2], sum[4 * jj + 3]};
+            const int g0 = kSumQuads * gb + 4 * jj;
+            const float4 v4[4] = {descale(g0, sum[4 * jj]), descale(g0 + 1, sum[4 * jj + 1]),
+                                  descale(g0 + 2, sum[4 * jj + 2]), descale(g0 + 3, sum[4 * jj + 3])};
             store_group(kSumQuads / 4 * gb + jj, v4);
           }
         }
@@ -473,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q2 = 0; q2 < 4; ++q2) {
           const int g = 4 * j + q2;
-          v4[q2] = make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+          v4[q2] = descale(g, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
         }
         store_group(j, v4);
       }
@@ -505,12 +583,35 @@ cudaError_t configure(int dev) {
   static bool done[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        sgemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(sgemm_split_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(sgemm_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
   return cudaSuccess;
+}
+
+template <bool F16>
+cudaError_t launch_split(const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
+                         const CUtensorMap& b2, const CUtensorMap& b1h, const CUtensorMap& b2h,
+                         const Tf32Args& args, int grid, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = configure(dev)) != cudaSuccess) return e;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
+  if (args.pdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
+  e = cudaLaunchKernelEx(&cfg, sgemm_split_kernel<F16>, a1, a2, b1, b2, b1h, b2h, args);
+  if (e != cudaSuccess) return e;
+  return counted_launch(cudaGetLastError());
 }
 
 }  // namespace
@@ -523,7 +624,7 @@ int sgemm_3xtf32_max_pairs() {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, sgemm_3xtf32_kernel, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, sgemm_split_kernel<false>, &cfg) != cudaSuccess) return 0;
   cached[dev] = n;
   return n;
 }
@@ -532,20 +633,13 @@ cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs
                                 const CUtensorMap& tmBb, const CUtensorMap& tmBs,
                                 const CUtensorMap& tmBbh, const CUtensorMap& tmBsh,
                                 const Tf32Args& args, int grid, cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if ((e = configure(dev)) != cudaSuccess) return e;
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
-  if (args.pdl) {
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.numAttrs = 2;
-  }
-  e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, tmAb, tmAs, tmBb, tmBs, tmBbh, tmBsh, args);
-  if (e != cudaSuccess) return e;
-  return counted_launch(cudaGetLastError());
+  return launch_split<false>(tmAb, tmAs, tmBb, tmBs, tmBbh, tmBsh, args, grid, stream);
+}
+
+cudaError_t launch_sgemm_3xf16(const CUtensorMap& tmA1, const CUtensorMap& tmA2,
+                               const CUtensorMap& tmB1, const CUtensorMap& tmB2,
+                               const Tf32Args& args, int grid, cudaStream_t stream) {
+  return launch_split<true>(tmA1, tmA2, tmB1, tmB2, tmB1, tmB2, args, grid, stream);
 }
 
 }  // namespace gb300

@@ -117,13 +117,20 @@ int gemm_f16_f32out(const uint16_t* A, const uint16_t* B, float* C,
 int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t stream);
 
 /* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 operands and
- * result.  Shapes with K >= 64 run on the tensor cores as three
- * tf32 products of split operands (A = Ab + As, B = Bb + Bs; the As*Bs term,
- * about 2^-22 of |A||B|, is dropped) with fp32 accumulation, after a pre-pass
- * that writes the split operands to library-owned scratch (few output tiles
- * with a long K: every tile cut into K slices whose fp32 partial sums are
- * added in slice order, so results are reproducible run to run); a shorter K
- * uses an FFMA kernel (exact fp32 products). */
+ * result, within the fp32 bound 1e-6 * K * max|A| * max|B| per element.
+ * Shapes with K >= 64 run on the tensor cores as three products of split
+ * operands with fp32 accumulation: each row of A and each column of B is
+ * scaled by a power of two that brings its largest magnitude into
+ * [2^14, 2^15) and split into two halves, x * 2^e = h1 + h2 (11 + 11
+ * significand bits), so A*B ~= A1*B1 + A1*B2 + A2*B1 (the A2*B2 term, about
+ * 2^-22 of |A||B|, is dropped) and the epilogue undoes the scaling exactly
+ * (3xFP16; gemm_force_path(8) takes tf32 parts instead, 3xTF32, at half the
+ * rate).  A pre-pass writes the parts to library-owned scratch (few output
+ * tiles with a long K: every tile cut into K slices whose fp32 partial sums
+ * are added in slice order, so results are reproducible run to run); a
+ * shorter K uses an FFMA kernel (exact fp32 products).  An Inf or NaN operand
+ * makes every output of its row or column NaN on the tensor-core path (its
+ * remainder part is Inf - Inf); the FFMA kernel follows IEEE. */
 int sgemm_f32(const float* A, const float* B, float* C,
               int M, int N, int K, float alpha, float beta, cudaStream_t stream);
 
@@ -195,7 +202,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * kernel with predicated scalar loads; 5 = whole tiles only (no stream-K, no
  * splitting of the last wave); 6 = no CTA pairs (one
  * CTA per 128-row tile); 7 = (fp32) FFMA kernel only, no tensor cores;
- * 8 = (fp32) 3xTF32 tensor-core kernel whatever the shape; 9 = the last,
+ * 8 = (fp32) the 3xTF32 tensor-core kernel (tf32 parts) whatever the shape; 9 = the last,
  * partial wave of tiles cut into two equal K slices (instead of two
  * half-width units); 10 = stream-K over the last waves of tiles (k-block
  * ranges shared out evenly); 11 = stream-K over all tiles, one CTA per worker
@@ -208,7 +215,8 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * half the workers into two K slices each, the first slice one worker's
  * first unit and the second another worker's last (it adds the first one's
  * partial sums, published long before); else it runs them as half-width
- * units; 15 = half-width units for them.
+ * units; 15 = half-width units for them; 16 = (fp32) the 3xFP16 tensor-core
+ * kernel whatever the shape (8 = 3xTF32).
  * A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.
@@ -261,11 +269,12 @@ int gemm_plan_stream_k(long long tiles, long long slots, int kb, int all_tiles, 
 
 /*
  * The K-slice plan of the fp32 tensor-core path for `tiles` 256x256 output
- * tiles of `kb` 32-deep k-blocks on `pairs` concurrent CTA pairs, as the
- * automatic choice makes it (`forced_slices` > 1 plays gemm_force_splits).
- * Writes out[0] = slices per tile (1 = whole-K units, no slicing) and
- * out[1] = k-blocks per slice (a multiple of 4; the last slice may be
- * shorter).  Host-only; returns GEMM_OK, GEMM_ERR_NULL for a null `out`, or
+ * tiles of `kb` planning k-blocks (128 bytes of K per row: 32 floats, or 64
+ * halves for 3xFP16; the kernel runs each as two 64-byte k-blocks) on `pairs`
+ * concurrent CTA pairs, as the automatic choice makes it (`forced_slices` > 1
+ * plays gemm_force_splits).  Writes out[0] = slices per tile (1 = whole-K
+ * units, no slicing) and out[1] = planning k-blocks per slice (a multiple of
+ * 4; the last slice may be shorter).  Host-only; returns GEMM_OK, GEMM_ERR_NULL for a null `out`, or
  * GEMM_ERR_ARG for a negative argument.
  */
 int gemm_plan_tf32_slices(long long tiles, long long pairs, int kb, int forced_slices,

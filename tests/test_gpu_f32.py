@@ -51,7 +51,7 @@ def test_random_parity(path, M, N, K, alpha, beta, c_fill):
 ])
 def test_leading_dimensions(M, N, K, lda, ldb, ldc):
     """Leading dimensions on the FFMA kernel (vector or scalar accesses) and on
-    the automatic 3xTF32 path, whose split pre-pass reads any stride."""
+    the automatic tensor-core path, whose split pre-pass reads any stride."""
     A, B, C0 = operands(17 + lda, M, N, K, lda, ldb, ldc, np.float32)
     got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc, path=FFMA_ONLY)
     vec = lda % 4 == 0 and ldb % 4 == 0 and ldc % 4 == 0
@@ -59,7 +59,7 @@ def test_leading_dimensions(M, N, K, lda, ldb, ldc):
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
     assert padding_untouched(got, C0, N)
     got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
-    assert taken.startswith("f32.3xtf32.pair"), taken
+    assert taken.startswith("f32.3xf16.pair"), taken
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
     assert padding_untouched(got, C0, N)
 
@@ -83,44 +83,51 @@ def test_deterministic():
     assert np.array_equal(r1, r2)
 
 
-# ---------------------------------------------------------------- 3xTF32 tensor-core path
-FFMA_ONLY, TF32_FORCED = 7, 8
+# ---------------------------------------------------------------- tensor-core paths (split operands)
+FFMA_ONLY, TF32_FORCED, F16X3_FORCED = 7, 8, 16
+# (forced path, path prefix): the automatic choice takes 3xFP16 (scaled half
+# parts, kind::f16); path 8 forces 3xTF32 (tf32 parts, kind::tf32)
+KINDS = [(0, "f32.3xf16.pair"), (TF32_FORCED, "f32.3xtf32.pair")]
 
 
+@pytest.mark.parametrize("kind,prefix", KINDS)
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 520, 200), (129, 257, 65), (7, 9, 13),
                                    (1000, 1000, 1000), (513, 1025, 4100), (64, 2000, 33)])
 @pytest.mark.parametrize("alpha,beta,c_fill", [(1.0, 0.0, "nan"), (1.5, 0.5, "uniform"),
                                                (0.75, -0.25, "uniform")])
-def test_3xtf32_parity(M, N, K, alpha, beta, c_fill):
+def test_split_parity(kind, prefix, M, N, K, alpha, beta, c_fill):
+    path = kind if kind else F16X3_FORCED   # K < 64 takes the FFMA kernel unless forced
     A, B, C0 = operands(900 + M + N + K, M, N, K, K, N, N, np.float32, c_fill=c_fill)
-    got, taken = run("f32", A, B, C0, alpha, beta, M, N, K, K, N, N, path=TF32_FORCED)
-    assert taken.startswith("f32.3xtf32.pair")
+    got, taken = run("f32", A, B, C0, alpha, beta, M, N, K, K, N, N, path=path)
+    assert taken.startswith(prefix), taken
     check("f32", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
 
 
+@pytest.mark.parametrize("kind,prefix", KINDS)
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 700, 1000)])
-def test_3xtf32_small_integers_bit_exact(M, N, K):
-    """Integers in {-3..3} are tf32 values: the small parts are zero and every
-    partial sum is exact."""
+def test_split_small_integers_bit_exact(kind, prefix, M, N, K):
+    """Integers in {-3..3}: tf32 values, and halves after any power-of-two
+    scaling, so the small parts are zero and every partial sum is exact."""
     rng = np.random.default_rng(M + N + K)
     A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
     B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
     C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
-    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=TF32_FORCED)
-    assert taken.startswith("f32.3xtf32.pair")
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=kind)
+    assert taken.startswith(prefix), taken
     assert np.array_equal(got.astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0))
 
 
-def test_3xtf32_close_to_ffma_and_split_pins():
+@pytest.mark.parametrize("kind,prefix", KINDS)
+def test_split_close_to_ffma(kind, prefix):
     """The split keeps enough bits: at K = 1024 both the tensor-core and the
-    FFMA product stay below an eighth of the fp32 bound (a single tf32 product,
-    with its 2^-11 relative rounding per term, lands near or above the whole
-    bound)."""
+    FFMA product stay below an eighth of the fp32 bound (a single tf32 or half
+    product, with its 2^-11 relative rounding per term, lands near or above
+    the whole bound)."""
     M = N = K = 1024
     A, B, C0 = operands(77, M, N, K, K, N, N, np.float32)
-    tc, t1 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    tc, t1 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=kind)
     ff, t2 = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=FFMA_ONLY)
-    assert t1.startswith("f32.3xtf32.pair") and t2.startswith("f32.ffma")
+    assert t1.startswith(prefix) and t2.startswith("f32.ffma")
     ref = oracle.gemm(A, B, None, 1.0, 0.0)
     err_tc = np.abs(tc - ref).max()
     err_ff = np.abs(ff - ref).max()
@@ -128,15 +135,16 @@ def test_3xtf32_close_to_ffma_and_split_pins():
     assert err_tc < bound / 8 and err_ff < bound / 8, (err_tc, err_ff, bound)
 
 
-def test_3xtf32_long_k_no_drift():
+@pytest.mark.parametrize("kind,prefix", KINDS)
+def test_split_long_k_no_drift(kind, prefix):
     """Long K: the tensor core's own fp32 accumulation drifts toward zero by a
     bias growing like K*|C| (past the bound by K = 16384); the kernel folds
     128-deep chunks into round-to-nearest register sums, so the error stays a
     small fraction of the bound and shows no systematic sign."""
     M, N, K = 256, 256, 16384
     A, B, C0 = operands(4242, M, N, K, K, N, N, np.float32)
-    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=TF32_FORCED)
-    assert taken.startswith("f32.3xtf32.pair")
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=kind)
+    assert taken.startswith(prefix), taken
     ref = oracle.gemm(A, B, None, 1.0, 0.0)
     err = got.astype(np.float64) - ref
     bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
@@ -146,25 +154,46 @@ def test_3xtf32_long_k_no_drift():
     assert abs(bias) < bound / 100, (bias, bound)
 
 
+def test_f16x3_scaled_rows_and_columns():
+    """3xFP16 scales each row of A and each column of B by its own power of
+    two before the split: rows and columns whose magnitudes differ by 2^+-60
+    (far outside the half range, and far apart) keep fp32 accuracy, each
+    output within the fp32 bound taken over its own row and column."""
+    rng = np.random.default_rng(61)
+    M, N, K = 300, 260, 700
+    A = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-60, 61, (M, 1)))).astype(np.float32)
+    B = (rng.standard_normal((K, N)) * np.exp2(rng.integers(-60, 61, (1, N)))).astype(np.float32)
+    C0 = np.zeros((M, N), np.float32)
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    assert taken.startswith("f32.3xf16.pair"), taken
+    ref = oracle.gemm(A, B, None, 1.0, 0.0)
+    per = 1e-6 * K * np.abs(A).max(axis=1)[:, None] * np.abs(B).max(axis=0)[None, :]
+    assert (np.abs(got.astype(np.float64) - ref) <= per).all()
+    check("f32", got, A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+
+
+@pytest.mark.parametrize("kind,prefix", KINDS)
 @pytest.mark.parametrize("M,N,K", [(2560, 2560, 512), (2500, 2000, 300)])
-def test_3xtf32_half_width_tail(M, N, K):
+def test_split_half_width_tail(kind, prefix, M, N, K):
     """The last, partial wave of pair tiles runs as half-width units: exact on
-    integers, and within the fp32 bound of both the oracle and whole tiles."""
+    integers, and within the fp32 bound of the oracle (and, for the automatic
+    path, of whole tiles)."""
     rng = np.random.default_rng(M + K)
     A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
     B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
     C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
-    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N)
-    assert taken == "f32.3xtf32.pair.halves", taken
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=kind)
+    assert taken == prefix + ".halves", taken
     rows = oracle.sample_rows(M, block=64)
     assert np.array_equal(got[rows].astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0, rows=rows))
     A, B, C0 = operands(55 + M, M, N, K, K, N, N, np.float32)
-    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
-    whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=5)
-    assert t2 == "f32.3xtf32.pair"
+    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind)
     check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N, rows=rows)
-    bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
-    assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
+    if kind == 0:
+        whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=5)
+        assert t2 == "f32.3xf16.pair"
+        bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
+        assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 65536), (300, 260, 1), (257, 1000, 64), (3000, 1, 4)])
@@ -174,13 +203,11 @@ def test_fp32_extreme_dimensions(M, N, K):
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
 
 
-# ---------------------------------------------------------------- 3xTF32 K slices (few tiles)
-KSPLIT = "f32.3xtf32.pair.ksplit"
-
-
-@pytest.mark.parametrize("M,N,K", [(1000, 1100, 4000), (256, 256, 2048), (513, 1025, 4100),
+# ---------------------------------------------------------------- K slices (few tiles)
+@pytest.mark.parametrize("kind,prefix", KINDS)
+@pytest.mark.parametrize("M,N,K", [(1000, 1100, 4000), (256, 256, 4096), (513, 1025, 4100),
                                    (300, 300, 8200)])
-def test_3xtf32_k_slices(M, N, K):
+def test_split_k_slices(kind, prefix, M, N, K):
     """Few pair tiles and a long K: every tile is cut into K slices whose fp32
     partial sums the last slice to finish adds up.  Exact on integers; within
     the fp32 bound of the oracle and of whole-K units; bit-identical run to
@@ -189,55 +216,58 @@ def test_3xtf32_k_slices(M, N, K):
     A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
     B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
     C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
-    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N)
-    assert taken == KSPLIT, taken
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=kind)
+    assert taken == prefix + ".ksplit", taken
     assert np.array_equal(got.astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0))
     A, B, C0 = operands(606 + M + K, M, N, K, K, N, N, np.float32)
-    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
-    again, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
+    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind)
+    again, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind)
     assert np.array_equal(got, again)
     check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N)
-    whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, splits=1)
+    whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind, splits=1)
     assert not t2.endswith(".ksplit"), t2
     bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
     assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
 
 
+@pytest.mark.parametrize("kind,prefix", KINDS)
 @pytest.mark.parametrize("splits", [2, 3, 7, 16])
-def test_3xtf32_forced_slice_counts(splits):
+def test_split_forced_slice_counts(kind, prefix, splits):
     """Any slice count (slices are whole 4-k-block chunks; a count that would
     leave a slice empty is reduced): parity with the oracle, NaN-filled C with
     beta = 0 never read."""
-    M, N, K = 700, 900, 1500
+    M, N, K = 700, 900, 3000
     A, B, C0 = operands(707 + splits, M, N, K, K, N, N, np.float32, c_fill="nan")
-    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, splits=splits)
-    assert taken == KSPLIT, taken
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=kind, splits=splits)
+    assert taken == prefix + ".ksplit", taken
     check("f32", got, A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
 
 
-def test_3xtf32_k_slices_padded_ldc():
+@pytest.mark.parametrize("kind,prefix", KINDS)
+def test_split_k_slices_padded_ldc(kind, prefix):
     """Sliced tiles with ldc > N: the padding of C stays untouched."""
-    M, N, K, ldc = 600, 700, 2000, 712
+    M, N, K, ldc = 600, 700, 4000, 712
     A, B, C0 = operands(808, M, N, K, K, N, ldc, np.float32)
-    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc)
-    assert taken == KSPLIT, taken
+    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc, path=kind)
+    assert taken == prefix + ".ksplit", taken
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, ldc)
     assert padding_untouched(got, C0, N)
 
 
+@pytest.mark.parametrize("kind,prefix", KINDS)
 @pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (256, 256, 256), (1000, 1100, 900)])
-def test_3xtf32_short_k_keeps_whole_units(M, N, K):
+def test_split_short_k_keeps_whole_units(kind, prefix, M, N, K):
     """Few tiles with a short K: slicing would cost more in its fix-up than it
     saves, so the tiles run as whole-K half-width units."""
     A, B, C0 = operands(909 + K, M, N, K, K, N, N, np.float32)
-    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
-    assert taken == "f32.3xtf32.pair.halves", taken
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=kind)
+    assert taken == prefix + ".halves", taken
     check("f32", got, A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
 
 
 @pytest.mark.parametrize("M,N,K,expect", [
-    (16, 8192, 1024, "f32.3xtf32"), (1, 4096, 512, "f32.3xtf32"), (200, 200, 200, "f32.3xtf32"),
-    (16, 16, 4096, "f32.3xtf32"), (1024, 1024, 16, "f32.ffma"), (300, 260, 1, "f32.ffma"),
+    (16, 8192, 1024, "f32.3xf16"), (1, 4096, 512, "f32.3xf16"), (200, 200, 200, "f32.3xf16"),
+    (16, 16, 4096, "f32.3xf16"), (1024, 1024, 16, "f32.ffma"), (300, 260, 1, "f32.ffma"),
 ])
 def test_fp32_path_choice_small_and_skinny(M, N, K, expect):
     """K >= 64 takes the tensor cores whatever M and N (skinny and tiny shapes

@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 
 AUTO, MANUAL, SPLITK = 0, 2, 3
 NO_TAIL, NO_PAIR, TAIL2, SK, SK_ALL = 5, 6, 9, 10, 11
-FFMA_ONLY, TF32 = 7, 8
+FFMA_ONLY, TF32, F16X3 = 7, 8, 16
 
 # values of C at and near the top of the half range and at a spacing-2 binade
 EDGE_C = np.array([65504, -65504, 65472, -65472, 65440, 32768, -32768, 2048, -2048, 1024, 0],
@@ -164,11 +164,12 @@ def test_host_form_overflow():
     assert np.array_equal(pC.numpy().view(np.uint16), want.view(np.uint16))
 
 
-@pytest.mark.parametrize("path", [FFMA_ONLY, TF32])
+@pytest.mark.parametrize("path", [FFMA_ONLY, TF32, F16X3])
 def test_fp32_non_finite_operands(path):
-    """fp32: the FFMA kernel follows IEEE exactly.  The 3xTF32 path splits each
-    operand into a tf32 part and a remainder (Inf - Inf = NaN for an infinite
-    operand), so an output that meets an infinite operand is NaN there: it is
+    """fp32: the FFMA kernel follows IEEE exactly.  The tensor-core paths split
+    each operand into a part and a remainder (Inf - Inf = NaN for an infinite
+    operand; 3xFP16 also leaves the row or column of an infinite operand
+    unscaled), so an output that meets an infinite operand is NaN there: it is
     still non-finite, and every other output is exact."""
     M, N, K = 300, 400, 200
     A, B, C0 = _operands(9, M, N, K, dtype=np.float32)
@@ -186,4 +187,4 @@ def test_fp32_non_finite_operands(path):
         assert np.array_equal(np.isnan(g), np.isnan(ref))
         assert np.array_equal(g[np.isinf(ref)], ref[np.isinf(ref)])
     else:
-        assert taken.startswith("f32.3xtf32")
+        assert taken.startswith("f32.3xtf32" if path == TF32 else "f32.3xf16"), taken
