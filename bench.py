@@ -517,8 +517,9 @@ def run_ours(args, rank, world):
                            "gb_s": round(gbs, 1), "frac_tensor": round(tf / peak16_local, 3),
                            "frac_hbm": round(gbs / hbm, 3), "kernel_path": g.last_path()})
             del eA, eB, eC
-        # the fp32 square configurations below 4096 (4096 is the fp32 leg above)
-        ceiling32 = peak16_local * (1.1 / 2.25) / 3.0
+        # the fp32 square configurations below 4096 (4096 is the fp32 leg
+        # above); each one's fraction of its own kernel's ceiling is added
+        # once the tf32 rate has been measured
         for n in (256, 512, 1024, 2048):
             seed_s = synthetic.config_seed(1)
             sA, _ = _fill_device((n, n), np.float32, seed_s, synthetic.STREAM_A)
@@ -530,7 +531,6 @@ def run_ours(args, rank, world):
             tf = 2.0 * n ** 3 / (t * 1e-3) / 1e12
             squares.append({"workload": "fp32 SGEMM %d^3, alpha=1 beta=0" % n,
                             "us": round(t * 1e3, 2), "tflops": round(tf, 2),
-                            "frac_3xtf32_ceiling": round(tf / ceiling32, 4),
                             "kernel_path": g.last_path()})
             del sA, sB, sC
         del fA, fB, fC
@@ -568,11 +568,29 @@ def run_ours(args, rank, world):
     peak16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_ffma = sm_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     traffic = _profiled_traffic("tc_f16_4096")
-    if path32.startswith("f32.3xtf32"):
-        # three tf32 tensor products per fp32 multiply-add: the fp32 ceiling is
-        # a third of the dense tf32 rate (measured in this run when possible,
-        # else the bf16 peak x the nominal tf32/bf16 ratio of 1.1/2.25)
-        nominal32 = peak16 * (1.1 / 2.25) / 3.0
+    # ceilings of the two split-operand fp32 kernels: three tensor products per
+    # fp32 multiply-add, so a third of the dense fp16 rate (3xFP16; the
+    # measured bf16 burst, the same tensor rate) or of the dense tf32 rate
+    # (3xTF32: measured in this run when possible, else the bf16 peak x the
+    # nominal tf32/bf16 ratio 1.1/2.25)
+    ceil_f16x3 = peak16 / 3.0
+    nominal32 = peak16 * (1.1 / 2.25) / 3.0
+    ceil_tf32x3 = tf32_meas / 3.0 if tf32_meas else nominal32
+    for sq in squares:
+        c = ceil_f16x3 if sq["kernel_path"].startswith("f32.3xf16") else (
+            ceil_tf32x3 if sq["kernel_path"].startswith("f32.3xtf32") else None)
+        sq["frac_ceiling"] = round(sq["tflops"] / c, 4) if c else None
+    if path32.startswith("f32.3xf16"):
+        peak32 = ceil_f16x3
+        roof32 = {"bound": "tensor", "achieved": round(tflops32, 2), "peak": round(peak32, 2),
+                  "unit": "TFLOP/s", "frac": round(tflops32 / peak32, 4),
+                  "traffic": _profiled_traffic("sgemm_3xf16_4096"),
+                  "peak_source": ("%s bf16 dense burst (the same tensor rate as fp16) / 3 fp16 "
+                                  "products per fp32 FLOP" % peaks_src),
+                  "launches_per_step": launches32,
+                  "note": "time includes the operand-split pre-passes",
+                  "vs_ffma_peak": round(tflops32 / peak_ffma, 3)}
+    elif path32.startswith("f32.3xtf32"):
         if tf32_meas:
             peak32 = tf32_meas / 3.0
             src32 = ("dense tf32 rate measured in this run (torch.matmul fp32 with tf32 allowed, "

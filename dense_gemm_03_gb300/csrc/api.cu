@@ -853,11 +853,16 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
   // elements: measured faster than the FFMA kernel at every M and N tried,
   // skinny and tiny shapes included (3xTF32: 16 x 8192 x 8192 274 us against
   // 830 us; 128^3: 14 us against 18 us); a shorter K stays on the FFMA kernel.
-  // The parts are scaled halves (3xFP16, twice the tf32 rate) unless 3xTF32 is
-  // forced (path 8); path 16 forces 3xFP16.
+  // The parts are scaled halves (3xFP16, twice the tf32 rate) once the
+  // 256 x 256 tiles fill every CTA pair at least once; with fewer tiles the
+  // kernel runs at the pace of its loads, not of its MMAs, and the 3xFP16
+  // pre-pass (a column-maximum pass over B before B's split) costs more than
+  // it saves (1024^3: 53 us against 39 us for 3xTF32; 2048^3: 87 against 82;
+  // 4096^3: 334 against 500).  Path 8 forces 3xTF32, path 16 3xFP16.
   if (force != 4 && force != 7 && (force == 8 || force == 16 || K >= 64)) {
-    const bool x16 = force != 8;
     const int pairs = sgemm_3xtf32_max_pairs();
+    const long long all_tiles = 1ll * ((M + 255) / 256) * ((N + 255) / 256);
+    const bool x16 = force == 16 || (force != 8 && pairs > 0 && all_tiles >= pairs);
     auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
     const long long K2 = (K + 3) / 4 * 4;
     const long long lda2 = (K + 7) / 8 * 8, ldb2 = (N + 7) / 8 * 8;

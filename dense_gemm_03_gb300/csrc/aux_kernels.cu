@@ -455,18 +455,20 @@ __device__ __forceinline__ void f16x3_column_max(const float* __restrict__ B, lo
   }
 }
 
-// First launch: blocks [0, grid_a) split the rows of A, the others take the
-// column maxima of B.
+// First launch: the last grid_a blocks split the rows of A, the others take
+// the column maxima of B.
 __global__ void f16x3_split_a_kernel(const float* __restrict__ A, long long lda,
                                      uint16_t* __restrict__ A1, uint16_t* __restrict__ A2,
                                      long long lda2, int* __restrict__ ea, const float* __restrict__ B,
                                      long long ldb, unsigned int* __restrict__ colmax, int M, int N,
                                      int K, int grid_a) {
+  // the column-maximum blocks come first, so they start in the first wave
   __shared__ float red[8];
-  if (static_cast<int>(blockIdx.x) < grid_a)
-    f16x3_split_rows(A, lda, A1, A2, lda2, ea, M, K, blockIdx.x, grid_a, red);
+  const int grid_b = static_cast<int>(gridDim.x) - grid_a;
+  if (static_cast<int>(blockIdx.x) >= grid_b)
+    f16x3_split_rows(A, lda, A1, A2, lda2, ea, M, K, blockIdx.x - grid_b, grid_a, red);
   else
-    f16x3_column_max(B, ldb, colmax, K, N, blockIdx.x - grid_a, gridDim.x - grid_a);
+    f16x3_column_max(B, ldb, colmax, K, N, blockIdx.x, grid_b);
   griddep_launch_dependents();
 }
 

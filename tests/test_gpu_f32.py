@@ -58,10 +58,11 @@ def test_leading_dimensions(M, N, K, lda, ldb, ldc):
     assert taken == ("f32.ffma.vec" if vec else "f32.ffma.scalar")
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
     assert padding_untouched(got, C0, N)
-    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
-    assert taken.startswith("f32.3xf16.pair"), taken
-    check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
-    assert padding_untouched(got, C0, N)
+    for path, prefix in ((0, "f32.3xtf32.pair"), (16, "f32.3xf16.pair")):
+        got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc, path=path)
+        assert taken.startswith(prefix), taken
+        check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
+        assert padding_untouched(got, C0, N)
 
 
 def test_alpha_zero_and_K_zero():
@@ -85,9 +86,10 @@ def test_deterministic():
 
 # ---------------------------------------------------------------- tensor-core paths (split operands)
 FFMA_ONLY, TF32_FORCED, F16X3_FORCED = 7, 8, 16
-# (forced path, path prefix): the automatic choice takes 3xFP16 (scaled half
-# parts, kind::f16); path 8 forces 3xTF32 (tf32 parts, kind::tf32)
-KINDS = [(0, "f32.3xf16.pair"), (TF32_FORCED, "f32.3xtf32.pair")]
+# (forced path, path prefix): path 16 forces 3xFP16 (scaled half parts,
+# kind::f16), path 8 3xTF32 (tf32 parts, kind::tf32); the automatic choice
+# between them is tested on its own below
+KINDS = [(F16X3_FORCED, "f32.3xf16.pair"), (TF32_FORCED, "f32.3xtf32.pair")]
 
 
 @pytest.mark.parametrize("kind,prefix", KINDS)
@@ -96,9 +98,8 @@ KINDS = [(0, "f32.3xf16.pair"), (TF32_FORCED, "f32.3xtf32.pair")]
 @pytest.mark.parametrize("alpha,beta,c_fill", [(1.0, 0.0, "nan"), (1.5, 0.5, "uniform"),
                                                (0.75, -0.25, "uniform")])
 def test_split_parity(kind, prefix, M, N, K, alpha, beta, c_fill):
-    path = kind if kind else F16X3_FORCED   # K < 64 takes the FFMA kernel unless forced
     A, B, C0 = operands(900 + M + N + K, M, N, K, K, N, N, np.float32, c_fill=c_fill)
-    got, taken = run("f32", A, B, C0, alpha, beta, M, N, K, K, N, N, path=path)
+    got, taken = run("f32", A, B, C0, alpha, beta, M, N, K, K, N, N, path=kind)
     assert taken.startswith(prefix), taken
     check("f32", got, A, B, C0, alpha, beta, M, N, K, K, N, N)
 
@@ -164,7 +165,7 @@ def test_f16x3_scaled_rows_and_columns():
     A = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-60, 61, (M, 1)))).astype(np.float32)
     B = (rng.standard_normal((K, N)) * np.exp2(rng.integers(-60, 61, (1, N)))).astype(np.float32)
     C0 = np.zeros((M, N), np.float32)
-    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N)
+    got, taken = run("f32", A, B, C0, 1.0, 0.0, M, N, K, K, N, N, path=F16X3_FORCED)
     assert taken.startswith("f32.3xf16.pair"), taken
     ref = oracle.gemm(A, B, None, 1.0, 0.0)
     per = 1e-6 * K * np.abs(A).max(axis=1)[:, None] * np.abs(B).max(axis=0)[None, :]
@@ -189,7 +190,7 @@ def test_split_half_width_tail(kind, prefix, M, N, K):
     A, B, C0 = operands(55 + M, M, N, K, K, N, N, np.float32)
     got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind)
     check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N, rows=rows)
-    if kind == 0:
+    if kind == F16X3_FORCED:   # these shapes have more tiles than pairs: automatic 3xFP16
         whole, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=5)
         assert t2 == "f32.3xf16.pair"
         bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
@@ -266,16 +267,20 @@ def test_split_short_k_keeps_whole_units(kind, prefix, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,expect", [
-    (16, 8192, 1024, "f32.3xf16"), (1, 4096, 512, "f32.3xf16"), (200, 200, 200, "f32.3xf16"),
-    (16, 16, 4096, "f32.3xf16"), (1024, 1024, 16, "f32.ffma"), (300, 260, 1, "f32.ffma"),
+    (16, 8192, 1024, "f32.3xtf32"), (1, 4096, 512, "f32.3xtf32"), (200, 200, 200, "f32.3xtf32"),
+    (16, 16, 4096, "f32.3xtf32"), (1024, 1024, 16, "f32.ffma"), (300, 260, 1, "f32.ffma"),
+    (2560, 2048, 64, "f32.3xf16"), (2048, 2048, 2048, "f32.3xtf32"),
 ])
 def test_fp32_path_choice_small_and_skinny(M, N, K, expect):
     """K >= 64 takes the tensor cores whatever M and N (skinny and tiny shapes
-    included); a shorter K takes the FFMA kernel.  Parity either way."""
+    included): 3xFP16 once the 256 x 256 tiles fill every CTA pair (80 tiles
+    here), 3xTF32 with fewer; a shorter K takes the FFMA kernel.  Parity
+    either way."""
     A, B, C0 = operands(3030 + M + K, M, N, K, K, N, N, np.float32)
     got, taken = run("f32", A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
     assert taken.startswith(expect), taken
-    check("f32", got, A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
+    rows = oracle.sample_rows(M, block=64) if M * N * K > 2e9 else None
+    check("f32", got, A, B, C0, 1.25, -0.5, M, N, K, K, N, N, rows=rows)
 
 
 @pytest.mark.parametrize("M,N,K,ldc", [(700, 900, 500, 900), (2600, 1000, 700, 1004)])
