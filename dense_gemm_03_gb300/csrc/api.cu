@@ -853,16 +853,17 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
   // elements: measured faster than the FFMA kernel at every M and N tried,
   // skinny and tiny shapes included (3xTF32: 16 x 8192 x 8192 274 us against
   // 830 us; 128^3: 14 us against 18 us); a shorter K stays on the FFMA kernel.
-  // The parts are scaled halves (3xFP16, twice the tf32 rate) once the
-  // 256 x 256 tiles fill every CTA pair at least once; with fewer tiles the
-  // kernel runs at the pace of its loads, not of its MMAs, and the 3xFP16
-  // pre-pass (a column-maximum pass over B before B's split) costs more than
-  // it saves (1024^3: 53 us against 39 us for 3xTF32; 2048^3: 87 against 82;
-  // 4096^3: 334 against 500).  Path 8 forces 3xTF32, path 16 3xFP16.
+  // The parts are scaled halves (3xFP16, twice the tf32 rate) unless the
+  // product is tiny (M*N*K at most 256^3), where the 3xTF32 form's simpler
+  // pre-pass is as fast or faster (measured, same box, L2 flushed: 128^3
+  // 17.0 us against 14.9 for 3xTF32, 200^3 19.0 / 17.0, 256^3 19.0 / 18.7,
+  // 512^3 21.5 / 25.2, 1024^3 29.6 / 39.5, 16 x 8192 x 1024 37.5 / 53.9,
+  // 8192 x 64 x 4096 111 / 136, 4096^3 302 / 502).  Path 8 forces 3xTF32,
+  // path 16 3xFP16.
   if (force != 4 && force != 7 && (force == 8 || force == 16 || K >= 64)) {
     const int pairs = sgemm_3xtf32_max_pairs();
-    const long long all_tiles = 1ll * ((M + 255) / 256) * ((N + 255) / 256);
-    const bool x16 = force == 16 || (force != 8 && pairs > 0 && all_tiles >= pairs);
+    const bool x16 = force == 16 ||
+                     (force != 8 && static_cast<double>(M) * N * K > 256.0 * 256.0 * 256.0);
     auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
     const long long K2 = (K + 3) / 4 * 4;
     const long long lda2 = (K + 7) / 8 * 8, ldb2 = (N + 7) / 8 * 8;
@@ -870,9 +871,12 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
                               : static_cast<size_t>(M) * K2 * 4;
     const size_t b_part = x16 ? round256(static_cast<size_t>(K) * ldb2 * 2)
                               : static_cast<size_t>(N) * K2 * 4;
-    const size_t e_bytes = x16 ? round256(static_cast<size_t>(M) * 4) +
-                                     2 * round256((static_cast<size_t>(N) + 8) * 4)
-                               : 0;
+    // 3xFP16 exponents per K chunk: ea M x kchunks, eb kchunks x ldeb
+    const int kchunks = (K + kF16x3ChunkK - 1) / kF16x3ChunkK;
+    const long long ldeb = (N + 3) / 4 * 4 + 4;
+    const size_t ea_bytes = round256(static_cast<size_t>(M) * kchunks * 4);
+    const size_t e_bytes =
+        x16 ? ea_bytes + round256(static_cast<size_t>(kchunks) * static_cast<size_t>(ldeb) * 4) : 0;
     const size_t need = 2 * (a_part + b_part) + e_bytes + 1024;
     if (pairs > 0 && need <= (static_cast<size_t>(16) << 30)) {
       uint8_t* buf = nullptr;
@@ -893,18 +897,17 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
         parts.B2 = reinterpret_cast<uint16_t*>(buf + 2 * a_part + b_part);
         uint8_t* const eptr = buf + 2 * (a_part + b_part);
         parts.ea = reinterpret_cast<int*>(eptr);
-        parts.eb = reinterpret_cast<int*>(eptr + round256(static_cast<size_t>(M) * 4));
-        parts.colmax = reinterpret_cast<unsigned int*>(
-            eptr + round256(static_cast<size_t>(M) * 4) + round256((static_cast<size_t>(N) + 8) * 4));
+        parts.eb = reinterpret_cast<int*>(eptr + ea_bytes);
+        parts.ldeb = ldeb;
         parts.lda2 = lda2;
         parts.ldb2 = ldb2;
-        // first launch: one block per row of A, and B's column maxima over
-        // bands of 16 rows; second: B's parts, 4 columns per thread over a
-        // share of rows
-        const int grid_a = static_cast<int>(std::min<long long>(M, 8ll * d->sm_count));
-        const int grid_bmax = scale_grid(*d, ((N + 3) / 4) * ((K + 15) / 16ll));
-        const int grid_b = scale_grid(*d, ((N + 3) / 4) * static_cast<long long>(K));
-        if (launch_f16x3_split(A, lda, B, ldb, parts, M, N, K, grid_a, grid_bmax, grid_b, stream) !=
+        // one launch: a block per (K chunk, 128 columns) of B, a warp per
+        // (row, K chunk) of A
+        const long long b_items = 1ll * kchunks * ((N + 127) / 128);
+        const int grid_b = static_cast<int>(std::min<long long>(b_items, 2ll * d->sm_count));
+        const int grid_a = static_cast<int>(
+            std::max(1ll, std::min<long long>((1ll * M * kchunks + 31) / 32, 2ll * d->sm_count)));
+        if (launch_f16x3_split(A, lda, B, ldb, parts, M, N, K, grid_a, grid_b, stream) !=
             cudaSuccess)
           return GEMM_ERR_CUDA;
         // k-blocks of 32 halves: A parts in 64-byte rows, B parts as 64-column
@@ -917,6 +920,8 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
         if (int rc = make_map_f16(&m4, parts.B2, K, N, ldb2, 64, 32)) return rc;
         t.ea = parts.ea;
         t.eb = parts.eb;
+        t.ldeb = ldeb;
+        t.kchunks = kchunks;
         t.kb_total = (K + 31) / 32;
       } else {
         float* Ab = reinterpret_cast<float*>(buf);

@@ -310,9 +310,11 @@ __global__ void split_tf32_ab_kernel(const float* __restrict__ A, long long lda,
 // x * 2^e = h1 + h2 + r with h1 = half(x * 2^e) and h2 = half(x * 2^e - h1),
 // both rounded to nearest: |r| <= 2^-22 |x * 2^e| (the same 11 + 11
 // significand bits as the tf32 split).  e is a power-of-two exponent per row
-// of A and per column of B, chosen so that the largest magnitude of the row
-// (column) lands in [2^14, 2^15): no part overflows half, and the scaling and
-// its undoing in the epilogue are exact.
+// of A and per column of B within each K chunk of kF16x3ChunkK (the GEMM's
+// accumulation chunk), chosen so that the largest magnitude of the row's
+// (column's) chunk lands in [2^14, 2^15): no part overflows half, and the
+// scaling and its undoing, chunk by chunk in the GEMM, are exact.  Chunks make
+// every split local: one pass over each operand, no pass for maxima first.
 
 // Exponent that takes the largest magnitude m into [2^14, 2^15); 0 when m is
 // zero or not finite (the parts then carry the Inf or NaN).
@@ -336,185 +338,144 @@ __device__ __forceinline__ uint32_t f16x3_parts(float x, float2 f, uint32_t* lo)
   return __half_as_ushort(h1);
 }
 
-// Rows of A, one block of 256 threads per row (grid-stride over rows): the
-// row's largest magnitude, then its two parts with that row's exponent;
-// ea[row] = the exponent.  A row of up to kRowRegs * 256 elements is read once
-// and kept in registers between the two steps; with many rows in flight a
-// second read of each row missed L2 and doubled the traffic.  Longer rows
-// are read a second time.  A is read with the streaming hint (used once), so
-// that B, read by the other blocks of this launch and again by the next one,
-// stays in L2.
-constexpr int kRowVec = 8;   // float4 per thread held in registers: K <= 8192
-__device__ __forceinline__ void f16x3_split_rows(const float* __restrict__ A, long long lda,
-                                                 uint16_t* __restrict__ A1,
-                                                 uint16_t* __restrict__ A2, long long ld2,
-                                                 int* __restrict__ ea, int M, int K,
-                                                 long long block, long long nblocks,
-                                                 float* red) {
-  const int tid = static_cast<int>(threadIdx.x);
-  const int lane = tid & 31, warp = tid >> 5;
+// Four consecutive floats from a[k..k+3], zero past n (16-byte load when vec).
+__device__ __forceinline__ float4 f16x3_load4(const float* a, int k, int n, bool vec) {
+  if (vec && k + 4 <= n) return __ldcs(reinterpret_cast<const float4*>(a + k));
+  float x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = (k + i < n) ? __ldcs(a + k + i) : 0.0f;
+  return make_float4(x[0], x[1], x[2], x[3]);
+}
+
+// The two parts of four values with the factors f, as two 8-byte stores.
+__device__ __forceinline__ void f16x3_put4(uint16_t* d1, uint16_t* d2, float4 v, float2 f) {
+  uint32_t h[4], l[4];
+  h[0] = f16x3_parts(v.x, f, &l[0]);
+  h[1] = f16x3_parts(v.y, f, &l[1]);
+  h[2] = f16x3_parts(v.z, f, &l[2]);
+  h[3] = f16x3_parts(v.w, f, &l[3]);
+  __stcs(reinterpret_cast<uint2*>(d1), make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16)));
+  __stcs(reinterpret_cast<uint2*>(d2), make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16)));
+}
+
+__device__ __forceinline__ void f16x3_put4(uint16_t* d1, uint16_t* d2, float4 v, const float2 (&f)[4]) {
+  uint32_t h[4], l[4];
+  h[0] = f16x3_parts(v.x, f[0], &l[0]);
+  h[1] = f16x3_parts(v.y, f[1], &l[1]);
+  h[2] = f16x3_parts(v.z, f[2], &l[2]);
+  h[3] = f16x3_parts(v.w, f[3], &l[3]);
+  __stcs(reinterpret_cast<uint2*>(d1), make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16)));
+  __stcs(reinterpret_cast<uint2*>(d2), make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16)));
+}
+
+// A, one warp per (row, chunk) item: the chunk's 256 values are two float4s
+// per lane, held in registers between the maximum and the split; ea[row][c] =
+// the exponent.
+__device__ __forceinline__ void f16x3_split_a(const float* __restrict__ A, long long lda,
+                                              uint16_t* __restrict__ A1, uint16_t* __restrict__ A2,
+                                              long long ld2, int* __restrict__ ea, int M, int K,
+                                              int kc, long long block, long long nblocks) {
+  static_assert(kF16x3ChunkK == 256, "a chunk is two float4s per lane");
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const long long warps = nblocks * (blockDim.x / 32);
   const bool vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0;
-  const bool held = K <= kRowVec * 4 * 256;
-  auto load4 = [&](const float* a, int k) -> float4 {
-    if (vec && k + 4 <= K) return __ldcs(reinterpret_cast<const float4*>(a + k));
-    float x[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = (k + i < K) ? __ldcs(a + k + i) : 0.0f;
-    return make_float4(x[0], x[1], x[2], x[3]);
-  };
-  for (long long r = block; r < M; r += nblocks) {
+  const long long items = static_cast<long long>(M) * kc;
+  for (long long it = block * (blockDim.x / 32) + threadIdx.x / 32; it < items; it += warps) {
+    const int r = static_cast<int>(it / kc), c = static_cast<int>(it % kc);
     const float* const a = A + r * lda;
-    float4 v[kRowVec];
-    float m = 0.0f;
-    if (held) {
-#pragma unroll
-      for (int i = 0; i < kRowVec; ++i) {
-        const int k = 4 * (tid + 256 * i);
-        v[i] = k < K ? load4(a, k) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int i = 0; i < kRowVec; ++i)
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-    } else {
-      for (int k = 4 * tid; k < K; k += 1024) {
-        const float4 w = load4(a, k);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
-      }
-    }
-    // block maximum (NaN does not propagate through fmaxf: a NaN element is
-    // carried into its parts by the split below whatever the exponent)
+    const int k0 = c * kF16x3ChunkK + 4 * lane, k1 = k0 + 128;
+    const float4 v0 = f16x3_load4(a, k0, K, vec), v1 = f16x3_load4(a, k1, K, vec);
+    float m = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                    fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    m = red[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
-    __syncthreads();   // red is reused by the next row
     const int e = f16x3_exponent(m);
     const float2 f = f16x3_factors(e);
-    if (tid == 0) ea[r] = e;
+    if (lane == 0) ea[static_cast<long long>(r) * kc + c] = e;
     uint16_t* const d1 = A1 + r * ld2;
     uint16_t* const d2 = A2 + r * ld2;
-    // groups of 4 elements: one 8-byte store per part (ld2 % 8 == 0; the
-    // padding columns of the last group get zeros)
-    auto put = [&](int k, float4 w) {
-      uint32_t h[4], l[4];
-      h[0] = f16x3_parts(w.x, f, &l[0]);
-      h[1] = f16x3_parts(w.y, f, &l[1]);
-      h[2] = f16x3_parts(w.z, f, &l[2]);
-      h[3] = f16x3_parts(w.w, f, &l[3]);
-      __stcs(reinterpret_cast<uint2*>(d1 + k), make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16)));
-      __stcs(reinterpret_cast<uint2*>(d2 + k), make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16)));
-    };
-    if (held) {
-#pragma unroll
-      for (int i = 0; i < kRowVec; ++i) {
-        const int k = 4 * (tid + 256 * i);
-        if (k < K) put(k, v[i]);
-      }
-    } else {
-      for (int k = 4 * tid; k < K; k += 1024) put(k, load4(a, k));
-    }
+    // groups of 4 elements (ld2 % 8 == 0; a group that crosses K gets zeros)
+    if (k0 < K) f16x3_put4(d1 + k0, d2 + k0, v0, f);
+    if (k1 < K) f16x3_put4(d1 + k1, d2 + k1, v1, f);
   }
 }
 
-// Largest magnitude of each column of B (K x N): each thread takes 4
-// consecutive columns over a band of 16 rows (all 16 loads in flight) and
-// folds its maxima into colmax (the magnitudes' bit patterns, which order
-// like the values; colmax starts at zero).
-__device__ __forceinline__ void f16x3_column_max(const float* __restrict__ B, long long ldb,
-                                                 unsigned int* __restrict__ colmax, int K, int N,
-                                                 long long block, long long nblocks) {
-  const long long groups = (N + 3) / 4;
-  const long long bands = (K + 15) / 16;
+// B, one block of kF16x3Threads threads per (chunk, 128 columns) item: warp w
+// takes the chunk's rows kRowsPerWarp * w .. + kRowsPerWarp - 1 (all its loads
+// in flight at once, held in registers), lane l columns 4l .. 4l + 3.  The
+// column maxima go through shared memory, then each thread writes the parts
+// of the values it holds; eb[c][col] = the exponent.  (With 256-thread blocks,
+// 32 rows a warp and a second read of B the item was latency-bound.)
+constexpr int kF16x3Threads = 1024;
+constexpr int kF16x3Warps = kF16x3Threads / 32;
+constexpr int kRowsPerWarp = kF16x3ChunkK / kF16x3Warps;
+__device__ __forceinline__ void f16x3_split_b(const float* __restrict__ B, long long ldb,
+                                              uint16_t* __restrict__ B1, uint16_t* __restrict__ B2,
+                                              long long ld2, int* __restrict__ eb, long long ldeb,
+                                              int K, int N, int kc, long long block,
+                                              long long nblocks, float (&red)[kF16x3Warps][128],
+                                              int (&es)[128]) {
+  const int tid = static_cast<int>(threadIdx.x);
+  const int lane = tid & 31, w = tid >> 5;
   const bool vec = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0;
-  for (long long g = block * blockDim.x + threadIdx.x; g < groups * bands;
-       g += nblocks * blockDim.x) {
-    const int c0 = static_cast<int>(g % groups) * 4;
-    const int k0 = static_cast<int>(g / groups) * 16;
+  const int groups = (N + 127) / 128;
+  const long long items = static_cast<long long>(kc) * groups;
+  for (long long it = block; it < items; it += nblocks) {
+    const int c = static_cast<int>(it / groups), g = static_cast<int>(it % groups);
+    const int col = g * 128 + 4 * lane;
+    const int r0 = c * kF16x3ChunkK + kRowsPerWarp * w;
+    float4 v[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+      v[i] = (r0 + i < K) ? f16x3_load4(B + static_cast<long long>(r0 + i) * ldb, col, N, vec)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
     float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 16
-    for (int i = 0; i < 16; ++i) {
-      const int k = k0 + i;
-      if (k >= K) break;
-      const float* const b = B + static_cast<long long>(k) * ldb + c0;
-      if (vec && c0 + 4 <= N) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(b));
-        m[0] = fmaxf(m[0], fabsf(v.x)); m[1] = fmaxf(m[1], fabsf(v.y));
-        m[2] = fmaxf(m[2], fabsf(v.z)); m[3] = fmaxf(m[3], fabsf(v.w));
-      } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (c0 + i < N) m[i] = fmaxf(m[i], fabsf(__ldg(b + i)));
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      m[0] = fmaxf(m[0], fabsf(v[i].x));
+      m[1] = fmaxf(m[1], fabsf(v[i].y));
+      m[2] = fmaxf(m[2], fabsf(v[i].z));
+      m[3] = fmaxf(m[3], fabsf(v[i].w));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) red[w][4 * lane + j] = m[j];
+    __syncthreads();
+    if (tid < 128) {
+      float mm = red[0][tid];
+#pragma unroll
+      for (int u = 1; u < kF16x3Warps; ++u) mm = fmaxf(mm, red[u][tid]);
+      const int e = f16x3_exponent(mm);
+      es[tid] = e;
+      if (g * 128 + tid < N) eb[c * ldeb + g * 128 + tid] = e;
+    }
+    __syncthreads();
+    if (col < N) {
+      float2 f[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = f16x3_factors(es[4 * lane + j]);
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {   // the rows' values are still in registers
+        const int k = r0 + i;
+        if (k < K) f16x3_put4(B1 + k * ld2 + col, B2 + k * ld2 + col, v[i], f);
       }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (c0 + i < N && m[i] > 0.0f) atomicMax(colmax + c0 + i, __float_as_uint(m[i]));
+    __syncthreads();   // red and es are reused by the next item
   }
 }
 
-// First launch: the last grid_a blocks split the rows of A, the others take
-// the column maxima of B.
-__global__ void f16x3_split_a_kernel(const float* __restrict__ A, long long lda,
-                                     uint16_t* __restrict__ A1, uint16_t* __restrict__ A2,
-                                     long long lda2, int* __restrict__ ea, const float* __restrict__ B,
-                                     long long ldb, unsigned int* __restrict__ colmax, int M, int N,
-                                     int K, int grid_a) {
-  // the column-maximum blocks come first, so they start in the first wave
-  __shared__ float red[8];
-  const int grid_b = static_cast<int>(gridDim.x) - grid_a;
-  if (static_cast<int>(blockIdx.x) >= grid_b)
-    f16x3_split_rows(A, lda, A1, A2, lda2, ea, M, K, blockIdx.x - grid_b, grid_a, red);
+// One launch: blocks [0, grid_b) split B, the others A.
+__global__ void __launch_bounds__(kF16x3Threads) f16x3_split_kernel(const float* __restrict__ A, long long lda,
+                                   const float* __restrict__ B, long long ldb, const F16x3Parts p,
+                                   int M, int N, int K, int grid_b) {
+  __shared__ float red[kF16x3Warps][128];
+  __shared__ int es[128];
+  const int kc = (K + kF16x3ChunkK - 1) / kF16x3ChunkK;
+  if (static_cast<int>(blockIdx.x) < grid_b)
+    f16x3_split_b(B, ldb, p.B1, p.B2, p.ldb2, p.eb, p.ldeb, K, N, kc, blockIdx.x, grid_b, red, es);
   else
-    f16x3_column_max(B, ldb, colmax, K, N, blockIdx.x, grid_b);
-  griddep_launch_dependents();
-}
-
-// Second launch: B's two parts with each column's exponent, 4 columns per
-// thread: each work item is one group of columns (its factors computed once)
-// and every per_group-th row; the items that start at row 0 write eb.  A grid
-// smaller than the column groups takes several items per thread.
-__global__ void f16x3_split_b_kernel(const float* __restrict__ B, long long ldb,
-                                     uint16_t* __restrict__ B1, uint16_t* __restrict__ B2,
-                                     long long ldb2, const unsigned int* __restrict__ colmax,
-                                     int* __restrict__ eb, int K, int N) {
-  griddep_wait();   // the column maxima of the launch before
-  const long long groups = (N + 3) / 4;
-  const bool vec = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0;
-  const long long threads = static_cast<long long>(gridDim.x) * blockDim.x;
-  const long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  // threads per column group: the rows are shared out among them
-  const long long per_group = max(1ll, threads / groups);
-  for (long long u = t; u < per_group * groups; u += threads) {
-  const int c0 = static_cast<int>(u % groups) * 4;
-  float2 f[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = (c0 + i < N) ? f16x3_exponent(__uint_as_float(__ldg(colmax + c0 + i))) : 0;
-    f[i] = f16x3_factors(e);
-    if (u < groups && c0 + i < N) eb[c0 + i] = e;
-  }
-#pragma unroll 4
-  for (long long k = u / groups; k < K; k += per_group) {
-    const float* const b = B + k * ldb + c0;
-    float x[4];
-    if (vec && c0 + 4 <= N) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(b));
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = (c0 + i < N) ? __ldg(b + i) : 0.0f;
-    }
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = f16x3_parts(x[i], f[i], &l[i]);
-    const long long o = k * ldb2 + c0;
-    *reinterpret_cast<uint2*>(B1 + o) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-    *reinterpret_cast<uint2*>(B2 + o) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
-  }
-  }
+    f16x3_split_a(A, lda, p.A1, p.A2, p.lda2, p.ea, M, K, kc, blockIdx.x - grid_b,
+                  gridDim.x - grid_b);
+  // as for the realignment: the GEMM launched next may be scheduled
   griddep_launch_dependents();
 }
 
@@ -584,28 +545,10 @@ cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float
 
 
 cudaError_t launch_f16x3_split(const float* A, long long lda, const float* B, long long ldb,
-                               const F16x3Parts& p, int M, int N, int K, int grid_a, int grid_bmax,
-                               int grid_b, cudaStream_t stream) {
-  if (cudaMemsetAsync(p.colmax, 0, static_cast<size_t>(N) * sizeof(unsigned int), stream) !=
-      cudaSuccess)
-    return cudaErrorUnknown;
-  f16x3_split_a_kernel<<<grid_a + grid_bmax, 256, 0, stream>>>(A, lda, p.A1, p.A2, p.lda2, p.ea, B,
-                                                               ldb, p.colmax, M, N, K, grid_a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  counted_launch(e);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid_b), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, f16x3_split_b_kernel, B, ldb, p.B1, p.B2, p.ldb2,
-                         static_cast<const unsigned int*>(p.colmax), p.eb, K, N);
-  if (e != cudaSuccess) return e;
+                               const F16x3Parts& p, int M, int N, int K, int grid_a, int grid_b,
+                               cudaStream_t stream) {
+  f16x3_split_kernel<<<grid_a + grid_b, kF16x3Threads, 0, stream>>>(A, lda, B, ldb, p, M, N, K,
+                                                                      grid_b);
   return counted_launch(cudaGetLastError());
 }
 

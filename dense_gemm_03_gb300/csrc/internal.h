@@ -177,22 +177,24 @@ cudaError_t launch_split_tf32_ab(const float* A, long long lda, float* Ab, float
                                  const float* B, long long ldb, float* Bb, float* Bs, long long ld2,
                                  int M, int N, int K, int grid_a, int grid_b, cudaStream_t stream);
 
-// The fp16 parts of the 3xFP16 SGEMM: x * 2^e = h1 + h2 (+ 2^-22 relative),
-// with e per row of A (ea) and per column of B (eb); A1, A2 are M x lda2,
-// B1, B2 are K x ldb2 (row-major, lda2 and ldb2 multiples of 8); colmax holds
-// B's column maxima between the two launches.
+// The fp16 parts of the 3xFP16 SGEMM, x * 2^e = h1 + h2 (+ 2^-22 relative):
+// 3xFP16 operand parts: A1, A2 (M x lda2 halves) and B1, B2 (K x ldb2), and
+// the power-of-two exponents they were scaled by, per K chunk of
+// kF16x3ChunkK: ea[row][chunk] (M x kchunks), eb[chunk][col] (kchunks x ldeb,
+// ldeb >= N + 4).
+constexpr int kF16x3ChunkK = 256;
 struct F16x3Parts {
   uint16_t *A1, *A2, *B1, *B2;
   long long lda2, ldb2;
   int* ea;
   int* eb;
-  unsigned int* colmax;
+  long long ldeb;
 };
-// Two launches (a memset of colmax first): A's rows and B's column maxima,
-// then B's parts (a programmatic dependent of the first).
+// One launch of 1024-thread blocks: blocks [0, grid_b) split B by (chunk,
+// 128 columns), the other grid_a blocks A by (row, chunk), one warp an item.
 cudaError_t launch_f16x3_split(const float* A, long long lda, const float* B, long long ldb,
                                const F16x3Parts& parts, int M, int N, int K, int grid_a,
-                               int grid_bmax, int grid_b, cudaStream_t stream);
+                               int grid_b, cudaStream_t stream);
 
 // 3xTF32 SGEMM on CTA pairs: C = alpha*(Ab*Bb + Ab*Bs + As*Bb) + beta*C with
 // the split operands dense and K-contiguous: A parts M x roundup(K,4), B parts
@@ -227,10 +229,13 @@ struct Tf32Args {
   unsigned long long* counters;     // [tile][rank][warp]: (epoch << 32) | arrivals
   unsigned int epoch;
   bool pdl;                         // host only: as TcArgs::pdl (after the split pre-pass)
-  // 3xFP16 only: the power-of-two exponent of each row of A and of each column
-  // of B (eb padded to a multiple of 4 entries) that the parts were scaled by
+  // 3xFP16 only: the power-of-two exponents the parts were scaled by, per K
+  // chunk of kF16x3ChunkK (the accumulation chunk): ea[row * kchunks + c],
+  // eb[c * ldeb + col] (ldeb >= N + 4)
   const int* ea;
   const int* eb;
+  long long ldeb;
+  int kchunks;
 };
 // tmBbh / tmBsh: the B parts with 64-row boxes, for the half-width units.
 cudaError_t launch_sgemm_3xtf32(const CUtensorMap& tmAb, const CUtensorMap& tmAs,

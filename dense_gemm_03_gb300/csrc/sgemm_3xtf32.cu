@@ -42,7 +42,9 @@
 // column blocks of 32 k-rows (128-byte swizzle, no transpose), chunks are 8
 // k-blocks (256 deep: a 128-deep chunk left the fold of the chunks into
 // registers, not the MMAs, setting the pace), and the
-// epilogue undoes the scaling (an exact multiply by 2^-(e_row + e_col)).
+// epilogue undoes the scaling chunk by chunk (the exponents are per 256-deep K
+// chunk; each chunk's sums are multiplied by 2^-(e_row + e_col) as they are
+// folded into the registers, exactly).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -75,6 +77,7 @@ constexpr int kEpiExpOff = kEpiOff + kEpiWarps * kEpiTileF4 * 16;
 constexpr int kSmemAlloc = kEpiExpOff + kEpiWarps * 32 * 16 + 1024;
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
+static_assert(kChunkKb * 32 == kF16x3ChunkK, "3xFP16 exponent chunks are the accumulation chunks");
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, DeviceStatus* st, int where) {
   if (mbar_try_wait(bar, parity)) return;
@@ -98,6 +101,20 @@ __device__ __forceinline__ void tmem_wait_regs32(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
+}
+
+// 32 lanes x 16 consecutive columns (the 3xFP16 fold: half the registers of
+// the 32-column load, which leaves room for the chunk's exponents).
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
 // Partial sums of one K slice for one epilogue warp: [32 column quads][32
@@ -148,20 +165,6 @@ __device__ __forceinline__ bool publish_slice(const Tf32Args& p, int u, int rank
   return true;
 }
 
-// Multiplies four values of the scaled 3xFP16 domain by 2^-E (exact unless a
-// result is subnormal or overflows).  When every E of the warp is within
-// +-126 -- all but extreme inputs -- 2^-E is a normal float and one multiply
-// does it; otherwise ldexpf.  The vote keeps the ldexpf code off the common
-// path: as a per-element select it made the whole store phase ~4x slower.
-// Warp-uniform calls only.
-__device__ __forceinline__ float4 unscale4(float4 v, int e_row, int4 ec) {
-  const int E0 = e_row + ec.x, E1 = e_row + ec.y, E2 = e_row + ec.z, E3 = e_row + ec.w;
-  auto in = [](int E) { return static_cast<unsigned>(E + 126) <= 252u; };
-  if (__all_sync(0xffffffffu, in(E0) && in(E1) && in(E2) && in(E3)))
-    return make_float4(v.x * __int_as_float((127 - E0) << 23), v.y * __int_as_float((127 - E1) << 23),
-                       v.z * __int_as_float((127 - E2) << 23), v.w * __int_as_float((127 - E3) << 23));
-  return make_float4(ldexpf(v.x, -E0), ldexpf(v.y, -E1), ldexpf(v.z, -E2), ldexpf(v.w, -E3));
-}
 
 template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -399,24 +402,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = row0 + lane;
       const int colw = n0 + h * wcols;
       const bool active = row0 < p.M && colw < p.N;   // warp-uniform
-      // 3xFP16: this row's exponent, and the exponents of the warp's columns
-      // into shared memory (lane l: columns colw + 4l .. +3) -- loaded now,
-      // while the MMAs run, since loads issued among the stores of C below
-      // would each wait a full round trip (that made the store phase ~8x
-      // slower)
-      int e_row = 0;
+      // 3xFP16: each chunk's sums leave the scaled domain as they are folded,
+      // multiplied by 2^-(e_row + e_col) with the chunk's exponents: e_row
+      // for the thread's row, and for the warp's columns 2^-e_col as float
+      // bits to add to 2^-e_row's (-(e_col << 23); lane l holds columns
+      // colw + 4l .. +3 in shared memory).  Both are read before the chunk's
+      // accumulator is waited for.  When every e_row + e_col of the warp is
+      // within +-126 the factor is one normal power of two and the fold one
+      // fused multiply-add (exact product, one rounding, as the plain add);
+      // otherwise two normal factors.
       int4* const e_col = reinterpret_cast<int4*>(base_ptr + kEpiExpOff) + ew * 32;
-      if (F16 && active) {
-        if (row < p.M) e_row = __ldg(p.ea + row);
-        if (colw + 4 * lane < p.N)   // eb holds N + 8 entries: the int4 stays inside
-          e_col[lane] = __ldg(reinterpret_cast<const int4*>(p.eb + colw + 4 * lane));
-        __syncwarp();
-      }
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
       for (int kc = kb0; kc < kb1; kc += kChunkKb, ++chunk) {
         const uint32_t buf = chunk & 1u, use = chunk >> 1;
+        int e_row = 0, rbits = 0;
+        bool fast = true;
+        if (F16 && active) {
+          const int ci = kc / kChunkKb;
+          if (row < p.M) e_row = __ldg(p.ea + static_cast<long long>(row) * p.kchunks + ci);
+          int4 ec = make_int4(0, 0, 0, 0);
+          if (4 * lane < wcols && colw + 4 * lane < p.N)   // eb rows hold N + 4 entries or more
+            ec = __ldg(reinterpret_cast<const int4*>(p.eb + ci * p.ldeb + colw + 4 * lane));
+          const int lo = __reduce_min_sync(0xffffffffu, min(min(ec.x, ec.y), min(ec.z, ec.w))) +
+                         __reduce_min_sync(0xffffffffu, e_row);
+          const int hi = __reduce_max_sync(0xffffffffu, max(max(ec.x, ec.y), max(ec.z, ec.w))) +
+                         __reduce_max_sync(0xffffffffu, e_row);
+          fast = lo >= -126 && hi <= 126;
+          rbits = (127 - e_row) << 23;
+          e_col[lane] = make_int4(-(ec.x << 23), -(ec.y << 23), -(ec.z << 23), -(ec.w << 23));
+          __syncwarp();
+        }
         if (!wait_parity(accf_bar(buf), use & 1u, limit, st, 28)) {
           ok = false;
           break;
@@ -428,11 +445,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kCols / 32; ++k) {
             if (32 * k >= wcols) break;
-            uint32_t t[32];
-            tmem_ld_32x32b_x32(tbase + 32 * k, t);
-            tmem_wait_regs32(t);
+            if (!F16) {
+              uint32_t t[32];
+              tmem_ld_32x32b_x32(tbase + 32 * k, t);
+              tmem_wait_regs32(t);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * k + j] += __uint_as_float(t[j]);
+              for (int j = 0; j < 32; ++j) acc[32 * k + j] += __uint_as_float(t[j]);
+              continue;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {   // 16 columns at a time
+              uint32_t t[16];
+              tmem_ld16_wait(tbase + 32 * k + 16 * hh, t);
+              if (fast) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const int4 cb = e_col[8 * k + 4 * hh + g];
+                  const int b4[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    float& a = acc[32 * k + 16 * hh + 4 * g + i];
+                    a = fmaf(__uint_as_float(t[4 * g + i]), __int_as_float(rbits + b4[i]), a);
+                  }
+                }
+                continue;
+              }
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int4 cb = e_col[8 * k + 4 * hh + g];
+                const int b4[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  // 2^-E as two normal powers of two: exact whenever the result
+                  // is a normal float (an intermediate that leaves the range
+                  // means the result does too)
+                  const int E = e_row - (b4[i] >> 23);
+                  const int e1 = max(-126, min(126, E));
+                  const int e2 = max(-126, min(126, E - e1));
+                  acc[32 * k + 16 * hh + 4 * g + i] += (__uint_as_float(t[4 * g + i]) *
+                                                        __int_as_float((127 - e1) << 23)) *
+                                                       __int_as_float((127 - e2) << 23);
+                }
+              }
+            }
           }
         }
         tc_fence_before();
@@ -441,12 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok || !active) continue;
       float* const crow = p.C + static_cast<long long>(row) * p.ldc;
-      // 3xFP16: sums of quad g (columns colw + 4g ..) back from the scaled
-      // domain
-      auto descale = [&](int g, float4 v) -> float4 {
-        if (!F16 || colw + 4 * g >= p.N) return v;
-        return unscale4(v, e_row, e_col[g]);
-      };
       // C[row][colw + 4g ..] := alpha * v + beta * C (columns past N and rows
       // past M are not written)
       float4* const tile = reinterpret_cast<float4*>(base_ptr + kEpiOff) + ew * kEpiTileF4;
@@ -538,8 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < kSumQuads / 4; ++jj) {
             const int g0 = kSumQuads * gb + 4 * jj;
-            const float4 v4[4] = {descale(g0, sum[4 * jj]), descale(g0 + 1, sum[4 * jj + 1]),
-                                  descale(g0 + 2, sum[4 * jj + 2]), descale(g0 + 3, sum[4 * jj + 3])};
+            const float4 v4[4] = {sum[4 * jj], sum[4 * jj + 1], sum[4 * jj + 2], sum[4 * jj + 3]};
             store_group(kSumQuads / 4 * gb + jj, v4);
           }
         }
@@ -551,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q2 = 0; q2 < 4; ++q2) {
           const int g = 4 * j + q2;
-          v4[q2] = descale(g, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
+          v4[q2] = make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
         }
         store_group(j, v4);
       }

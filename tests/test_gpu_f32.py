@@ -58,7 +58,7 @@ def test_leading_dimensions(M, N, K, lda, ldb, ldc):
     assert taken == ("f32.ffma.vec" if vec else "f32.ffma.scalar")
     check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
     assert padding_untouched(got, C0, N)
-    for path, prefix in ((0, "f32.3xtf32.pair"), (16, "f32.3xf16.pair")):
+    for path, prefix in ((0, "f32.3xtf32.pair"), (16, "f32.3xf16.pair")):   # tiny: 3xTF32
         got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc, path=path)
         assert taken.startswith(prefix), taken
         check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc)
@@ -267,15 +267,15 @@ def test_split_short_k_keeps_whole_units(kind, prefix, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,expect", [
-    (16, 8192, 1024, "f32.3xtf32"), (1, 4096, 512, "f32.3xtf32"), (200, 200, 200, "f32.3xtf32"),
+    (16, 8192, 1024, "f32.3xf16"), (1, 4096, 512, "f32.3xtf32"), (200, 200, 200, "f32.3xtf32"),
     (16, 16, 4096, "f32.3xtf32"), (1024, 1024, 16, "f32.ffma"), (300, 260, 1, "f32.ffma"),
-    (2560, 2048, 64, "f32.3xf16"), (2048, 2048, 2048, "f32.3xtf32"),
+    (2560, 2048, 64, "f32.3xf16"), (2048, 2048, 2048, "f32.3xf16"), (256, 256, 256, "f32.3xtf32"),
+    (256, 256, 257, "f32.3xf16"),
 ])
 def test_fp32_path_choice_small_and_skinny(M, N, K, expect):
     """K >= 64 takes the tensor cores whatever M and N (skinny and tiny shapes
-    included): 3xFP16 once the 256 x 256 tiles fill every CTA pair (80 tiles
-    here), 3xTF32 with fewer; a shorter K takes the FFMA kernel.  Parity
-    either way."""
+    included): 3xFP16 when M*N*K exceeds 256^3, 3xTF32 up to that; a shorter
+    K takes the FFMA kernel.  Parity either way."""
     A, B, C0 = operands(3030 + M + K, M, N, K, K, N, N, np.float32)
     got, taken = run("f32", A, B, C0, 1.25, -0.5, M, N, K, K, N, N)
     assert taken.startswith(expect), taken
