@@ -119,13 +119,14 @@ int gemm_f32_to_f16(const float* src, uint16_t* dst, long long n, cudaStream_t s
 /* Single-precision GEMM (SGEMM, "advanced SGEMM" page): fp32 operands and
  * result, within the fp32 bound 1e-6 * K * max|A| * max|B| per element.
  * Shapes with K >= 64 run on the tensor cores as three products of split
- * operands with fp32 accumulation: each row of A and each column of B is
- * scaled by a power of two that brings its largest magnitude into
- * [2^14, 2^15) and split into two halves, x * 2^e = h1 + h2 (11 + 11
- * significand bits), so A*B ~= A1*B1 + A1*B2 + A2*B1 (the A2*B2 term, about
- * 2^-22 of |A||B|, is dropped) and the epilogue undoes the scaling exactly
- * (3xFP16; gemm_force_path(8) takes tf32 parts instead, 3xTF32, at half the
- * rate).  A pre-pass writes the parts to library-owned scratch (few output
+ * operands with fp32 accumulation: within each 256-deep K chunk, each row of
+ * A and each column of B is scaled by a power of two that brings its largest
+ * magnitude into [2^14, 2^15) and split into two halves, x * 2^e = h1 + h2
+ * (11 + 11 significand bits), so A*B ~= A1*B1 + A1*B2 + A2*B1 (the A2*B2 term,
+ * about 2^-22 of |A||B|, is dropped); each chunk's products are scaled back
+ * exactly as they are added up (3xFP16, for M*N*K above 256^3; tiny products
+ * take tf32 parts instead, 3xTF32, at half the rate, as does
+ * gemm_force_path(8)).  A pre-pass writes the parts to library-owned scratch (few output
  * tiles with a long K: every tile cut into K slices whose fp32 partial sums
  * are added in slice order, so results are reproducible run to run); a
  * shorter K uses an FFMA kernel (exact fp32 products).  An Inf or NaN operand
