@@ -654,6 +654,10 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
     slots = pair_slots;
   }
   long long workers = std::min<long long>(units_tiles, slots);
+  // an operand that only one row (column) of single-CTA tiles reads -- B of a
+  // skinny shape, A of a tall one -- is streamed once: loaded evict-first
+  a.stream_a = !pair && a.tiles_n == 1;
+  a.stream_b = !pair && a.tiles_m == 1;
 
   a.dp_tiles = static_cast<int>(units_tiles);
   a.tail_splits = 1;

@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0;
         bool ok = true;
+        const uint64_t evict_first = l2_evict_first_policy();
         UnitCursor cur = first_unit(p, worker);
         Unit t;
         while (ok && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t)) {
@@ -586,12 +587,20 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
                                    t.n0 + static_cast<int>(rank) * bcols + 64 * c, kb * BK);
             } else {
               mbar_arrive_expect_tx(full_bar(stage), bytes);
-              tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
+              if (p.stream_a)
+                tma_load_2d_hint(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0, evict_first);
+              else
+                tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
-                if (64 * c < bcols)
-                  tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
-                              t.n0 + 64 * c, kb * BK);
+                if (64 * c < bcols) {
+                  if (p.stream_b)
+                    tma_load_2d_hint(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
+                                     t.n0 + 64 * c, kb * BK, evict_first);
+                  else
+                    tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
+                                t.n0 + 64 * c, kb * BK);
+                }
             }
             ++issued;
             if (++stage == S) {

@@ -88,6 +88,10 @@ struct TcArgs {
   // partial sums) is its worker's first unit and a second slice (it finishes
   // the tile) its worker's last, long after the first was published.
   int tail_first;
+  // single-CTA kernels: A (B) is read by one column (row) of tiles only, i.e.
+  // streamed once -- loaded evict-first, so it does not push out of L2 lines
+  // that are still useful (or dirty lines that would be written back)
+  int stream_a, stream_b;
   unsigned long long wait_limit_ns;
   DeviceStatus* status;
   // host only: the launch directly follows this call's pre-pass kernel on the
