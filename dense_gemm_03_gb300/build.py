@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgemm.so")
 SOURCES = ["api.cu", "gemm_f16_tc.cu", "gemm_f16_pair_narrow.cu", "gemm_f16_f32out.cu",
-           "gemm_f16_skinny.cu", "sgemm_ffma.cu", "sgemm_3xtf32.cu", "aux_kernels.cu",
+           "gemm_f16_skinny.cu", "sgemm_ffma.cu", "sgemm_split.cu", "aux_kernels.cu",
            "splitk_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

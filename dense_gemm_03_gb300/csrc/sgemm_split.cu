@@ -1,4 +1,5 @@
-// sgemm_3xtf32.cu -- fp32 SGEMM on the tensor cores with three tf32 products.
+// sgemm_split.cu -- fp32 SGEMM on the tensor cores as three products of split
+// operands (3xTF32: tf32 parts; 3xFP16: scaled half parts).
 //
 // C := alpha*A*B + beta*C in fp32.  Each operand is split (by a pre-pass) into
 // a tf32 "big" part (low 13 mantissa bits cleared) and a tf32 "small" part
