@@ -983,22 +983,42 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       }
       bool halves = false;
       t.splits = 1;
-      if (splits > 1) {
-        t.splits = splits;
-        t.dp_tiles = tiles;
-        t.num_units = tiles * splits;
-        // per tile: 2 CTAs x 8 epilogue warps x splits x (32 rows x 128 fp32)
-        const size_t wneed = static_cast<size_t>(tiles) * splits * 2 * 8 * 32 * 128 * sizeof(float);
+      // partial sums of `sliced` tiles cut into `per` slices: per tile 2 CTAs x
+      // 8 epilogue warps x slices x (32 rows x 128 fp32)
+      auto slice_scratch = [&](long long sliced, int per) -> int {
+        const size_t wneed = static_cast<size_t>(sliced) * per * 2 * 8 * 32 * 128 * sizeof(float);
         std::lock_guard<std::mutex> lk(g_mu);
         StreamWs* w = nullptr;
-        if (int rc = stream_scratch(d, stream, wneed, static_cast<size_t>(tiles) * 16, &w))
+        if (int rc = stream_scratch(d, stream, wneed, static_cast<size_t>(sliced) * 16, &w))
           return rc;
         t.part_ws = static_cast<float4*>(w->ptr);
         t.counters = static_cast<unsigned long long*>(w->counters);
         t.epoch = ++w->epoch;
         if (t.epoch == 0) t.epoch = ++w->epoch;   // 0 marks never-used counters
+        return GEMM_OK;
+      };
+      const int rem = tiles % pairs;
+      const int chunks = (t.kb_total + kSplitChunkKb - 1) / kSplitChunkKb;
+      if (splits > 1) {
+        t.splits = splits;
+        t.dp_tiles = tiles;
+        t.num_units = tiles * splits;
+        if (int rc = slice_scratch(tiles, splits)) return rc;
+      } else if (force != 5 && force != 15 && tiles > pairs && rem > 0 && 2 * rem <= pairs &&
+                 chunks >= 6) {
+        // The tiles of the last, partial wave as two K slices each, publisher
+        // first (tail_first): the first slice (about 56% of the chunks, the
+        // first wave's loads being the slow ones) is a worker's first unit,
+        // the second a worker's last.  Half-width units instead took nearly a
+        // full tile's time for half the work (3xFP16, same box: 4096^3 302 ->
+        // 288 us, 5120^3 553 -> 536 us; first slices of 50% or 62% of the
+        // chunks were slower than 56%).
+        t.tail_first = 1;
+        t.kb_per_split = std::min(chunks - 1, (chunks + 2) / 2) * kSplitChunkKb;
+        t.dp_tiles = tiles - rem;
+        t.num_units = t.dp_tiles + 2 * rem;
+        if (int rc = slice_scratch(rem, 2)) return rc;
       } else {
-        const int rem = tiles % pairs;
         halves = force != 5 && rem > 0 && 2 * rem <= pairs;
         t.dp_tiles = halves ? tiles - rem : tiles;
         t.num_units = t.dp_tiles + 2 * (tiles - t.dp_tiles);
@@ -1011,10 +1031,12 @@ int sgemm_f32_device(const float* A, const float* B, float* C, int M, int N, int
       const int grid = 2 * std::min(t.num_units, pairs);
       if (x16)
         t_last_path = splits > 1 ? "f32.3xf16.pair.ksplit"
-                                 : (halves ? "f32.3xf16.pair.halves" : "f32.3xf16.pair");
+                      : t.tail_first ? "f32.3xf16.pair.ktail"
+                                     : (halves ? "f32.3xf16.pair.halves" : "f32.3xf16.pair");
       else
         t_last_path = splits > 1 ? "f32.3xtf32.pair.ksplit"
-                                 : (halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair");
+                      : t.tail_first ? "f32.3xtf32.pair.ktail"
+                                     : (halves ? "f32.3xtf32.pair.halves" : "f32.3xtf32.pair");
       const cudaError_t e = x16 ? launch_sgemm_3xf16(m1, m2, m3, m4, t, grid, stream)
                                 : launch_sgemm_3xtf32(m1, m2, m3, m4, m5, m6, t, grid, stream);
       return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

@@ -203,6 +203,9 @@ cudaError_t launch_f16x3_split(const float* A, long long lda, const float* B, lo
 // 3xTF32 SGEMM on CTA pairs: C = alpha*(Ab*Bb + Ab*Bs + As*Bb) + beta*C with
 // the split operands dense and K-contiguous: A parts M x roundup(K,4), B parts
 // transposed, N x roundup(K,4).
+// k-blocks (64 bytes of K per row) in one TMEM accumulation chunk of the
+// split-operand kernel: 128 floats (3xTF32) or 256 halves (3xFP16).
+constexpr int kSplitChunkKb = 8;
 struct Tf32Args {
   const float* Ab;
   const float* As;
@@ -233,6 +236,12 @@ struct Tf32Args {
   unsigned long long* counters;     // [tile][rank][warp]: (epoch << 32) | arrivals
   unsigned int epoch;
   bool pdl;                         // host only: as TcArgs::pdl (after the split pre-pass)
+  // Two-slice tail (splits == 1): the tail tiles -- T = (num_units -
+  // dp_tiles) / 2 of them, the first T in visiting order -- are cut into a
+  // first slice of kb_per_split k-blocks (whole accumulation chunks), a
+  // worker's first unit, and a second slice, a worker's last; the slice that
+  // arrives last adds both up, as with K slices.
+  int tail_first;
   // 3xFP16 only: the power-of-two exponents the parts were scaled by, per K
   // chunk of kF16x3ChunkK (the accumulation chunk): ea[row * kchunks + c],
   // eb[c * ldeb + col] (ldeb >= N + 4)

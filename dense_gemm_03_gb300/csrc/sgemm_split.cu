@@ -63,7 +63,7 @@ constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
 constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;
 constexpr int kCols = BN / 2;               // accumulator columns per epilogue thread
-constexpr int kChunkKb = 8;                 // k-blocks per TMEM accumulation chunk (K = 128 floats, 256 halves)
+constexpr int kChunkKb = kSplitChunkKb;     // k-blocks per TMEM accumulation chunk (K = 128 floats, 256 halves)
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kBarOff = kStages * kStageBytes;
@@ -131,12 +131,12 @@ constexpr int kSumQuads = 16;   // column quads the finisher sums at a time
 // finisher adds them in slice order, so the result does not depend on which
 // slice finishes.  The finisher also clears the counter, so the next launch
 // starts from zero whatever its epoch.
-__device__ __forceinline__ bool publish_slice(const Tf32Args& p, int u, int rank, int ew, int lane,
+__device__ __forceinline__ bool publish_slice(const Tf32Args& p, int tile, int slice, int nslices,
+                                              int rank, int ew, int lane,
                                               const float (&acc)[kCols], const float4*& part) {
-  const int tile = u / p.splits, slice = u - tile * p.splits;
   const long long slot = (static_cast<long long>(tile) * 2 + rank) * kEpiWarps + ew;
   unsigned long long* const cnt = p.counters + slot;
-  float4* const mine = p.part_ws + (slot * p.splits + slice) * kSliceF4 + lane;
+  float4* const mine = p.part_ws + (slot * nslices + slice) * kSliceF4 + lane;
 #pragma unroll
   for (int g = 0; g < kCols / 4; ++g)
     __stcg(mine + g * 32, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
@@ -159,11 +159,39 @@ __device__ __forceinline__ bool publish_slice(const Tf32Args& p, int u, int rank
     }
   }
   arrived = __shfl_sync(0xffffffffu, arrived, 0);
-  if (arrived != static_cast<uint32_t>(p.splits)) return false;
+  if (arrived != static_cast<uint32_t>(nslices)) return false;
   __threadfence();
   if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(cnt) = 0ull;
-  part = p.part_ws + slot * p.splits * kSliceF4 + lane;
+  part = p.part_ws + slot * nslices * kSliceF4 + lane;
   return true;
+}
+
+// Unit u's shared tile, if it is one K slice of a tile: the tile's index among
+// the sliced tiles, the slice and the slices per tile (nslices = 1: a whole
+// tile or half-width unit).  K slices of every tile (splits > 1): unit = tile
+// * splits + slice.  Two-slice tail (tail_first): units [0, T) are the first
+// slices of the tiles [0, T) (visiting order), [T, T + dp_tiles) whole tiles,
+// then the second slices -- a first slice is a worker's first unit, a second
+// slice its last, long after the first was published.
+__device__ __forceinline__ void slice_of(const Tf32Args& p, int u, int& tile, int& slice,
+                                         int& nslices) {
+  tile = u;
+  slice = 0;
+  nslices = 1;
+  if (p.splits > 1) {
+    tile = u / p.splits;
+    slice = u - tile * p.splits;
+    nslices = p.splits;
+  } else if (p.tail_first) {
+    const int T = (p.num_units - p.dp_tiles) >> 1;
+    if (u < T) {
+      nslices = 2;
+    } else if (u >= T + p.dp_tiles) {
+      tile = u - T - p.dp_tiles;
+      slice = 1;
+      nslices = 2;
+    }
+  }
 }
 
 
@@ -243,6 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile = u / p.splits;
       kb0 = (u - tile * p.splits) * p.kb_per_split;
       kb1 = min(kb0 + p.kb_per_split, p.kb_total);
+    } else if (p.tail_first) {
+      int slice, nslices;
+      slice_of(p, u, tile, slice, nslices);
+      if (nslices > 1) {
+        kb0 = slice ? p.kb_per_split : 0;
+        kb1 = slice ? p.kb_total : p.kb_per_split;
+      }
     } else if (u >= p.dp_tiles) {
       tile = p.dp_tiles + ((u - p.dp_tiles) >> 1);
       half = (u - p.dp_tiles) & 1;
@@ -561,18 +596,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      if (p.splits > 1) {
+      int stile, sslice, nslices;
+      slice_of(p, u, stile, sslice, nslices);
+      if (nslices > 1) {
         // K slices: publish; the last slice of the tile to arrive adds all
         // slices up in slice order, kSumQuads column quads at a time (as many
         // loads in flight per slice), and writes C from the sums
         const float4* part = nullptr;
-        if (!publish_slice(p, u, static_cast<int>(rank), ew, lane, acc, part)) continue;
+        if (!publish_slice(p, stile, sslice, nslices, static_cast<int>(rank), ew, lane, acc, part))
+          continue;
 #pragma unroll
         for (int gb = 0; gb < kCols / 4 / kSumQuads; ++gb) {
           float4 sum[kSumQuads];
 #pragma unroll
           for (int i = 0; i < kSumQuads; ++i) sum[i] = __ldcg(part + (kSumQuads * gb + i) * 32);
-          for (int s2 = 1; s2 < p.splits; ++s2) {
+          for (int s2 = 1; s2 < nslices; ++s2) {
             float4 v[kSumQuads];
 #pragma unroll
             for (int i = 0; i < kSumQuads; ++i)

@@ -212,8 +212,9 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * (whole tiles; the automatic choice keeps 256); 14 = the tiles of the last,
  * partial wave shared out as stream-K pieces, each worker taking the piece
  * that starts a tile first and the piece that ends a tile last.  The
- * automatic choice cuts the tiles of a last, partial wave that fills at most
- * half the workers into two K slices each, the first slice one worker's
+ * automatic choice (fp16 and fp32 tensor-core kernels alike; for fp32 when K
+ * holds at least 6 accumulation chunks) cuts the tiles of a last, partial
+ * wave that fills at most half the workers into two K slices each, the first slice one worker's
  * first unit and the second another worker's last (it adds the first one's
  * partial sums, published long before); else it runs them as half-width
  * units; 15 = half-width units for them; 16 = (fp32) the 3xFP16 tensor-core

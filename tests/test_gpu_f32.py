@@ -197,6 +197,33 @@ def test_split_half_width_tail(kind, prefix, M, N, K):
         assert np.abs(got.astype(np.float64) - whole).max() <= 2 * bound
 
 
+@pytest.mark.parametrize("kind,prefix", KINDS)
+def test_split_two_slice_tail(kind, prefix):
+    """The tiles of the last, partial wave cut into two K slices each, the
+    first a worker's first unit and the second a worker's last (90 pair
+    tiles on at most 76 pairs, 2048-deep K): exact on integers, within the fp32
+    bound of the oracle, bit-identical run to run, and within twice the bound
+    of the half-width form of the same wave (path 15, 3xFP16)."""
+    M, N, K = 2560, 2304, 2048
+    rng = np.random.default_rng(2304)
+    A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    got, taken = run("f32", A, B, C0, 2.0, -1.0, M, N, K, K, N, N, path=kind)
+    assert taken == prefix + ".ktail", taken
+    rows = oracle.sample_rows(M, block=64)
+    assert np.array_equal(got[rows].astype(np.float64), oracle.gemm(A, B, C0, 2.0, -1.0, rows=rows))
+    A, B, C0 = operands(2305, M, N, K, K, N, N, np.float32)
+    got, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind)
+    again, _ = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=kind)
+    assert np.array_equal(got, again)
+    check("f32", got, A, B, C0, 1.5, 0.5, M, N, K, K, N, N, rows=rows)
+    halves, t2 = run("f32", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=15)   # 3xFP16 halves
+    assert t2.endswith(".halves"), t2
+    bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
+    assert np.abs(got.astype(np.float64) - halves).max() <= 2 * bound
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 65536), (300, 260, 1), (257, 1000, 64), (3000, 1, 4)])
 def test_fp32_extreme_dimensions(M, N, K):
     A, B, C0 = operands(4242 + M + K, M, N, K, K, N, N, np.float32)
