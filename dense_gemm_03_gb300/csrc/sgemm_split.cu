@@ -12,32 +12,35 @@
 // nearest: summed over a long K in tensor memory, the result drifts toward
 // zero by a bias that grows like K*|C| (measured: at K = 16384 it exceeds the
 // fp32 error bound).  So the MMA accumulates only chunks of 128 along K (256
-// for the 3xFP16 form below) into tensor memory (alternating between two buffers), and the epilogue warps add
-// each chunk into fp32 registers with ordinary round-to-nearest adds; the
-// result is then as accurate as the FFMA kernel's.
+// for the 3xFP16 form below) into tensor memory, alternating between two
+// buffers, and the epilogue warps add each chunk into fp32 registers with
+// ordinary round-to-nearest adds; the result is then as accurate as the FFMA
+// kernel's.
 //
 // Kernel: CTA pairs (clusters of 2) share tcgen05.mma.cta_group::2.kind::tf32
 // with M = 256 (128 rows of A in each CTA) and N = 256 (each CTA stages 128 of
 // the columns of B); per 16-deep k-block each CTA stages Ab, As (128 x 16) and
-// Bb, Bs (128 columns x 16) by TMA into a 6-stage ring (32 KB per stage), and
-// the leader issues 3 MMAs per 8-deep K step.  Small stages keep five of the
-// six in flight while one is consumed: with 64 KB stages (three of them) a
-// load took ~2.3 us from issue to arrival and the pipeline ran at the rate of
-// the loads, not of the MMAs.  Warp roles and barriers follow
-// the fp16 tensor-core kernel; the 8 epilogue warps keep fp32 row sums in
-// registers and write C through a small shared-memory tile each, so that
-// stores cover whole 64-byte row pieces.  Both operands are K-major (the pre-pass stores the B
-// parts transposed): 64-byte swizzle, 16 floats per row, SBO 512 B.
+// Bb, Bs (128 columns x 16) by TMA into a 6-stage ring (32 KB per stage; three
+// stages of 64 KB ran at the same speed), and the leader issues 3 MMAs per
+// 8-deep K step.  Warp roles and barriers follow the fp16 tensor-core kernel;
+// the 8 epilogue warps keep fp32 row sums in registers and write C through a
+// small shared-memory tile each, so that stores cover whole 64-byte row
+// pieces.  Both operands are K-major (the pre-pass stores the B parts
+// transposed): 64-byte swizzle, 16 floats per row, SBO 512 B.
 //
-// Units: whole 256 x 256 tiles; the tiles of a last, partial wave as two
+// Units: whole 256 x 256 tiles; the tiles of a last, partial wave as two K
+// slices each, publisher first (the first slice a worker's first unit, the
+// second a worker's last; see slice_of), or, with a short K, as two
 // half-width units each; or, when few tiles meet a long K, equal K slices of
-// every tile (whole accumulation chunks), whose fp32 partial sums the last
-// slice of a tile to arrive adds up in slice order before writing C.
+// every tile (whole accumulation chunks).  The fp32 partial sums of a tile's
+// slices are added up in slice order by the slice that arrives last, before
+// it writes C.
 //
 // 3xFP16 (the same kernel, F16 = true): the parts are halves instead of tf32
 // values -- x * 2^e = h1 + h2 with e a power-of-two exponent per row of A and
-// per column of B that keeps the parts inside the half range (the same 11 + 11
-// significand bits as the tf32 split), written by the split pre-pass -- and
+// per column of B within each 256-deep K chunk that keeps the parts inside the
+// half range (the same 11 + 11 significand bits as the tf32 split), written
+// by the split pre-pass -- and
 // the three products run as kind::f16 MMAs at twice the tf32 rate.  A k-block
 // is then 32 deep (one 64-byte row of halves), B is staged N-major as 64-
 // column blocks of 32 k-rows (128-byte swizzle, no transpose), chunks are 8
@@ -63,7 +66,7 @@ constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
 constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;
 constexpr int kCols = BN / 2;               // accumulator columns per epilogue thread
-constexpr int kChunkKb = kSplitChunkKb;     // k-blocks per TMEM accumulation chunk (K = 128 floats, 256 halves)
+constexpr int kChunkKb = kSplitChunkKb;     // k-blocks per TMEM chunk: 128 floats / 256 halves
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kBarOff = kStages * kStageBytes;
