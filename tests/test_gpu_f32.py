@@ -224,6 +224,24 @@ def test_split_two_slice_tail(kind, prefix):
     assert np.abs(got.astype(np.float64) - halves).max() <= 2 * bound
 
 
+@pytest.mark.parametrize("kind,prefix", KINDS)
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
+    (2560, 2303, 2100, 2103, 2305, 2307),   # ragged last K chunk, odd N, unaligned rows
+    (2304, 2560, 1800, 1800, 2560, 2561),
+])
+def test_split_two_slice_tail_ragged(kind, prefix, M, N, K, lda, ldb, ldc):
+    """The two-slice tail with a K that ends inside an accumulation chunk, a
+    column count that is not a multiple of 4 and leading dimensions off the
+    16-byte grid (the pre-pass reads them with element loads, C is written row
+    by row): parity with the oracle on sampled rows and C's padding intact."""
+    A, B, C0 = operands(7000 + K, M, N, K, lda, ldb, ldc, np.float32)
+    got, taken = run("f32", A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc, path=kind)
+    assert taken == prefix + ".ktail", taken
+    check("f32", got, A, B, C0, 0.75, -0.25, M, N, K, lda, ldb, ldc,
+          rows=oracle.sample_rows(M, block=64))
+    assert padding_untouched(got, C0, N)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 65536), (300, 260, 1), (257, 1000, 64), (3000, 1, 4)])
 def test_fp32_extreme_dimensions(M, N, K):
     A, B, C0 = operands(4242 + M + K, M, N, K, K, N, N, np.float32)
