@@ -859,7 +859,8 @@ def run_sweep(args):
 # ---------------------------------------------------------------- fp16 tile-heuristic sweep
 
 F16_VARIANTS = [(0, "auto"), (6, "no_pairs"), (5, "whole_tiles"), (9, "k_slices_tail"),
-                (10, "stream_k")]
+                (10, "stream_k"), (15, "halves_tail"), (14, "stream_k_tail"),
+                (12, "width_224"), (13, "width_192")]
 
 
 def run_sweep_f16(args):
