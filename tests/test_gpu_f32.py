@@ -222,6 +222,10 @@ def test_split_two_slice_tail(kind, prefix):
     assert t2.endswith(".halves"), t2
     bound = 1e-6 * K * np.abs(A).max() * np.abs(B).max()
     assert np.abs(got.astype(np.float64) - halves).max() <= 2 * bound
+    # beta = 0: C (NaN-filled here) is never read, by whole tiles or by the slices
+    Cn = np.full_like(C0, np.nan)
+    got0, _ = run("f32", A, B, Cn, 1.5, 0.0, M, N, K, K, N, N, path=kind)
+    check("f32", got0, A, B, Cn, 1.5, 0.0, M, N, K, K, N, N, rows=rows)
 
 
 @pytest.mark.parametrize("kind,prefix", KINDS)
