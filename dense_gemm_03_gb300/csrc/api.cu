@@ -18,7 +18,8 @@
 //      it back; predicated accesses when that is forced or too large; a float
 //      C is written from registers
 //   6. few tiles for many SMs with a long K: stream-K over all tiles when it
-//      is expected to beat half-width units (few_tiles_prefer_stream_k)
+//      is expected to beat half-width units, or one wave of whole tiles for
+//      64-wide tiles (few_tiles_prefer_stream_k)
 //   7. CTA pairs (256 x 256 tiles) for 256-wide TMA shapes with at least two
 //      tile rows; 32 or 64 rows of A staged per k-block when M <= 64
 //   8. the tiles of the last, partial wave are shared out as stream-K pieces
@@ -352,13 +353,26 @@ int tail_first_slice(long long tiles, long long slots, int kb) {
 // (32 tiles of 16 k-blocks) half-width units 16 us, stream-K 24 us;
 // 1000x1001x4096 (32 tiles of 64) 38 us and 61 us; 16x8192x8192 (64 tiles of
 // 128, 16 rows) stream-K 42 us, equal K slices 51 us.
+// 64-wide TMA tiles have no half-width units; there stream-K is weighed
+// against one wave of whole-K tiles (kb k-blocks per CTA), and its ranges
+// can go no faster than HBM streams A: a CTA takes ~0.25 us per k-block
+// (whatever the tile's height or the number of CTAs), the time HBM takes for
+// the k-blocks of about 96 128-row tiles.  Measured over M = 512..9728,
+// N = 32 and 64, K = 512..16384 (median of 20 after the page's flush):
+// whole tiles win for K <= 2048 (8192x64x1024 14.3 us against 18.4 us),
+// stream-K for K >= 8192 (4096x64x8192 26.9 against 43.0 us); in between
+// the estimate picks the faster one to within ~1 us.
 bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool halves_ok,
-                               int rows, int bn) {
+                               bool whole_ok, int rows, int bn) {
   const SkPlan sk = plan_stream_k(tiles, slots, kb, true);
   if (sk.sk_tiles == 0) return false;
-  if (!halves_ok) return true;
   const long long range = (sk.sk_tiles * kb + sk.workers - 1) / sk.workers;
   const long long per_piece = std::max(1ll, 8ll * std::min(rows, kBM) * bn / (kBM * 128));
+  if (!halves_ok) {
+    if (!whole_ok) return true;
+    const long long floor_kb = (sk.sk_tiles * kb * std::min(rows, kBM) + 96 * kBM - 1) / (96 * kBM);
+    return std::max(range, floor_kb) + kSkFixKb + per_piece * (sk.max_pieces - 1) < kb;
+  }
   const long long sk_cost = range + kSkFixKb + per_piece * (sk.max_pieces - 1);
   const long long waves = (2 * tiles + slots - 1) / slots;
   const long long halves_cost = (3 * kb * waves + 3) / 4;
@@ -608,10 +622,17 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   // Few tiles for many SMs: stream-K over all tiles when it beats half-width
   // whole-K units (few_sk; then one CTA per worker, no pairs).
   const bool few = tiles * 2 <= d->sm_count && a.kb_total >= 8;
-  const bool few_sk =
+  // Tall shapes (one column of 64-wide tiles): 64-row tiles (M = 64 MMAs)
+  // double the tiles, so that whole-K units fill one wave without stream-K
+  // partial sums.
+  const long long tiles64 = 1ll * ((M + 63) / 64) * a.tiles_n;
+  const bool m64 = force == 17 && load == kLoadTma && epi == kEpiTma && bn == 64 &&
+                   tiles64 <= d->sm_count;
+  if (m64) a.tiles_m = (M + 63) / 64;
+  const bool few_sk = !m64 &&
       (few && force == 0 &&
-       few_tiles_prefer_stream_k(tiles, d->sm_count, a.kb_total, load == kLoadTma && bn >= 128, M,
-                                 bn)) ||
+       few_tiles_prefer_stream_k(tiles, d->sm_count, a.kb_total, load == kLoadTma && bn >= 128,
+                                 load == kLoadTma && bn == 64, M, bn)) ||
       force == 11;
   if (force == 3) {
     // as many K slices as fit in ONE wave of CTAs (a second, partial wave would
@@ -646,7 +667,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   // 16-byte aligned and N is a multiple of 4 (a TMA store writes whole 16-byte
   // pieces of a row)
   if (epi == kEpiF32 && pair && a.vec_c && N % 4 == 0) epi = kEpiF32Tma;
-  long long units_tiles = tiles;   // tiles in units of the worker (CTA or pair)
+  long long units_tiles = m64 ? tiles64 : tiles;   // tiles in units of the worker (CTA or pair)
   long long slots = d->sm_count;   // workers that can run at once
   if (pair) {
     a.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
@@ -713,7 +734,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
       if (int rc = take_scratch(sk.sk_tiles * (pair ? 2 : 1), sk.max_pieces)) return rc;
       cut = ".sk";
     }
-  } else if (force != 5 && force != 12 && force != 13 && !few_sk) {
+  } else if (!m64 && force != 5 && force != 12 && force != 13 && !few_sk) {
     // The tiles of the last, partial wave: two K slices each, the first slice
     // a worker's first unit and the second another worker's last
     // (tail_first_slice); else two half-width units each (whole K, no partial
@@ -777,15 +798,18 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
 
   // At most 64 rows on 128-wide single-CTA tiles: stage only the A rows that
   // exist (32 or 64), which leaves room for more stages of B.
-  const int am = (load == kLoadTma && !pair && bn == 128 && M <= 64) ? (M <= 32 ? 32 : 64) : kBM;
+  const int am = m64 ? 64
+                     : ((load == kLoadTma && !pair && bn == 128 && M <= 64) ? (M <= 32 ? 32 : 64)
+                                                                           : kBM);
   CUtensorMap tmA{}, tmB{}, tmC{};
   if (load == kLoadTma) {
     if (int rc = make_map_f16(&tmA, A, M, K, lda, 64, am)) return rc;
     if (int rc = make_map_f16(&tmB, B, K, N, ldb, 64, 64)) return rc;
   }
   if (epi == kEpiTma) {
-    // epilogue staging tile: 32 rows x 32 halves, 64-byte swizzle
-    if (int rc = make_map_f16(&tmC, a.C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
+    // epilogue staging tile: 32 rows (16 on 64-row tiles) x 32 halves, 64-byte swizzle
+    if (int rc = make_map_f16(&tmC, a.C, M, N, ldc, 32, m64 ? 16 : 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return rc;
   } else if (epi == kEpiF32Tma) {
     // the same 64-byte rows: 32 rows x 16 floats
     if (int rc = make_map_f32(&tmC, a.Cf, M, N, ldc, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return rc;
@@ -816,7 +840,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   }
   const int grid = static_cast<int>(nw);
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  const char* rows = am == 32 ? ".a32" : (am == 64 ? ".a64" : "");
+  const char* rows = m64 ? ".m64" : (am == 32 ? ".a32" : (am == 64 ? ".a64" : ""));
   if (c_f32)
     snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.bn%d.%s.epi_f32%s%s%s", bn,
              load == kLoadTma ? "tma" : "manual", rows, cut, how);
@@ -824,9 +848,10 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
     snprintf(t_path_buf, sizeof(t_path_buf), "%s%s%s%s", kPathNames[bi][load][epi], rows, cut,
              how);
   t_last_path = t_path_buf;
-  const cudaError_t e = am < kBM
-                            ? launch_gemm_f16_tc_skinny(am, epi, tmA, tmB, tmC, a, grid, stream)
-                            : launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream);
+  const cudaError_t e =
+      m64 ? launch_gemm_f16_tc_m64(tmA, tmB, tmC, a, grid, stream)
+          : (am < kBM ? launch_gemm_f16_tc_skinny(am, epi, tmA, tmB, tmC, a, grid, stream)
+                      : launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream));
   if (e != cudaSuccess) return GEMM_ERR_CUDA;
   return copy_back();
 }
@@ -1236,7 +1261,7 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 }
 
 int gemm_force_path(int path) {
-  if (path < 0 || path > 16) return GEMM_ERR_ARG;
+  if (path < 0 || path > 17) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
 }
 

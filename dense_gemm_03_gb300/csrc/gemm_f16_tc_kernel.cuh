@@ -16,10 +16,11 @@
 //   producer warp(s)  TMA tile loads (or, for unaligned operands, 4 warps of
 //                     predicated element loads written in the same layout)
 //   MMA warp          one thread issues tcgen05.mma (M=128, or M=256 on a CTA
-//                     pair; N=BN or BN/2; K=16) into a double-buffered TMEM
-//                     accumulator (2 x BN fp32 columns)
-//   8 epilogue warps  warp (q, h) owns TMEM lanes 32q..32q+31 (= tile rows)
-//                     and the h-th half of the unit's columns; in 32-column
+//                     pair, or M=64 on 64-row tiles; N=BN or BN/2; K=16) into
+//                     a double-buffered TMEM accumulator (2 x BN fp32 columns)
+//   8 epilogue warps  warp (q, h) owns TMEM lanes 32q..32q+31 (= tile rows;
+//                     on 64-row tiles the first 16 of them hold rows
+//                     16q..16q+15) and the h-th half of the unit's columns; in 32-column
 //                     sub-chunks it loads the accumulator (the next sub-chunk's
 //                     load in flight), applies alpha/beta in fp32, rounds to
 //                     fp16 and stores by TMA through 2 KB staging tiles (on
@@ -464,7 +465,7 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* 
   }
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128>
 __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -477,12 +478,15 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   static_assert(AM == 128 || LOAD == kLoadTma, "skinny stages take TMA loads");
   constexpr int S = Cfg::kStages;
   static_assert(!PAIR || (LOAD == kLoadTma && EPI != kEpiPartial), "pair configuration");
+  // MM = 64: 64-row tiles (tcgen05.mma with M = 64), whole-K units only, TMA
+  // loads of 64 rows of A and the TMA epilogue
+  static_assert(MM == 128 || (MM == 64 && AM == 64 && !PAIR && EPI == kEpiTma), "64-row tiles");
   // Units are handed out per CTA, or per CTA pair (cluster of 2).
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
   const int worker = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int nworkers = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
-  const int bm_tile = PAIR ? 2 * BM : BM;
+  const int bm_tile = PAIR ? 2 * BM : MM;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -672,8 +676,8 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   } else if (warp == R::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc_full = make_idesc(0u, PAIR ? 2 * BM : BM, BN, 0u, 1u);
-      constexpr uint32_t idesc_half = make_idesc(0u, PAIR ? 2 * BM : BM, BN / 2, 0u, 1u);
+      constexpr uint32_t idesc_full = make_idesc(0u, PAIR ? 2 * BM : MM, BN, 0u, 1u);
+      constexpr uint32_t idesc_half = make_idesc(0u, PAIR ? 2 * BM : MM, BN / 2, 0u, 1u);
       int stage = 0;
       uint32_t phase = 0, local = 0;
       bool ok = true;
@@ -751,6 +755,11 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     constexpr int kSubs = (BN / kSubCols + kParts - 1) / kParts;
     const int ew = warp - R::kEpiWarp0;   // 0 .. kEpiWarps-1
     const int q = warp & 3;               // TMEM lane quadrant -> rows 32q .. 32q+31
+    // Tile rows per lane quadrant: 32 (row 32q + l in TMEM lane 32q + l), or
+    // 16 on 64-row tiles, whose M = 64 accumulator holds row 16q + l in lane
+    // 32q + l for l < 16 only (the other lanes are not written; their threads
+    // take a row past M, so that they neither read nor write C).
+    constexpr int kQRows = MM / 4;
     const int h = ew >> 2;                // column part of the tile
     // first column (within the unit) and number of sub-chunks of this warp
     auto warp_cols = [&](const Unit& u, int& first, int& nchunks) {
@@ -800,7 +809,7 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       int first2, nch2;
       warp_cols(u2, first2, nch2);
       const int wc = nch2 * kSubCols;
-      const int r0 = u2.m0 + 32 * q, cw = u2.n0 + first2;
+      const int r0 = u2.m0 + kQRows * q, cw = u2.n0 + first2;
       if (!has_c || r0 >= p.M || cw >= p.N) return;
 #pragma unroll
       for (int j = 0; j < NB; ++j)
@@ -814,14 +823,14 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
       // kCs looks one unit ahead (its C tile is loaded during the next main loop)
       const bool have_next = kCs && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, tn);
       const uint32_t buf = local & 1u, use = local >> 1;
-      const int row0 = t.m0 + 32 * q;
+      const int row0 = t.m0 + kQRows * q;
       // tail bookkeeping is per CTA: the rows of one CTA of a pair form their own part
       const int tail_part = PAIR ? 2 * t.tail_idx + static_cast<int>(rank) : t.tail_idx;
       int wcol0, nsub;                              // this warp's columns of the unit
       warp_cols(t, wcol0, nsub);
       const int wcols = nsub * kSubCols;
       const int colw = t.n0 + wcol0;                // first column of this warp
-      const int row = row0 + lane;                  // this thread's row
+      const int row = lane < kQRows ? row0 + lane : p.M;   // this thread's row
       bool finish = nsub > 0 && row0 < p.M && colw < p.N;   // this warp has outputs to produce
       if (EPI != kEpiPartial && has_c && finish && row < p.M) {
         // While this unit's main loop runs, bring this row's part of C into
@@ -1155,13 +1164,13 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   // the MMA warp only after all epilogue warps have signalled tmem_free.
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128>
 cudaError_t configure(int dev) {
   using L = Smem<BN, EPI, PAIR, AM>;
   static bool configured[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM, MM>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1170,14 +1179,14 @@ cudaError_t configure(int dev) {
   return cudaSuccess;
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                        const TcArgs& args, int grid, cudaStream_t stream) {
   using L = Smem<BN, EPI, PAIR, AM>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if ((e = configure<BN, LOAD, EPI, PAIR, AM>(dev)) != cudaSuccess) return e;
+  if ((e = configure<BN, LOAD, EPI, PAIR, AM, MM>(dev)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(Roles<LOAD>::kThreads, 1, 1);
@@ -1199,7 +1208,8 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   }
   cfg.attrs = nattr ? attr : nullptr;
   cfg.numAttrs = nattr;
-  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM>, tmA, tmB, tmC, args);
+  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM, MM>, tmA, tmB, tmC,
+                         args);
   if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());
 }

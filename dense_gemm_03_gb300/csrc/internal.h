@@ -121,6 +121,11 @@ int tc_pair_max_clusters_f32(int epi_mode);
 cudaError_t launch_gemm_f16_tc_skinny(int am, int epi_mode, const CUtensorMap& tmA,
                                       const CUtensorMap& tmB, const CUtensorMap& tmC,
                                       const TcArgs& args, int grid, cudaStream_t stream);
+// 64-wide tiles of 64 rows (tcgen05.mma with M = 64), TMA loads and epilogue,
+// whole-K units only (gemm_f16_skinny.cu); C's map has 32 x 16-row boxes.
+cudaError_t launch_gemm_f16_tc_m64(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                   const CUtensorMap& tmC, const TcArgs& args, int grid,
+                                   cudaStream_t stream);
 
 // One thread waits on an mbarrier that nothing arrives on, so the bounded wait
 // runs out after limit_ns and records GEMM_ERR_TIMEOUT in *status.

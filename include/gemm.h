@@ -218,7 +218,11 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  * first unit and the second another worker's last (it adds the first one's
  * partial sums, published long before); else it runs them as half-width
  * units; 15 = half-width units for them; 16 = (fp32) the 3xFP16 tensor-core
- * kernel whatever the shape (8 = 3xTF32).
+ * kernel whatever the shape (8 = 3xTF32); 17 = 64-row tiles (tcgen05.mma with
+ * M = 64) for a half C at most 64 columns wide with TMA loads and epilogue,
+ * whole-K tiles in one wave (at most one per SM; the automatic choice keeps
+ * 128-row tiles, which run as fast: a CTA's time goes with its k-blocks, not
+ * with its rows).
  * A forced path that cannot serve a call (e.g. TMA
  * loads on unaligned operands) falls back to the automatic choice.  Process
  * wide; returns the previous value, or GEMM_ERR_ARG for an unknown value.

@@ -61,7 +61,7 @@ def test_strerror_and_switches(L):
     assert g.force_path(3) == 0
     assert g.force_path(0) == 3
     with pytest.raises(g.GemmError):
-        g.force_path(17)
+        g.force_path(18)
     assert g.force_splits(4) == 0 and g.force_splits(0) == 4
     prev = g.set_wait_limit_ns(12345)
     assert g.set_wait_limit_ns(prev) == 12345

@@ -11,7 +11,7 @@ from helpers import check, operands, padding_untouched, run, to_dev, torch
 pytestmark = pytest.mark.gpu
 
 AUTO, MANUAL, SPLITK = 0, 2, 3
-NO_TAIL, NO_PAIR, TAIL2, SK, SK_ALL, SKTAIL, HALVES = 5, 6, 9, 10, 11, 14, 15
+NO_TAIL, NO_PAIR, TAIL2, SK, SK_ALL, SKTAIL, HALVES, M64 = 5, 6, 9, 10, 11, 14, 15, 17
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -265,7 +265,9 @@ def test_tail_deterministic(path, mark):
     (3300, 2001, 700, AUTO, ".halves.realigned.c"),               # every operand realigned, halved
     (3300, 2001, 700, MANUAL, ".manual.epi_manual"),              # predicated loads and epilogue
     (16, 8192, 8192, AUTO, ".bn128.tma.epi_tma.a32.sk"),   # skinny: every tile shared
-    (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma.sk"),      # tall: every tile shared
+    (4096, 64, 8192, AUTO, ".bn64.tma.epi_tma.sk"),      # tall, long K: every tile shared
+    (4096, 64, 2048, AUTO, ".bn64.tma.epi_tma"),         # tall, shorter K: one wave of whole tiles
+    (4096, 64, 2048, M64, ".bn64.tma.epi_tma.m64"),      # the same on 64-row tiles
     (64, 128, 4096, SK_ALL, ".sk"),                      # one tile cut into 16 pieces
     (100, 300, 1000, SK_ALL, ".sk"),                     # ragged, small
     (64, 128, 4096, AUTO, ".halves"),                    # the same, as two half-width units
@@ -492,3 +494,57 @@ def test_unaligned_c_copied_back(offset_elems, M, N, ldc, beta):
     out_bits = out.view(np.uint16)
     assert np.array_equal(out_bits[:pad + offset_elems], ref_bits[:pad + offset_elems])
     assert np.array_equal(out_bits[pad + offset_elems + C0.size:], ref_bits[pad + offset_elems + C0.size:])
+
+
+# ---------------------------------------------------------------- 64-row tiles (tcgen05.mma with M = 64)
+
+@pytest.mark.parametrize("M,N,K,ldc", [
+    (8192, 64, 4096, 64),     # the tall shape: 128 tiles, one wave of whole-K units
+    (1000, 64, 700, 64),      # a 40-row last tile and a ragged k-block
+    (64, 64, 64, 64),         # one tile, one k-block
+    (4000, 40, 1000, 48),     # N < 64 with a padded C
+    (129, 56, 4100, 56),      # three tiles, the last with one row; a long ragged K
+])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(0.75, -0.25, "uniform"), (1.0, 0.0, "nan")])
+def test_m64_tiles_parity(M, N, K, ldc, alpha, beta, c_fill):
+    """64-row tiles: the M = 64 accumulator holds row 16q + l of the tile in
+    TMEM lane 32q + l (l < 16) and each epilogue warp stores 16 rows; rows past
+    M and the padding of C stay untouched."""
+    A, B, C0 = operands(640 + M + N + K, M, N, K, K, N, ldc, np.float16, c_fill=c_fill)
+    got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, ldc, path=M64)
+    assert ".m64" in taken, taken
+    big = M * N * K > 1e9
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, ldc,
+          rows=oracle.sample_rows(M, block=16) if big else None)   # every 16-row quadrant
+    assert padding_untouched(got, C0, N)
+
+
+def test_m64_tiles_integers_exact():
+    """Small integers: every partial sum is exact, so the 64-row tiles give
+    the oracle's bits."""
+    M, N, K = 3000, 64, 2000
+    rng = np.random.default_rng(64)
+    A = rng.integers(-2, 3, size=(M, K)).astype(np.float16)
+    B = rng.integers(-2, 3, size=(K, N)).astype(np.float16)
+    C0 = rng.integers(-3, 4, size=(M, N)).astype(np.float16)
+    got, taken = run("f16", A, B, C0, 1.0, -1.0, M, N, K, K, N, N, path=M64)
+    assert ".m64" in taken, taken
+    ref = oracle.gemm(A, B, C0, 1.0, -1.0)
+    assert np.array_equal(got.view(np.uint16), _exact16(ref).view(np.uint16))
+
+
+@pytest.mark.parametrize("M,N,K,stream_k", [
+    (8192, 64, 1024, False),   # 64 tiles of 16 k-blocks: one wave of whole tiles
+    (4096, 32, 2048, False),
+    (4096, 64, 8192, True),    # 32 tiles of 128 k-blocks: stream-K over every tile
+    (512, 64, 16384, True),    # 4 tiles of 256 k-blocks
+])
+def test_tall_schedule_choice(M, N, K, stream_k):
+    """64-wide tiles have no half-width units: stream-K is taken only when its
+    ranges plus the fix-up of the shared tiles beat one wave of whole-K tiles."""
+    A, B, C0 = operands(1100 + M + N + K, M, N, K, K, N, N, np.float16)
+    got, taken = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
+    assert ".bn64.tma.epi_tma" in taken and taken.endswith(".sk") == stream_k, taken
+    big = M * N * K > 1e9
+    check("f16", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N,
+          rows=oracle.sample_rows(M, block=32) if big else None)

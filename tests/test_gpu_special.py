@@ -12,7 +12,7 @@ overflow to +-Inf, a tie at the top of the range (65488 -> 65472), or a tie
 between two halves (2049 -> 2048) -- bit for bit, on every schedule (CTA
 pairs, single CTAs, predicated loads and epilogue, realigned operands,
 split-K, stream-K, two-slice tails, half-width units, skinny and tall
-shapes).
+shapes, 64-row tiles).
 
 Operands holding +-Inf follow IEEE arithmetic: a product with Inf is +-Inf
 (NaN for Inf * 0) and a sum that meets both +Inf and -Inf is NaN, whatever
@@ -89,7 +89,9 @@ PATHS = [
     (600, 1000, 300, 300, 1000, 1000, 12, 0, ".pair.bn224.tma.epi_tma"),
     (600, 1001, 300, 300, 1001, 1001, 13, 0, ".pair.bn192.tma.epi_tma"),
     (16, 1000, 700, 700, 1000, 1000, AUTO, 0, ".a32"),
-    (4096, 64, 2048, 2048, 64, 64, AUTO, 0, ".bn64.tma.epi_tma.sk"),
+    (4096, 64, 8192, 8192, 64, 64, AUTO, 0, ".bn64.tma.epi_tma.sk"),
+    (4096, 64, 2048, 2048, 64, 64, AUTO, 0, ".bn64.tma.epi_tma"),
+    (4096, 64, 2048, 2048, 64, 64, 17, 0, ".bn64.tma.epi_tma.m64"),
 ]
 
 
