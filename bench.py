@@ -18,6 +18,8 @@ while the replays run.
   python bench.py --sweep [--sweep-out FILE]    # fp32 size sweep 1024..12800
   python bench.py --sweep-f16 [--sweep-out FILE] [--sweep-sizes a,b,...]
                                                 # fp16: automatic path vs the alternatives
+  python bench.py --sweep-tall [--sweep-out FILE]
+                                                # fp16 tall shapes (N <= 64): schedules
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas, no collective on the data path); rank 0 prints the
@@ -913,6 +915,65 @@ def run_sweep_f16(args):
                       "auto_best": best_is_auto, "auto_within_2pct": within, "clocks": clocks}))
 
 
+TALL_VARIANTS = [(0, "auto"), (5, "whole_tiles"), (11, "stream_k"), (17, "rows_64")]
+
+
+def run_sweep_tall(args):
+    """Tall half-precision GEMMs (C = 0.75*A*B - 0.25*C, N = 64 and 32, so
+    64-wide tiles with no half-width units): the automatic choice beside
+    whole 128-row tiles in one wave, stream-K over every tile and 64-row
+    tiles, each timed the same way (L2 cleared before every replay,
+    second-half mean of 24 replays)."""
+    import torch
+    import dense_gemm_03_gb300 as g
+    import synthetic
+    from dense_gemm_03_gb300 import build as _b
+    _b.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(0)
+    flush = 2 * int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    out = open(args.sweep_out, "a") if args.sweep_out else None
+    ms_list, ks_list = (512, 1024, 2048, 4096, 6144, 8192, 9728), (512, 1024, 2048, 4096, 8192, 16384)
+    max_mk = 9728 * 16384
+    seed = synthetic.config_seed(6)
+    A, _ = _fill_device((max_mk,), np.float16, seed, synthetic.STREAM_A)
+    B, _ = _fill_device((16384 * 64,), np.float16, seed, synthetic.STREAM_B)
+    C, _ = _fill_device((9728 * 64,), np.float16, seed, synthetic.STREAM_C)
+    sampler = ClockSampler(0).start()
+    n = auto_best = within_1us = 0
+    lost_us = 0.0
+    for N in (64, 32):
+        for M in ms_list:
+            for K in ks_list:
+                if M * K > max_mk:
+                    continue
+                rec = {"M": M, "N": N, "K": K}
+                for path, name in TALL_VARIANTS:
+                    prev = g.force_path(path)
+                    try:
+                        fn = lambda: g.gemm_f16(A, B, C, 0.75, -0.25, M=M, N=N, K=K, lda=K, ldb=N,
+                                                ldc=N, stream=stream)
+                        ms = timed_replays(fn, 24, 3, stream, flush)
+                        rec[name] = {"us": round(second_half_mean(ms) * 1e3, 2),
+                                     "path": g.last_path()}
+                    finally:
+                        g.force_path(prev)
+                best = min(v["us"] for v in rec.values() if isinstance(v, dict))
+                rec["auto_minus_best_us"] = round(rec["auto"]["us"] - best, 2)
+                n += 1
+                auto_best += rec["auto"]["us"] <= best
+                within_1us += rec["auto_minus_best_us"] <= 1.0
+                lost_us += rec["auto_minus_best_us"]
+                if out:
+                    out.write(json.dumps(rec) + "\n")
+                    out.flush()
+    clocks = sampler.stop().summary()
+    print(json.dumps({"sweep": "fp16 tall M 512..9728 x N 32, 64 x K 512..16384", "shapes": n,
+                      "auto_best": auto_best, "auto_within_1us": within_1us,
+                      "auto_lost_us_total": round(lost_us, 1), "clocks": clocks}))
+
+
 # ---------------------------------------------------------------- profiler cases
 
 def run_ncu_case(case):
@@ -975,6 +1036,8 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-f16", action="store_true",
                     help="fp16 sweep: the automatic path beside the forced alternatives")
+    ap.add_argument("--sweep-tall", action="store_true",
+                    help="fp16 tall shapes: the automatic schedule beside the forced ones")
     ap.add_argument("--sweep-out", default=None)
     ap.add_argument("--sweep-sizes", default=None)
     args = ap.parse_args()
@@ -995,6 +1058,9 @@ def main():
         return
     if args.sweep_f16:
         run_sweep_f16(args)
+        return
+    if args.sweep_tall:
+        run_sweep_tall(args)
         return
     if world > 1:
         import torch
