@@ -915,15 +915,18 @@ def run_sweep_f16(args):
                       "auto_best": best_is_auto, "auto_within_2pct": within, "clocks": clocks}))
 
 
-TALL_VARIANTS = [(0, "auto"), (5, "whole_tiles"), (11, "stream_k"), (17, "rows_64")]
+# (forced path, k-blocks per ring stage (0 = automatic), name)
+TALL_VARIANTS = [(0, 0, "auto"), (5, 1, "whole_tiles"), (5, 2, "whole_tiles_2kb"),
+                 (11, 1, "stream_k"), (11, 2, "stream_k_2kb"), (17, 0, "rows_64")]
 
 
 def run_sweep_tall(args):
     """Tall half-precision GEMMs (C = 0.75*A*B - 0.25*C, N = 64 and 32, so
     64-wide tiles with no half-width units): the automatic choice beside
-    whole 128-row tiles in one wave, stream-K over every tile and 64-row
-    tiles, each timed the same way (L2 cleared before every replay,
-    second-half mean of 24 replays)."""
+    whole 128-row tiles in one wave and stream-K over every tile (each with
+    one and with two k-blocks per ring stage) and 64-row tiles, each timed
+    the same way (L2 cleared before every replay, second-half mean of 24
+    replays)."""
     import torch
     import dense_gemm_03_gb300 as g
     import synthetic
@@ -949,8 +952,9 @@ def run_sweep_tall(args):
                 if M * K > max_mk:
                     continue
                 rec = {"M": M, "N": N, "K": K}
-                for path, name in TALL_VARIANTS:
+                for path, kpb, name in TALL_VARIANTS:
                     prev = g.force_path(path)
+                    prev_k = g.stage_kblocks(kpb)
                     try:
                         fn = lambda: g.gemm_f16(A, B, C, 0.75, -0.25, M=M, N=N, K=K, lda=K, ldb=N,
                                                 ldc=N, stream=stream)
@@ -959,6 +963,7 @@ def run_sweep_tall(args):
                                      "path": g.last_path()}
                     finally:
                         g.force_path(prev)
+                        g.stage_kblocks(prev_k)
                 best = min(v["us"] for v in rec.values() if isinstance(v, dict))
                 rec["auto_minus_best_us"] = round(rec["auto"]["us"] - best, 2)
                 n += 1

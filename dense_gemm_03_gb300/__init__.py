@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16", "gemm_f16_f32out", "f32_to_f16",
     "sgemm_f32", "gemm_f16_host",
-    "sgemm_f32_host", "gemm_f16_splitk_noalloc", "l2_flush", "force_path", "force_splits", "set_wait_limit_ns",
+    "sgemm_f32_host", "gemm_f16_splitk_noalloc", "l2_flush", "force_path", "force_splits", "stage_kblocks",
+    "set_wait_limit_ns",
     "debug_status", "last_path", "launch_count", "plan_stream_k", "release", "EXPORTS",
 ]
 
@@ -32,7 +33,7 @@ EXPORTS = (
     "gemm_l2_flush", "gemm_force_path", "gemm_force_splits", "gemm_set_wait_limit_ns",
     "gemm_debug_status", "gemm_last_path", "gemm_strerror", "gemm_release",
     "gemm_f16_splitk_noalloc", "gemm_launch_count", "gemm_plan_stream_k", "gemm_f16_f32out",
-    "gemm_f32_to_f16", "gemm_debug_wait_probe", "gemm_plan_tf32_slices",
+    "gemm_f32_to_f16", "gemm_debug_wait_probe", "gemm_plan_tf32_slices", "gemm_stage_kblocks",
 )
 
 PATH_AUTO, PATH_TMA, PATH_MANUAL, PATH_SPLITK, PATH_F32_SCALAR = 0, 1, 2, 3, 4
@@ -83,6 +84,8 @@ def lib():
             L.gemm_force_path.argtypes = [i]
             L.gemm_force_splits.restype = i
             L.gemm_force_splits.argtypes = [i]
+            L.gemm_stage_kblocks.restype = i
+            L.gemm_stage_kblocks.argtypes = [i]
             L.gemm_set_wait_limit_ns.restype = ctypes.c_longlong
             L.gemm_set_wait_limit_ns.argtypes = [ctypes.c_longlong]
             L.gemm_debug_status.restype = i
@@ -262,6 +265,13 @@ def force_splits(splits: int) -> int:
     prev = lib().gemm_force_splits(int(splits))
     if prev < 0:
         raise GemmError(prev, "gemm_force_splits")
+    return prev
+
+
+def stage_kblocks(kblocks: int) -> int:
+    prev = lib().gemm_stage_kblocks(int(kblocks))
+    if prev < 0:
+        raise GemmError(prev, "gemm_stage_kblocks")
     return prev
 
 

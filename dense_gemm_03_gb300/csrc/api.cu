@@ -95,6 +95,7 @@ std::mutex g_mu;
 std::mutex g_host_mu;   // host-buffer forms share their staging buffers: one call at a time
 DevState g_dev[kMaxDevices];
 std::atomic<int> g_force_path{0};
+std::atomic<int> g_stage_kblocks{0};   // 0 = automatic
 std::atomic<int> g_force_splits{0};
 std::atomic<long long> g_wait_limit_ns{2000000000ll};
 std::atomic<long long> g_launches{0};
@@ -354,14 +355,22 @@ int tail_first_slice(long long tiles, long long slots, int kb) {
 // 1000x1001x4096 (32 tiles of 64) 38 us and 61 us; 16x8192x8192 (64 tiles of
 // 128, 16 rows) stream-K 42 us, equal K slices 51 us.
 // 64-wide TMA tiles have no half-width units; there stream-K is weighed
-// against one wave of whole-K tiles (kb k-blocks per CTA), and its ranges
-// can go no faster than HBM streams A: a CTA takes ~0.25 us per k-block
-// (whatever the tile's height or the number of CTAs), the time HBM takes for
-// the k-blocks of about 96 128-row tiles.  Measured over M = 512..9728,
-// N = 32 and 64, K = 512..16384 (median of 20 after the page's flush):
-// whole tiles win for K <= 2048 (8192x64x1024 14.3 us against 18.4 us),
-// stream-K for K >= 8192 (4096x64x8192 26.9 against 43.0 us); in between
-// the estimate picks the faster one to within ~1 us.
+// against one wave of whole-K tiles.  A whole-K CTA takes ~0.25 us per
+// k-block whatever the tile's height or the number of CTAs (its TMA ring
+// completes about one stage per DRAM round trip, whatever the stage's size),
+// and ~4% less with two k-blocks per stage, which such tiles take from
+// kWholeTwoKb k-blocks on (whole_stage_kblocks).  Stream-K's ranges can go no
+// faster than HBM streams A: per k-block of a range, the time HBM takes for
+// the k-blocks of about 96 128-row tiles.  Measured over M = 512..9728, N = 32
+// and 64, K = 512..16384 (second-half mean of 24 replays after the page's
+// flush): whole tiles win for K <= 2048 (8192x64x1024 14.1 against 18.5 us)
+// and at K = 4096 for most M (8192x64x4096 24.4 against 26.1 us), stream-K
+// for K >= 8192 (4096x64x8192 26.9 against 43.1 us); the estimate is within
+// 1 us of the faster one at 81 of 84 shapes.
+constexpr int kWholeTwoKb = 16;
+
+int whole_stage_kblocks(int kb) { return kb >= kWholeTwoKb ? 2 : 1; }
+
 bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool halves_ok,
                                bool whole_ok, int rows, int bn) {
   const SkPlan sk = plan_stream_k(tiles, slots, kb, true);
@@ -371,7 +380,8 @@ bool few_tiles_prefer_stream_k(long long tiles, long long slots, int kb, bool ha
   if (!halves_ok) {
     if (!whole_ok) return true;
     const long long floor_kb = (sk.sk_tiles * kb * std::min(rows, kBM) + 96 * kBM - 1) / (96 * kBM);
-    return std::max(range, floor_kb) + kSkFixKb + per_piece * (sk.max_pieces - 1) < kb;
+    const long long whole_cost = whole_stage_kblocks(kb) == 2 ? kb * 24 / 25 : kb;
+    return std::max(range, floor_kb) + kSkFixKb + per_piece * (sk.max_pieces - 1) < whole_cost;
   }
   const long long sk_cost = range + kSkFixKb + per_piece * (sk.max_pieces - 1);
   const long long waves = (2 * tiles + slots - 1) / slots;
@@ -796,6 +806,20 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
                     : static_cast<int>(a.dp_tiles * static_cast<long long>(splits) +
                                        (units_tiles - a.dp_tiles) * a.tail_splits);
 
+  // k-blocks per ring stage: two for one wave of whole 64-wide tiles with a
+  // long enough K (whole_stage_kblocks), or where forced and the kernel has
+  // that form (64-wide single-CTA tiles, 256-wide pairs, TMA epilogue)
+  int kpb = 1;
+  const int fk = g_stage_kblocks.load();
+  const bool two_ok = load == kLoadTma && epi == kEpiTma && !m64 &&
+                      ((pair && bn == 256) || (!pair && bn == 64));
+  if (fk == 2 && two_ok) {
+    kpb = 2;
+  } else if (fk == 0 && two_ok && !pair && few && a.sk_tiles == 0 && a.tail_splits == 1 &&
+             a.splits == 1 && a.num_units == tiles) {
+    kpb = whole_stage_kblocks(a.kb_total);
+  }
+
   // At most 64 rows on 128-wide single-CTA tiles: stage only the A rows that
   // exist (32 or 64), which leaves room for more stages of B.
   const int am = m64 ? 64
@@ -829,18 +853,18 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
                                       : std::min<long long>(a.num_units, workers);
   if (pair) {
     const int grid = 2 * static_cast<int>(nw);
-    snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.pair.bn%d.tma.%s%s%s", bn,
+    snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.pair.bn%d.tma.%s%s%s%s", bn,
              epi == kEpiF32Tma ? "epi_f32_tma"
                                : (epi == kEpiF32 ? "epi_f32" : (epi == kEpiTma ? "epi_tma" : "epi_manual")),
-             cut, how);
+             kpb == 2 ? ".kb2" : "", cut, how);
     t_last_path = t_path_buf;
-    if (launch_gemm_f16_tc_pair(bn, epi, tmA, tmB, tmC, a, grid, stream) != cudaSuccess)
+    if (launch_gemm_f16_tc_pair(bn, epi, tmA, tmB, tmC, a, grid, stream, kpb) != cudaSuccess)
       return GEMM_ERR_CUDA;
     return copy_back();
   }
   const int grid = static_cast<int>(nw);
   const int bi = bn == 64 ? 0 : (bn == 128 ? 1 : 2);
-  const char* rows = m64 ? ".m64" : (am == 32 ? ".a32" : (am == 64 ? ".a64" : ""));
+  const char* rows = m64 ? ".m64" : (am == 32 ? ".a32" : (am == 64 ? ".a64" : (kpb == 2 ? ".kb2" : "")));
   if (c_f32)
     snprintf(t_path_buf, sizeof(t_path_buf), "f16.tc.bn%d.%s.epi_f32%s%s%s", bn,
              load == kLoadTma ? "tma" : "manual", rows, cut, how);
@@ -851,7 +875,7 @@ int gemm_f16_impl(const uint16_t* A, const uint16_t* B, void* C, bool c_f32, int
   const cudaError_t e =
       m64 ? launch_gemm_f16_tc_m64(tmA, tmB, tmC, a, grid, stream)
           : (am < kBM ? launch_gemm_f16_tc_skinny(am, epi, tmA, tmB, tmC, a, grid, stream)
-                      : launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream));
+                      : launch_gemm_f16_tc(bn, load, epi, tmA, tmB, tmC, a, grid, stream, kpb));
   if (e != cudaSuccess) return GEMM_ERR_CUDA;
   return copy_back();
 }
@@ -1182,6 +1206,8 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void set_last_path(const char* path) { t_last_path = path; }
 
+int stage_kblocks() { return g_stage_kblocks.load() == 2 ? 2 : 1; }
+
 }  // namespace gb300
 
 using namespace gb300;
@@ -1263,6 +1289,11 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream) {
 int gemm_force_path(int path) {
   if (path < 0 || path > 17) return GEMM_ERR_ARG;
   return g_force_path.exchange(path);
+}
+
+int gemm_stage_kblocks(int kblocks) {
+  if (kblocks < 0 || kblocks > 2) return GEMM_ERR_ARG;
+  return g_stage_kblocks.exchange(kblocks);
 }
 
 int gemm_force_splits(int splits) {

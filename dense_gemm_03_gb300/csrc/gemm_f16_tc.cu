@@ -25,9 +25,15 @@ cudaError_t launch_bn(int load, int epi, const CUtensorMap& a, const CUtensorMap
 
 cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, const CUtensorMap& tmC, const TcArgs& args,
-                               int grid, cudaStream_t stream) {
+                               int grid, cudaStream_t stream, int kpb) {
   if (epi_mode == kEpiF32)
     return launch_gemm_f16_tc_f32(bn, load_mode, tmA, tmB, args, grid, stream);
+  // two k-blocks per ring stage: 64-wide tiles with TMA loads and epilogue
+  if (kpb == 2)
+    return bn == 64 && load_mode == kLoadTma && epi_mode == kEpiTma
+               ? launch_one<64, kLoadTma, kEpiTma, false, 128, 128, 2>(tmA, tmB, tmC, args, grid,
+                                                                        stream)
+               : cudaErrorInvalidValue;
   switch (bn) {
     case 256: return launch_bn<256>(load_mode, epi_mode, tmA, tmB, tmC, args, grid, stream);
     case 128: return launch_bn<128>(load_mode, epi_mode, tmA, tmB, tmC, args, grid, stream);
@@ -38,14 +44,17 @@ cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtens
 
 cudaError_t launch_gemm_f16_tc_pair(int bn, int epi_mode, const CUtensorMap& tmA,
                                     const CUtensorMap& tmB, const CUtensorMap& tmC,
-                                    const TcArgs& args, int grid, cudaStream_t stream) {
+                                    const TcArgs& args, int grid, cudaStream_t stream, int kpb) {
   if (epi_mode == kEpiF32 || epi_mode == kEpiF32Tma)
     return bn == 256 ? launch_gemm_f16_tc_pair_f32(epi_mode, tmA, tmB, tmC, args, grid, stream)
                      : cudaErrorInvalidValue;
   if (bn != 256)
     return launch_gemm_f16_tc_pair_narrow(bn, epi_mode, tmA, tmB, tmC, args, grid, stream);
   if (epi_mode == kEpiTma)
-    return launch_one<256, kLoadTma, kEpiTma, true>(tmA, tmB, tmC, args, grid, stream);
+    return kpb == 2 ? launch_one<256, kLoadTma, kEpiTma, true, 128, 128, 2>(tmA, tmB, tmC, args,
+                                                                             grid, stream)
+                    : launch_one<256, kLoadTma, kEpiTma, true>(tmA, tmB, tmC, args, grid, stream);
+  if (kpb == 2) return cudaErrorInvalidValue;
   if (epi_mode == kEpiManual)
     return launch_one<256, kLoadTma, kEpiManual, true>(tmA, tmB, tmC, args, grid, stream);
   return cudaErrorInvalidValue;

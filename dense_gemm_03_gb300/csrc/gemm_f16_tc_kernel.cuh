@@ -71,24 +71,32 @@ constexpr int kCsBufs = 2;
 // M <= AM, whose stages then hold more of B (the MMA still reads 128 rows of
 // A: the rows past AM come from the stage's B region and only produce
 // accumulator rows >= M, which are never stored).
-template <int BN, bool PAIR, bool CS = false, int AM = 128>
+// KPB: k-blocks per ring stage (1 or 2).  A stage holds KPB consecutive
+// k-blocks, each as its A part followed by its B part, and is loaded and
+// released as one: a CTA's TMA ring completes about one stage per ~0.4 us of
+// DRAM latency whatever the stage's size, so two k-blocks per stage move
+// about 1.5x the bytes per CTA in the same time.
+template <int BN, bool PAIR, bool CS = false, int AM = 128, int KPB = 1>
 struct TcCfg {
   static constexpr int kBLoadCols = PAIR ? BN / 2 : BN;   // B columns this CTA gives the MMA
   static constexpr int kBStageCols = (kBLoadCols + 63) / 64 * 64;   // staged: whole boxes
   static constexpr int kBBytes = kBStageCols * BK * 2;
   static constexpr int kAStageBytes = AM * BK * 2;
-  static constexpr int kStageBytes = kAStageBytes + kBBytes;
-  // skinny stages: as many as fit beside the epilogue tiles, at most 16
+  static constexpr int kKbBytes = kAStageBytes + kBBytes;   // one k-block of A and B
+  static constexpr int kStageBytes = KPB * kKbBytes;
+  // skinny stages: as many as fit beside the epilogue tiles, at most 16 k-blocks
   static constexpr int kSkinnyStages = (232448 - 1024 - 1024 - 8 * 2 * kEpiBufBytes) / kStageBytes;
-  static constexpr int kStages =
-      AM < 128 ? (kSkinnyStages < 16 ? kSkinnyStages : 16)
+  static constexpr int kStages1 =
+      AM < 128 ? (kSkinnyStages < 16 / KPB ? kSkinnyStages : 16 / KPB)
                : (PAIR ? ((CS && kCsBufs > 2) ? 5 : 6) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)));
+  static constexpr int kStages = AM < 128 ? kStages1 : kStages1 / KPB;
   // TMEM columns per accumulator (a power of two) and for both of them
   static constexpr int kAccStride = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
   static constexpr int kTmemCols = 2 * kAccStride;
   static_assert(PAIR ? (BN == 256 || BN == 224 || BN == 192) : (BN == 64 || BN == 128 || BN == 256),
                 "tile width");
-  static_assert(AM == 128 || (!PAIR && kStageBytes >= kABytes), "skinny stages span 128 A rows");
+  static_assert(AM == 128 || (!PAIR && kKbBytes >= kABytes), "skinny stages span 128 A rows");
+  static_assert(KPB == 1 || KPB == 2, "k-blocks per stage");
 };
 
 // Warp roles.  With TMA loads: 1 producer, 1 MMA and 8 epilogue warps (two
@@ -108,12 +116,12 @@ struct Roles {
 // Counters per tail tile: one per epilogue warp (at most 8).
 constexpr int kTailCounters = 8;
 
-template <int BN, int EPI, bool PAIR, int AM = 128>
+template <int BN, int EPI, bool PAIR, int AM = 128, int KPB = 1>
 struct Smem {
   // C read by TMA into the epilogue's staging tiles: the CTA-pair kernel with
   // TMA stores
   static constexpr bool kCs = PAIR && (EPI == kEpiTma || EPI == kEpiF32Tma);
-  using Cfg = TcCfg<BN, PAIR, kCs, AM>;
+  using Cfg = TcCfg<BN, PAIR, kCs, AM, KPB>;
   // 32 x 32 staging tiles per epilogue warp
   static constexpr int kBufs = kCs ? kCsBufs : 2;
   static constexpr int kWarpEpiBytes = kBufs * kEpiBufBytes;
@@ -465,17 +473,18 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float4* 
   }
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128, int KPB = 1>
 __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
   using R = Roles<LOAD>;
-  using L = Smem<BN, EPI, PAIR, AM>;
+  using L = Smem<BN, EPI, PAIR, AM, KPB>;
   using Cfg = typename L::Cfg;
   constexpr bool kCs = L::kCs;
   constexpr int kAB = Cfg::kAStageBytes;   // A bytes per stage
   static_assert(AM == 128 || LOAD == kLoadTma, "skinny stages take TMA loads");
+  static_assert(KPB == 1 || LOAD == kLoadTma, "two k-blocks per stage take TMA loads");
   constexpr int S = Cfg::kStages;
   static_assert(!PAIR || (LOAD == kLoadTma && EPI != kEpiPartial), "pair configuration");
   // MM = 64: 64-row tiles (tcgen05.mma with M = 64), whole-K units only, TMA
@@ -568,43 +577,54 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         UnitCursor cur = first_unit(p, worker);
         Unit t;
         while (ok && next_unit(p, cur, worker, nworkers, BN, bm_tile, rank, t)) {
-          for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          for (int kb = t.kb0; kb < t.kb1; kb += KPB) {
             if (!wait_parity(empty_bar(stage), phase ^ 1u, limit, st, 1)) {
               ok = false;
               break;
             }
+            // k-blocks of this stage (the unit's last stage may hold one)
+            const int nk = KPB == 1 ? 1 : min(KPB, t.kb1 - kb);
             // B columns this CTA gives the MMA (a half-width unit needs half of
             // them), staged in whole 64-column boxes
             const int bcols = PAIR ? t.ncols / 2 : t.ncols;
-            const uint32_t bytes = static_cast<uint32_t>(kAB + ((bcols + 63) / 64) * kBBlockBytes);
+            const uint32_t bytes =
+                static_cast<uint32_t>(nk * (kAB + ((bcols + 63) / 64) * kBBlockBytes));
             if (PAIR) {
               // Both CTAs' bytes are counted on the leader's barrier; only the
               // leader arms it (for the pair's total), the peer's copies just
               // signal it.
               const uint32_t fb = map_to_cta(full_bar(stage), 0);
               if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
-              tma_load_2d_pair(stage_a(stage), &tmA, fb, kb * BK, t.m0);
+              for (int j = 0; j < nk; ++j) {
+                const uint32_t sa = stage_a(stage) + j * Cfg::kKbBytes, sb = sa + kAB;
+                const int k0 = (kb + j) * BK;
+                tma_load_2d_pair(sa, &tmA, fb, k0, t.m0);
 #pragma unroll
-              for (int c = 0; c < Cfg::kBStageCols / 64; ++c)
-                if (64 * c < bcols)
-                  tma_load_2d_pair(stage_b(stage) + c * kBBlockBytes, &tmB, fb,
-                                   t.n0 + static_cast<int>(rank) * bcols + 64 * c, kb * BK);
+                for (int c = 0; c < Cfg::kBStageCols / 64; ++c)
+                  if (64 * c < bcols)
+                    tma_load_2d_pair(sb + c * kBBlockBytes, &tmB, fb,
+                                     t.n0 + static_cast<int>(rank) * bcols + 64 * c, k0);
+              }
             } else {
               mbar_arrive_expect_tx(full_bar(stage), bytes);
-              if (p.stream_a)
-                tma_load_2d_hint(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0, evict_first);
-              else
-                tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * BK, t.m0);
+              for (int j = 0; j < nk; ++j) {
+                const uint32_t sa = stage_a(stage) + j * Cfg::kKbBytes, sb = sa + kAB;
+                const int k0 = (kb + j) * BK;
+                if (p.stream_a)
+                  tma_load_2d_hint(sa, &tmA, full_bar(stage), k0, t.m0, evict_first);
+                else
+                  tma_load_2d(sa, &tmA, full_bar(stage), k0, t.m0);
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                if (64 * c < bcols) {
-                  if (p.stream_b)
-                    tma_load_2d_hint(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
-                                     t.n0 + 64 * c, kb * BK, evict_first);
-                  else
-                    tma_load_2d(stage_b(stage) + c * kBBlockBytes, &tmB, full_bar(stage),
-                                t.n0 + 64 * c, kb * BK);
-                }
+                for (int c = 0; c < BN / 64; ++c)
+                  if (64 * c < bcols) {
+                    if (p.stream_b)
+                      tma_load_2d_hint(sb + c * kBBlockBytes, &tmB, full_bar(stage),
+                                       t.n0 + 64 * c, k0, evict_first);
+                    else
+                      tma_load_2d(sb + c * kBBlockBytes, &tmB, full_bar(stage), t.n0 + 64 * c,
+                                  k0);
+                  }
+              }
             }
             ++issued;
             if (++stage == S) {
@@ -689,21 +709,25 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
         tc_fence_after();
         const uint32_t idesc = t.ncols == BN ? idesc_full : idesc_half;
         const uint32_t d_tmem = tmem_base + buf * Cfg::kAccStride;
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; kb += KPB) {
           if (!wait_parity(full_bar(stage), phase, limit, st, 4)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
+          const int nk = KPB == 1 ? 1 : min(KPB, t.kb1 - kb);
+          for (int j = 0; j < nk; ++j) {
+            const uint32_t a0 = stage_a(stage) + j * Cfg::kKbBytes, b0 = a0 + kAB;
 #pragma unroll
-          for (int kk = 0; kk < BK / kUmmaK; ++kk) {
-            const uint64_t ad = smem_desc_sw128(a0 + kk * (kUmmaK * 2), 16u, 1024u);
-            const uint64_t bd = smem_desc_sw128(b0 + kk * (kUmmaK * 128), kBBlockBytes, 1024u);
-            if (PAIR)
-              mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
-            else
-              mma_f16_ss(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / kUmmaK; ++kk) {
+              const uint64_t ad = smem_desc_sw128(a0 + kk * (kUmmaK * 2), 16u, 1024u);
+              const uint64_t bd = smem_desc_sw128(b0 + kk * (kUmmaK * 128), kBBlockBytes, 1024u);
+              const uint32_t acc = (kb > t.kb0 || j > 0 || kk > 0) ? 1u : 0u;
+              if (PAIR)
+                mma_f16_ss_pair(d_tmem, ad, bd, idesc, acc);
+              else
+                mma_f16_ss(d_tmem, ad, bd, idesc, acc);
+            }
           }
           // frees the stage (in both CTAs of a pair) once these MMAs finish
           if (PAIR)
@@ -1164,13 +1188,13 @@ __global__ void __launch_bounds__(Roles<LOAD>::kThreads, 1)
   // the MMA warp only after all epilogue warps have signalled tmem_free.
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128, int KPB = 1>
 cudaError_t configure(int dev) {
-  using L = Smem<BN, EPI, PAIR, AM>;
+  using L = Smem<BN, EPI, PAIR, AM, KPB>;
   static bool configured[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM, MM>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM, MM, KPB>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1179,14 +1203,14 @@ cudaError_t configure(int dev) {
   return cudaSuccess;
 }
 
-template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128>
+template <int BN, int LOAD, int EPI, bool PAIR, int AM = 128, int MM = 128, int KPB = 1>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                        const TcArgs& args, int grid, cudaStream_t stream) {
-  using L = Smem<BN, EPI, PAIR, AM>;
+  using L = Smem<BN, EPI, PAIR, AM, KPB>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if ((e = configure<BN, LOAD, EPI, PAIR, AM, MM>(dev)) != cudaSuccess) return e;
+  if ((e = configure<BN, LOAD, EPI, PAIR, AM, MM, KPB>(dev)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(Roles<LOAD>::kThreads, 1, 1);
@@ -1208,8 +1232,8 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   }
   cfg.attrs = nattr ? attr : nullptr;
   cfg.numAttrs = nattr;
-  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM, MM>, tmA, tmB, tmC,
-                         args);
+  e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, LOAD, EPI, PAIR, AM, MM, KPB>, tmA, tmB,
+                         tmC, args);
   if (e != cudaSuccess) return e;
   return counted_launch(cudaGetLastError());
 }

@@ -101,10 +101,11 @@ struct TcArgs {
 };
 
 // Tensor-core fp16 GEMM (tcgen05).  Maps are ignored by the modes that do not
-// use them.  Returns a cudaError_t from the launch.
+// use them.  kpb: k-blocks per ring stage, 1, or 2 for 64-wide tiles with TMA
+// loads and epilogue.  Returns a cudaError_t from the launch.
 cudaError_t launch_gemm_f16_tc(int bn, int load_mode, int epi_mode, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, const CUtensorMap& tmC, const TcArgs& args,
-                               int grid, cudaStream_t stream);
+                               int grid, cudaStream_t stream, int kpb = 1);
 int tc_threads(int load_mode);
 
 // The same GEMM with an fp32 C (epilogue kEpiF32; gemm_f16_f32out.cu).
@@ -139,10 +140,12 @@ cudaError_t launch_f32_to_f16(const float* src, uint16_t* dst, long long n, int 
 // The same GEMM on CTA pairs (clusters of 2 sharing tcgen05.mma.cta_group::2):
 // 256 x bn output tiles (bn = 256, or 224 / 192 with a half C), TMA operand
 // loads only, epilogue kEpiTma or kEpiManual (or the fp32-C ones, bn = 256).
-// tiles_m counts 256-row tiles; grid = 2 x (number of pairs).
+// tiles_m counts 256-row tiles; grid = 2 x (number of pairs).  kpb: k-blocks
+// per ring stage, 1, or 2 for bn = 256 with the TMA epilogue.
 cudaError_t launch_gemm_f16_tc_pair(int bn, int epi_mode, const CUtensorMap& tmA,
                                     const CUtensorMap& tmB, const CUtensorMap& tmC,
-                                    const TcArgs& args, int grid, cudaStream_t stream);
+                                    const TcArgs& args, int grid, cudaStream_t stream,
+                                    int kpb = 1);
 // The 224- and 192-wide instances (gemm_f16_pair_narrow.cu).
 cudaError_t launch_gemm_f16_tc_pair_narrow(int bn, int epi_mode, const CUtensorMap& tmA,
                                            const CUtensorMap& tmB, const CUtensorMap& tmC,

@@ -229,6 +229,15 @@ int gemm_l2_flush(size_t bytes, cudaStream_t stream);
  */
 int gemm_force_path(int path);
 
+/* k-blocks (of 64 elements of K) per stage of the operand ring of the
+ * half-precision tensor-core kernels: 0 = automatic (two for one wave of
+ * whole 64-wide tiles with at least 16 k-blocks, else one), 1, or 2 (taken
+ * only where the kernel has that form: 64-wide single-CTA tiles and 256-wide
+ * CTA pairs, with TMA loads and the TMA epilogue).  Results do not depend on
+ * it.  For tests and benchmarks; process wide; returns the previous value, or
+ * GEMM_ERR_ARG for an unknown value. */
+int gemm_stage_kblocks(int kblocks);
+
 /* Fixes the split count of the split-K path (0 = automatic).  On the fp32
  * tensor-core path it also sets the K slices of few-tile shapes: 1 keeps
  * whole-K units, > 1 asks for that many slices (fewer when a slice would be

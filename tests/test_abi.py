@@ -63,5 +63,8 @@ def test_strerror_and_switches(L):
     with pytest.raises(g.GemmError):
         g.force_path(18)
     assert g.force_splits(4) == 0 and g.force_splits(0) == 4
+    assert g.stage_kblocks(2) == 0 and g.stage_kblocks(0) == 2
+    with pytest.raises(g.GemmError):
+        g.stage_kblocks(3)
     prev = g.set_wait_limit_ns(12345)
     assert g.set_wait_limit_ns(prev) == 12345

@@ -533,18 +533,67 @@ def test_m64_tiles_integers_exact():
     assert np.array_equal(got.view(np.uint16), _exact16(ref).view(np.uint16))
 
 
-@pytest.mark.parametrize("M,N,K,stream_k", [
-    (8192, 64, 1024, False),   # 64 tiles of 16 k-blocks: one wave of whole tiles
-    (4096, 32, 2048, False),
-    (4096, 64, 8192, True),    # 32 tiles of 128 k-blocks: stream-K over every tile
-    (512, 64, 16384, True),    # 4 tiles of 256 k-blocks
+@pytest.mark.parametrize("M,N,K,mark", [
+    (8192, 64, 512, "f16.tc.bn64.tma.epi_tma"),        # 64 tiles of 8 k-blocks: whole tiles
+    (8192, 64, 1024, "f16.tc.bn64.tma.epi_tma.kb2"),   # 16 k-blocks: two per ring stage
+    (4096, 32, 2048, "f16.tc.bn64.tma.epi_tma.kb2"),
+    (8192, 64, 4096, "f16.tc.bn64.tma.epi_tma.kb2"),
+    (4096, 64, 8192, "f16.tc.bn64.tma.epi_tma.sk"),    # 32 tiles of 128: stream-K over every tile
+    (512, 64, 16384, "f16.tc.bn64.tma.epi_tma.sk"),    # 4 tiles of 256 k-blocks
 ])
-def test_tall_schedule_choice(M, N, K, stream_k):
+def test_tall_schedule_choice(M, N, K, mark):
     """64-wide tiles have no half-width units: stream-K is taken only when its
-    ranges plus the fix-up of the shared tiles beat one wave of whole-K tiles."""
+    ranges plus the fix-up of the shared tiles beat one wave of whole-K tiles,
+    which stage two k-blocks at a time from 16 k-blocks on."""
     A, B, C0 = operands(1100 + M + N + K, M, N, K, K, N, N, np.float16)
     got, taken = run("f16", A, B, C0, 0.75, -0.25, M, N, K, K, N, N)
-    assert ".bn64.tma.epi_tma" in taken and taken.endswith(".sk") == stream_k, taken
+    assert taken == mark, taken
     big = M * N * K > 1e9
     check("f16", got, A, B, C0, 0.75, -0.25, M, N, K, K, N, N,
           rows=oracle.sample_rows(M, block=32) if big else None)
+
+
+# ---------------------------------------------------------------- two k-blocks per ring stage
+@pytest.mark.parametrize("M,N,K,ldc,path,kpb,mark", [
+    (5000, 64, 1030, 64, AUTO, 0, ".bn64.tma.epi_tma.kb2"),    # 17 k-blocks: the last stage holds one
+    (3000, 40, 2100, 48, AUTO, 0, ".bn64.tma.epi_tma.kb2"),    # N < 64, padded C, ragged last k-block
+    (8192, 64, 4096, 64, AUTO, 0, ".bn64.tma.epi_tma.kb2"),
+    (2000, 2600, 4100, 2600, AUTO, 2, ".pair.bn256.tma.epi_tma.kb2.ktail"),   # forced on pairs
+    (600, 1000, 1000, 1000, NO_TAIL, 2, ".pair.bn256.tma.epi_tma.kb2"),
+    (700, 64, 900, 64, SK_ALL, 2, ".bn64.tma.epi_tma.kb2.sk"),  # stream-K pieces of odd length
+])
+@pytest.mark.parametrize("alpha,beta,c_fill", [(0.75, -0.25, "uniform"), (1.0, 0.0, "nan")])
+def test_two_kblocks_per_stage_parity(M, N, K, ldc, path, kpb, mark, alpha, beta, c_fill):
+    """A ring stage holding two k-blocks (each A part followed by its B part),
+    loaded and released as one; a unit with an odd number of k-blocks ends on
+    a stage holding one."""
+    import dense_gemm_03_gb300 as g
+    A, B, C0 = operands(2200 + M + N + K, M, N, K, K, N, ldc, np.float16, c_fill=c_fill)
+    prev = g.stage_kblocks(kpb)
+    try:
+        got, taken = run("f16", A, B, C0, alpha, beta, M, N, K, K, N, ldc, path=path)
+    finally:
+        g.stage_kblocks(prev)
+    assert mark in taken, taken
+    big = M * N * K > 1e9
+    check("f16", got, A, B, C0, alpha, beta, M, N, K, K, N, ldc,
+          rows=oracle.sample_rows(M, block=32) if big else None,
+          cols=oracle.sample_cols(N, block=32) if big and N > 64 else None)
+    assert padding_untouched(got, C0, N)
+
+
+@pytest.mark.parametrize("M,N,K,path", [(3000, 64, 2000, AUTO), (1000, 1200, 1100, NO_TAIL)])
+def test_two_kblocks_per_stage_bitwise_equal(M, N, K, path):
+    """The MMAs run in the same order whatever the stage depth: one and two
+    k-blocks per stage give the same bits."""
+    import dense_gemm_03_gb300 as g
+    A, B, C0 = operands(3300 + M + N + K, M, N, K, K, N, N, np.float16)
+    outs = []
+    for kpb in (1, 2):
+        prev = g.stage_kblocks(kpb)
+        try:
+            outs.append(run("f16", A, B, C0, 1.5, 0.5, M, N, K, K, N, N, path=path))
+        finally:
+            g.stage_kblocks(prev)
+    assert ".kb2" not in outs[0][1] and ".kb2" in outs[1][1], (outs[0][1], outs[1][1])
+    assert np.array_equal(outs[0][0].view(np.uint16), outs[1][0].view(np.uint16))
