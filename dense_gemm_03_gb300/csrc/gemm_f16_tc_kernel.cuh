@@ -35,7 +35,9 @@
 // last (counted per launch) adds them up in k order and runs the epilogue, so
 // no CTA ever waits for another.
 //
-// Shared-memory operand layouts (128-byte swizzle, 1024-byte aligned):
+// Shared-memory operand layouts (128-byte swizzle, 1024-byte aligned; a ring
+// stage holds one k-block, or two, the second's A and B parts after the
+// first's):
 //   A stage: 128 rows x 64 halves, K-major; row r at r*128 B, 16-byte chunk c
 //            of the row stored at chunk (c ^ (r % 8)).  SBO = 1024 B.
 //   B stage: BN/64 column blocks of 64 (k) rows x 64 halves, N-major (MN-major
