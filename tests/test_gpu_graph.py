@@ -25,6 +25,8 @@ def _built():
     (2000, 2600, 4096, AUTO, ".ktail"),
     (2000, 2600, 4096, 14, ".sktail"),
     (64, 128, 4096, SK_ALL, ".sk"),
+    (4096, 64, 2048, AUTO, ".kb2"),      # whole 64-wide tiles, two k-blocks per ring stage
+    (4096, 64, 2048, 17, ".m64"),        # 64-row tiles
 ])
 def test_graph_replays(M, N, K, path, mark):
     import dense_gemm_03_gb300 as g
